@@ -1,0 +1,12 @@
+"""fp64 CPU oracle for the fused attention forward.
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke entry point and by the
+benchmark's CPU-baseline leg, never by the library. It shares no code with the
+CUDA path. ``attention`` is the two-pass definition; ``online_softmax`` is an
+independently written tiled recurrence used to cross-check it on tiny inputs.
+"""
+from .attention import attention_forward, attention_head, kv_head, probabilities, scores, softmax_two_pass
+from .online_softmax import attention_online
+
+__all__ = ["attention_forward", "attention_head", "kv_head", "probabilities", "scores",
+           "softmax_two_pass", "attention_online"]
