@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on the headline workload.
+
+One step = one attn_fwd call over the whole workload (B=2, H=32, Hkv=8, N=8192, d=128, causal,
+bf16 by default). Prints ONE JSON line on rank 0:
+  value      device-timed TFLOP/s (4*B*H*N^2*d, halved for causal), summed over ranks, with
+             inputs resident in HBM; CUDA events around each launch on the launching stream,
+             L2 flushed (256 MiB write) before every step outside the events;
+  e2e        the same metric through attn_fwd_host (pinned host buffers, H2D of q/k/v and D2H
+             of o/lse inside the timed region);
+  roofline   tensor-core bound: achieved TFLOP/s of the attention kernel against the measured
+             dense bf16 peak (e4m3: x2 nominal ratio);
+  cpu_baseline  the fp64 oracle on a bounded sample, on this host's cores (rank 0, N=1 only);
+  clocks     nvidia-smi SM clock samples taken during the timed region.
+--impl reference times the oracle itself (CPU) on bounded samples of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (weak scaling); time is
+the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s (bf16, causal, N=8192, d=128) and % of GB300 dense peak"
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None, help="name from exact_attention_72_gb300.inputs.WORKLOADS")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time box")
+    return ap.parse_args(argv)
+
+
+# ------------------------------------------------------------------------------------------ ranks
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, value: float) -> float:
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.samples = []   # (host time, [fields])
+        self.error = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def wait_first(self, timeout=5.0):
+        t0 = time.time()
+        while not self.samples and self.proc is not None and time.time() - t0 < timeout:
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.error or not self.samples:
+            return {"error": self.error or "no nvidia-smi samples"}
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1 + 0.06]
+        note = None
+        if not inside:
+            after = [s for (t, s) in self.samples if t >= t0]
+            inside = after[:3]
+            note = "timed region shorter than the sampling interval; nearest samples after its start"
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        mx = [num(s[1]) for s in inside if num(s[1]) is not None]
+        reasons = sorted({self.REASONS[i] for s in inside for i in range(4) if s[3 + i].lower() == "active"})
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": reasons, "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+# ------------------------------------------------------------------------------------------ helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return t.get("bytes_per_launch", {}).get(workload)
+
+
+def credited_flops(w, rows, N):
+    """Metric FLOPs for the given query rows (causal rows see i+1 keys, else N)."""
+    if w.causal:
+        return 4.0 * w.d * sum(int(r) + 1 for r in rows)
+    return 4.0 * w.d * N * len(rows)
+
+
+def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
+    """Runs the oracle on row blocks of successive heads until the time box is used up.
+
+    Returns (TFLOP/s credited by the metric's convention, description, seconds, steps)."""
+    import numpy as np
+    import oracle
+    g = w.H // w.Hkv
+    flops = 0.0
+    elapsed = 0.0
+    steps = 0
+    n_blocks = max(1, w.N // block_rows)
+    blocks_done = []
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    i = 0
+    cache = {}
+    while (elapsed < seconds) and (max_steps is None or steps < max_steps):
+        b, h = heads[i % len(heads)]
+        blk = (i * 7) % n_blocks
+        i += 1
+        r0 = blk * block_rows
+        rows = np.arange(r0, min(w.N, r0 + block_rows))
+        key = (b, h)
+        if key not in cache:
+            cache.clear()
+            def f64(t, hh, s):
+                a = t[b, :, hh, :].float().double().numpy()
+                return a * np.float64(np.float32(s)) if t.element_size() == 1 else a
+            cache[key] = (f64(x.q, h, x.descale_q), f64(x.k, h // g, x.descale_k), f64(x.v, h // g, x.descale_v))
+        q, k, v = cache[key]
+        t0 = time.perf_counter()
+        oracle.attention_head(q, k, v, w.scale, w.causal, rows=rows)
+        elapsed += time.perf_counter() - t0
+        flops += credited_flops(w, rows, w.N)
+        blocks_done.append((b, h, int(r0)))
+        steps += 1
+    desc = (f"{steps} blocks of {block_rows} query rows (full score rows, fp64) from heads of the "
+            f"{w.name} workload; FLOPs credited by the metric's convention")
+    return flops / elapsed / 1e12, desc, elapsed, steps
+
+
+def cores_used() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------------ arms
+def run_reference(args, w, x):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    block = 256
+    # warm-up steps (untimed), then K timed steps, each one oracle row block
+    cpu_oracle_sample(w, x, seconds=1e9, block_rows=block, max_steps=args.warmup)
+    tflops, desc, secs, steps = cpu_oracle_sample(w, x, seconds=1e9, block_rows=block, max_steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+            "qkv_dtype": w.dtype, "k_outliers": w.k_outlier_frac,
+            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "parallelism": "replicas (one full workload per GPU)"}
+
+
+def run_ours(args, w, x):
+    import torch
+    from exact_attention_72_gb300 import binding, build
+    rank, world, local = rank_info()
+    dist = init_dist(world)
+    build.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fp8 = w.dtype == "fp8_e4m3"
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    kw = {}
+    if fp8:
+        kw = {n: torch.tensor([s], dtype=torch.float32, device=dev)
+              for n, s in (("descale_q", x.descale_q), ("descale_k", x.descale_k), ("descale_v", x.descale_v))}
+    o = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, **kw)
+
+    for i in range(max(args.warmup, 0)):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.wait_first()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_host1 = time.time()
+    time.sleep(0.12)
+    sampler.stop()
+    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms per launch
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+    local_ms = sum(durs)
+    total_ms = max_over_ranks(dist, local_ms)
+    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    mean_ms = statistics.fmean(durs)
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    peak_bf16, peak_src = peaks()
+    peak = peak_bf16 * (2.0 if fp8 else 1.0)
+    if fp8:
+        peak_src += " x2 (e4m3/bf16 nominal dense ratio)"
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, x, dev, dist, world)
+
+    clocks = sampler.summary(t_host0, t_host1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops, desc, secs, steps = cpu_oracle_sample(w, x, args.cpu_seconds)
+        cpu = {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": desc + f"; {secs:.1f} s of CPU work"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+            "config": config_of(w),
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": measured_traffic(w.name),
+                         "kernel": "attn_fwd_kernel", "peak_source": peak_src,
+                         "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}},
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def measure_e2e(args, w, x, dev, dist, world):
+    """Same metric through attn_fwd_host: pinned host q/k/v in, o/lse back to pinned host memory."""
+    import torch
+    from exact_attention_72_gb300 import binding
+    code = binding.ATTN_DTYPE_FP8_E4M3 if w.dtype == "fp8_e4m3" else binding.ATTN_DTYPE_BF16
+    ws = torch.empty(binding.attn_fwd_host_workspace_bytes(w.B, w.H, w.Hkv, w.N, w.d, code), dtype=torch.uint8,
+                     device=dev)
+    qh, kh, vh = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
+    oh = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+
+    def step():
+        binding.attn_fwd_host(qh, kh, vh, oh, lh, w.causal, ws, scale=w.scale, descale_q=x.descale_q,
+                              descale_k=x.descale_k, descale_v=x.descale_v)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (12 if code else 0)
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+            "entry_point": "attn_fwd_host"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from exact_attention_72_gb300 import inputs
+    w = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    rank, world, _ = rank_info()
+    if args.impl == "reference" and rank != 0:
+        return 0
+    x = inputs.make_inputs(w)
+    if args.impl == "reference":
+        run_reference(args, w, x)
+    else:
+        run_ours(args, w, x)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

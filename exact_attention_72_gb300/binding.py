@@ -1,0 +1,169 @@
+"""ctypes binding of libattn_gb300.so (argument marshalling only; all compute runs in the library).
+
+The Python names mirror the C ABI in include/attn.h. ``attn_fwd`` takes torch CUDA tensors
+(PyTorch is used for device memory and streams only) and raises ``AttnError`` on any non-OK
+status. There is no fallback: if the library is missing the call fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+from . import build as _build
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT = range(5)
+ATTN_DTYPE_BF16, ATTN_DTYPE_FP8_E4M3 = 0, 1
+STATUS_NAMES = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+                4: "ATTN_ERR_TIMEOUT"}
+
+_LIB = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """Loads the library (it must have been built: ``exact_attention_72_gb300.build.build()``)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} is not built; call exact_attention_72_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.restype = i
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
+    L.attn_fwd_host.restype = i
+    L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
+    L.attn_fwd_host_workspace_bytes.restype = sz
+    L.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.attn_get_status.restype = i
+    L.attn_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.attn_clear_status.restype = i
+    L.attn_clear_status.argtypes = []
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_status_string.argtypes = [i]
+    L.attn_debug_set.restype = None
+    L.attn_debug_set.argtypes = [ctypes.c_ulonglong, i]
+    L.attn_version.restype = i
+    L.attn_version.argtypes = []
+    _LIB = L
+    return L
+
+
+def _check(status: int, what: str) -> None:
+    if status != ATTN_OK:
+        raise AttnError(status, what)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_DTYPE_BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return ATTN_DTYPE_FP8_E4M3
+    raise TypeError(f"q/k/v must be bfloat16 or float8_e4m3fn, got {t.dtype}")
+
+
+def _stream_handle(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def attn_fwd(q, k, v, causal: bool, scale: Optional[float] = None, descale_q=None, descale_k=None,
+             descale_v=None, out=None, lse=None, stream=None):
+    """O, LSE = attention forward of q [B,N,H,d], k/v [B,N,Hkv,d] (CUDA tensors, bf16 or e4m3).
+
+    ``descale_*`` (fp8 only) are one-element float32 CUDA tensors. ``out`` (bf16 [B,N,H,d]) and
+    ``lse`` (float32 [B,H,N]) are allocated if not given. Returns (out, lse).
+    """
+    import torch
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must be [B, N, Hkv, d] with q's dtype")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ptrs = [0, 0, 0]
+    if code == ATTN_DTYPE_FP8_E4M3:
+        for idx, t in enumerate((descale_q, descale_k, descale_v)):
+            if t is None or t.dtype != torch.float32 or not t.is_cuda:
+                raise ValueError("fp8 needs descale_q/k/v as float32 CUDA tensors")
+            ptrs[idx] = t.data_ptr()
+    st = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
+                        float(scale), int(bool(causal)), code, ptrs[0], ptrs[1], ptrs[2], _stream_handle(stream))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_host(q, k, v, out, lse, causal: bool, workspace, scale: Optional[float] = None,
+                  descale_q: float = 1.0, descale_k: float = 1.0, descale_v: float = 1.0, stream=None):
+    """The same forward on HOST (CPU, ideally pinned) tensors through attn_fwd_host.
+
+    ``workspace`` is a CUDA uint8 tensor of at least attn_fwd_host_workspace_bytes(...) bytes.
+    The call returns once o and lse are back in host memory.
+    """
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for t in (q, k, v, out, lse):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("attn_fwd_host takes contiguous host tensors")
+    dq, dk, dv = (ctypes.c_float(descale_q), ctypes.c_float(descale_k), ctypes.c_float(descale_v))
+    fp8 = code == ATTN_DTYPE_FP8_E4M3
+    st = lib().attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, N,
+                             d, float(scale), int(bool(causal)), code,
+                             ctypes.addressof(dq) if fp8 else None, ctypes.addressof(dk) if fp8 else None,
+                             ctypes.addressof(dv) if fp8 else None, workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    _check(st, "attn_fwd_host")
+    return out, lse
+
+
+def attn_fwd_host_workspace_bytes(B: int, H: int, Hkv: int, N: int, d: int, dtype_code: int) -> int:
+    return int(lib().attn_fwd_host_workspace_bytes(B, H, Hkv, N, d, dtype_code))
+
+
+def attn_get_status(stream=None) -> tuple[int, int]:
+    """(status, raw status word) after synchronizing ``stream``."""
+    detail = ctypes.c_uint32(0)
+    st = lib().attn_get_status(_stream_handle(stream), ctypes.byref(detail))
+    return st, detail.value
+
+
+def attn_clear_status() -> None:
+    _check(lib().attn_clear_status(), "attn_clear_status")
+
+
+def attn_status_string(status: int) -> str:
+    return lib().attn_status_string(status).decode()
+
+
+def attn_debug_set(timeout_ns: int = 0, skip_load: bool = False) -> None:
+    lib().attn_debug_set(int(timeout_ns), int(bool(skip_load)))
+
+
+def attn_version() -> int:
+    return int(lib().attn_version())

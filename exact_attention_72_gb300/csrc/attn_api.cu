@@ -1,0 +1,256 @@
+// C ABI of the attention forward library: argument checks, tensor-map encoding, dispatch to
+// the kernel instance for (head dim, causal, dtype), device status word, host-buffer variant.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.h"
+#include "launch.h"
+
+// First failure recorded by any kernel of this library on the device (0 = none).
+static __device__ uint32_t g_attn_status;
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;
+constexpr int kMaxDevices = 64;
+
+unsigned long long g_timeout_ns = 0;  // 0: default
+int g_skip_load = 0;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+struct DeviceInfo {
+  std::once_flag once;
+  int num_sms = 0;
+  uint32_t* status = nullptr;
+  bool ok = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo* di = &g_dev[dev];
+  std::call_once(di->once, [di, dev] {
+    void* p = nullptr;
+    di->ok = cudaDeviceGetAttribute(&di->num_sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+             cudaGetSymbolAddress(&p, g_attn_status) == cudaSuccess;
+    di->status = static_cast<uint32_t*>(p);
+  });
+  return di->ok ? di : nullptr;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// [B, N, heads, d] tensor -> 4-D map (d, N, heads, B), box (128-byte row, 128 rows, 1, 1),
+// 128-byte swizzle; rows past N read as zeros.
+bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int heads, int B) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t elt = fp8 ? 1 : 2;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)heads * d * elt, (cuuint64_t)d * elt, (cuuint64_t)N * heads * d * elt};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool supported_dim(int d, attn_dtype_t dtype) {
+  if (dtype == ATTN_DTYPE_BF16) return d == 64 || d == 128 || d == 256;
+  if (dtype == ATTN_DTYPE_FP8_E4M3) return d == 128;
+  return false;
+}
+
+// Shape checks shared by attn_fwd and attn_fwd_host.
+attn_status_t check_shape(int B, int H, int Hkv, int N, int d, float scale, attn_dtype_t dtype) {
+  if (B < 1 || H < 1 || Hkv < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
+  // The row max is taken on unscaled scores (needs scale > 0); scale == 0 would turn masked
+  // entries into NaN (-inf * 0).
+  if (scale <= 0.0f) return ATTN_ERR_UNSUPPORTED;
+  if (!supported_dim(d, dtype)) return ATTN_ERR_UNSUPPORTED;
+  const long long rows = gb300::rows_per_work_tile(d);
+  const long long tiles = (long long)B * H * ((N + rows - 1) / rows);
+  if (tiles >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * N * H * d >= (1LL << 40)) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+template <int D>
+cudaError_t dispatch_d(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
+  if constexpr (D == 128) {
+    if (fp8) return causal ? gb300::launch_attn_fwd<128, true, true>(a, s) : gb300::launch_attn_fwd<128, false, true>(a, s);
+  }
+  return causal ? gb300::launch_attn_fwd<D, true, false>(a, s) : gb300::launch_attn_fwd<D, false, false>(a, s);
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                       int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
+                       const float* descale_k, const float* descale_v, cudaStream_t stream) {
+  attn_status_t st = check_shape(B, H, Hkv, N, d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (fp8 && (!descale_q || !descale_k || !descale_v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t elt = fp8 ? 1 : 2;
+  const size_t nq = (size_t)B * N * H * d, nkv = (size_t)B * N * Hkv * d;
+  const size_t o_bytes = nq * 2, lse_bytes = (size_t)B * H * N * 4;
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {nq * elt, nkv * elt, nkv * elt};
+  for (int i = 0; i < 3; ++i)
+    if (ranges_overlap(o, o_bytes, ins[i], in_bytes[i]) || ranges_overlap(lse, lse_bytes, ins[i], in_bytes[i]))
+      return ATTN_ERR_INVALID_ARG;
+  if (ranges_overlap(o, o_bytes, lse, lse_bytes)) return ATTN_ERR_INVALID_ARG;
+
+  DeviceInfo* di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  gb300::LaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map(&a.tm_q, q, fp8, d, N, H, B) || !make_map(&a.tm_k, k, fp8, d, N, Hkv, B) ||
+      !make_map(&a.tm_v, v, fp8, d, N, Hkv, B))
+    return ATTN_ERR_CUDA;
+  const int rows = gb300::rows_per_work_tile(d);
+  gb300::AttnParams& p = a.params;
+  p.o = o;
+  p.lse = lse;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.n_mb = (N + rows - 1) / rows;
+  p.n_tiles = B * H * p.n_mb;
+  p.status = di->status;
+  p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
+  p.debug_skip_load = g_skip_load;
+  a.num_sms = di->num_sms;
+  cudaError_t e;
+  switch (d) {
+    case 64: e = dispatch_d<64>(a, causal != 0, fp8, stream); break;
+    case 128: e = dispatch_d<128>(a, causal != 0, fp8, stream); break;
+    default: e = dispatch_d<256>(a, causal != 0, fp8, stream); break;
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_dtype_t dtype) {
+  if (check_shape(B, H, Hkv, N, d, 1.0f, dtype) != ATTN_OK) return 0;
+  const size_t elt = dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2;
+  const size_t nq = (size_t)B * N * H * d, nkv = (size_t)B * N * Hkv * d;
+  return round_up(nq * elt, 256) + 2 * round_up(nkv * elt, 256) + round_up(nq * 2, 256) +
+         round_up((size_t)B * H * N * 4, 256) + 256;
+}
+
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                            int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
+                            const float* descale_k, const float* descale_v, void* workspace,
+                            size_t workspace_bytes, cudaStream_t stream) {
+  attn_status_t st = check_shape(B, H, Hkv, N, d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (fp8 && (!descale_q || !descale_k || !descale_v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256) || workspace_bytes < attn_fwd_host_workspace_bytes(B, H, Hkv, N, d, dtype))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t elt = fp8 ? 1 : 2;
+  const size_t nq = (size_t)B * N * H * d, nkv = (size_t)B * N * Hkv * d;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  uint8_t* dq = w;
+  uint8_t* dk = dq + round_up(nq * elt, 256);
+  uint8_t* dv = dk + round_up(nkv * elt, 256);
+  uint8_t* d_o = dv + round_up(nkv * elt, 256);
+  uint8_t* d_lse = d_o + round_up(nq * 2, 256);
+  float* d_desc = reinterpret_cast<float*>(d_lse + round_up((size_t)B * H * N * 4, 256));
+  if (cudaMemcpyAsync(dq, q, nq * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dk, k, nkv * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(dv, v, nkv * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (fp8) {
+    const float desc[3] = {*descale_q, *descale_k, *descale_v};
+    if (cudaMemcpyAsync(d_desc, desc, sizeof(desc), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  st = attn_fwd(dq, dk, dv, d_o, reinterpret_cast<float*>(d_lse), B, H, Hkv, N, d, scale, causal, dtype,
+                fp8 ? d_desc : nullptr, fp8 ? d_desc + 1 : nullptr, fp8 ? d_desc + 2 : nullptr, stream);
+  if (st != ATTN_OK) return st;
+  if (cudaMemcpyAsync(o, d_o, nq * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(lse, d_lse, (size_t)B * H * N * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {
+  if (detail) *detail = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (detail) *detail = v;
+  return v ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+attn_status_t attn_clear_status(void) {
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return cudaDeviceSynchronize() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_CUDA: return "CUDA error";
+    case ATTN_ERR_TIMEOUT: return "kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+void attn_debug_set(unsigned long long timeout_ns, int skip_load) {
+  g_timeout_ns = timeout_ns;
+  g_skip_load = skip_load;
+}
+
+int attn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,7 @@
+// bf16 instances of the attention forward, head dim 256 (non-causal and causal).
+#include "launch_impl.cuh"
+
+namespace gb300 {
+template cudaError_t launch_attn_fwd<256, false, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<256, true, false>(LaunchArgs&, cudaStream_t);
+}  // namespace gb300

@@ -1,0 +1,527 @@
+// Fused exact-attention forward for sm_103a: O = softmax(scale * Q K^T [+ causal mask]) V and
+// the per-row log-sum-exp, computed tile by tile with the online softmax so the N x N score
+// matrix never reaches global memory.
+//
+// The algorithm is the one the pages describe (tile the computation and keep a running max
+// and sum per row: "flash-attention-3" (ai.thesatyajit.com), opening paragraph; the consumer
+// does WGMMA(Q, K^T), rescale / exp / rowmax / rowsum, then WGMMA(P, V): "Lecture 9 — Hopper /
+// FlashAttention-3 / FlashAttention-4", "Warp specialisation in FA3"). The schedule is new and
+// written for Blackwell's tcgen05 tensor cores:
+//
+//   * one persistent CTA per SM walks work tiles (batch, head, block of NQ x 128 query rows);
+//     causal work is ordered longest first ("flash-attention-3", "Five schedulers": the
+//     longest-processing-time heuristic; "Hopper" tag page, section 9.2 title);
+//   * warp LOAD issues TMA copies: Q once per work tile, then K_j and V_j through a ring of
+//     NS shared-memory stages guarded by full/empty mbarriers ("FlashAttention-3 Deep Dive"
+//     (mojostudio.in), section 2, the producer's multi-stage TMA pipeline with expected
+//     transaction bytes);
+//   * warp MMA (one thread) issues tcgen05.mma: S = Q K_j^T into tensor memory (TMEM), and
+//     O += P V_j with P read from TMEM (aliasing S) and V from shared memory;
+//   * one softmax warpgroup per Q tile (one thread per query row) reads S from TMEM, masks,
+//     takes the row max, evaluates exp2 with the scale folded in, accumulates the row sum,
+//     writes P back to TMEM and rescales O in TMEM when the running max moves;
+//   * the epilogue (same warpgroup) divides O by the row sum and writes O (bf16) and LSE.
+//
+// Two Q tiles per CTA share each K/V stage: while one warpgroup runs its softmax the tensor
+// core works on the other tile's GEMMs (the role pingpong played on Hopper: "flash-attention-3",
+// "Why a schedule, and not an algorithm"; "Lecture 9", "Ping-pong scheduling").
+//
+// Running-max reference: a row keeps its old max m as the exponent shift until a new tile's
+// max exceeds it by more than 8 (log2 units). Until then p = exp2(s*x - m) <= 2^8, which fp32
+// sums, bf16 and e4m3 all hold; O and l share the same shift, so the final O / l is exact.
+// This skips almost every O rescale after the first few tiles.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include "ptx.cuh"
+
+namespace gb300 {
+
+struct AttnParams {
+  void* o;                  // bf16 [B, N, H, D]
+  float* lse;               // fp32 [B, H, N]
+  const float* descale_q;   // fp8 only: one fp32 each (device)
+  const float* descale_k;
+  const float* descale_v;
+  int B, H, Hkv, N;
+  float scale_log2;         // scale * log2(e)
+  int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head)
+  int n_tiles;              // B * H * n_mb
+  uint32_t* status;         // device status word (first failure)
+  unsigned long long timeout_ns;
+  int debug_skip_load;      // fault injection: CTA 0 never loads V_0 of its first tile
+};
+
+template <int D_, bool CAUSAL_, bool FP8_>
+struct AttnCfg {
+  static constexpr int D = D_;
+  static constexpr bool CAUSAL = CAUSAL_;
+  static constexpr bool FP8 = FP8_;
+  static constexpr int ELT = FP8 ? 1 : 2;                 // bytes per q/k/v element
+  static constexpr int NQ = (D <= 128) ? 2 : 1;           // 128-row Q tiles per CTA
+  static constexpr int BM = 128, BN = 128;                // query rows per Q tile, keys per KV tile
+  static constexpr int CE = 128 / ELT;                    // elements in one 128-byte swizzle row
+  static constexpr int NCH = D / CE;                      // 128-byte column chunks per row
+  static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes (one TMA box)
+  static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one Q, K or V tile
+  static constexpr int Q_BYTES = NQ * TILE_BYTES;
+  static constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
+  static constexpr int RESERVE = 1024 + 1024;             // alignment slack + static shared
+  static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES) / TILE_BYTES;
+  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;      // K/V ring stages
+  static constexpr int SMEM_BYTES = Q_BYTES + NS * TILE_BYTES + 1024;
+  static constexpr int KSTEPS_QK = D * ELT / 32;          // one MMA k-step covers 32 bytes of K
+  static constexpr int KSTEPS_PV = BN * ELT / 32;
+  static constexpr int PV_ROWS = 32 / ELT;                // V rows consumed per PV k-step
+  static constexpr int P_COLS = BN * ELT / 4;             // TMEM columns holding one P row
+  static constexpr int S_COL0 = 0, S_COL1 = 128;          // two S buffers
+  static constexpr int O_COL = 256;                       // O tile qt at O_COL + qt * D
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int WARP_MMA = 4 * NQ, WARP_LOAD = 4 * NQ + 1;
+  static constexpr int THREADS = (4 * NQ + 2) * 32;
+  static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
+  static constexpr uint32_t IDESC_QK = make_idesc(FMT, 128, BN, false, false);
+  static constexpr uint32_t IDESC_PV = make_idesc(FMT, 128, D, false, true);
+  static_assert(NS >= 2, "K/V ring needs at least two stages");
+  static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
+  static_assert(D % CE == 0, "head dim must fill whole 128-byte rows");
+};
+
+// Wait-site codes recorded in the status word when a bounded wait gives up.
+enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
+                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8 };
+
+struct TileCoord {
+  int b, h, mb;
+};
+
+// Work tile t -> (batch, head, query block). Causal tiles go longest first: every head's last
+// query block, then every head's second-to-last, and so on. Non-causal tiles keep a head's
+// blocks together so concurrently running CTAs share K/V in L2.
+template <bool CAUSAL>
+__device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
+  TileCoord c;
+  const int BH = p.B * p.H;
+  int bh;
+  if (CAUSAL) {
+    c.mb = p.n_mb - 1 - t / BH;
+    bh = t % BH;
+  } else {
+    c.mb = t % p.n_mb;
+    bh = t / p.n_mb;
+  }
+  c.b = bh / p.H;
+  c.h = bh % p.H;
+  return c;
+}
+
+// Number of KV tiles Q tile `qt` of query block `mb` visits (0 if all its rows are past N).
+template <class C>
+__device__ __forceinline__ int kv_tiles_for(int mb, int qt, int N) {
+  const int row0 = (mb * C::NQ + qt) * C::BM;
+  if (row0 >= N) return 0;
+  const int n_kv = (N + C::BN - 1) / C::BN;
+  return C::CAUSAL ? (row0 / C::BN + 1) : n_kv;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_kv_empty[C::NS];
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[C::NQ], bar_o_done[C::NQ];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile uint32_t abort_flag;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  const uint32_t sQ = smem_base;
+  const uint32_t sKV = smem_base + C::Q_BYTES;
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+
+  if (tid == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_addr(&bar_q_full), 1);
+    mbar_init(smem_addr(&bar_q_empty), 1);
+    mbar_init(smem_addr(&bar_drain), 1);
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(smem_addr(&bar_kv_full[i]), 1);
+      mbar_init(smem_addr(&bar_kv_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&bar_s_full[i]), 1);
+    for (int i = 0; i < C::NQ; ++i) {
+      mbar_init(smem_addr(&bar_p_full[i]), 128);
+      mbar_init(smem_addr(&bar_o_done[i]), 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(smem_addr(&tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == C::WARP_LOAD) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t ring = 0;      // K/V tiles issued so far (ring position)
+      uint32_t nq_loads = 0;  // Q loads issued so far
+      bool ok = true;
+      int iter = 0;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++iter) {
+        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
+        const int kvh = tc.h / (p.H / p.Hkv);
+        int nmax = 0, nq_valid = 0;
+        for (int qt = 0; qt < C::NQ; ++qt) {
+          const int n = kv_tiles_for<C>(tc.mb, qt, p.N);
+          nmax = n > nmax ? n : nmax;
+          nq_valid += (n > 0);
+        }
+        // Q: wait until the previous work tile's last S = Q K^T has completed.
+        if (nq_loads > 0 && !mbar_wait(smem_addr(&bar_q_empty), (nq_loads - 1) & 1, ctl, SITE_Q_EMPTY)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(smem_addr(&bar_q_full), nq_valid * C::TILE_BYTES);
+        for (int qt = 0; qt < C::NQ; ++qt) {
+          const int row0 = (tc.mb * C::NQ + qt) * C::BM;
+          if (row0 >= p.N) continue;
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_4d(sQ + (qt * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, smem_addr(&bar_q_full), ch * C::CE,
+                        row0, tc.h, tc.b);
+        }
+        ++nq_loads;
+        for (int j = 0; ok && j < nmax; ++j) {
+          for (int which = 0; which < 2; ++which) {  // 0: K_j, 1: V_j
+            const uint32_t slot = ring % C::NS;
+            if (ring >= (uint32_t)C::NS &&
+                !mbar_wait(smem_addr(&bar_kv_empty[slot]), ((ring / C::NS) - 1) & 1, ctl, SITE_KV_EMPTY)) {
+              ok = false;
+              break;
+            }
+            const bool skip = p.debug_skip_load && blockIdx.x == 0 && iter == 0 && j == 0 && which == 1;
+            if (!skip) {
+              const CUtensorMap* tm = which ? &tm_v : &tm_k;
+              mbar_arrive_expect_tx(smem_addr(&bar_kv_full[slot]), C::TILE_BYTES);
+              for (int ch = 0; ch < C::NCH; ++ch)
+                tma_load_4d(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES, tm, smem_addr(&bar_kv_full[slot]),
+                            ch * C::CE, j * C::BN, kvh, tc.b);
+            }
+            ++ring;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwinding: let every copy still in flight land before the CTA exits.
+        const uint32_t first = ring > (uint32_t)C::NS ? ring - C::NS : 0u;
+        for (uint32_t pos = first; pos < ring; ++pos) {
+          const uint32_t bar = smem_addr(&bar_kv_full[pos % C::NS]);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(bar, (pos / C::NS) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+        if (nq_loads > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_q_full), (nq_loads - 1) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+      }
+    }
+  } else if (warp == C::WARP_MMA) {
+    // ------------------------------------------------------------------ tcgen05 issuer
+    if (lane == 0) {
+      uint32_t ring = 0;        // K/V ring position (same sequence as the producer)
+      uint32_t nq_loads = 0;
+      uint32_t p_cnt[C::NQ];    // P tiles consumed per Q tile
+      for (int qt = 0; qt < C::NQ; ++qt) p_cnt[qt] = 0;
+      bool ok = true;
+      auto s_buf_col = [](int qt, int j) -> uint32_t {
+        return (C::NQ == 2 ? qt : (j & 1)) ? (uint32_t)C::S_COL1 : (uint32_t)C::S_COL0;
+      };
+      auto s_buf_idx = [](int qt, int j) -> int { return C::NQ == 2 ? qt : (j & 1); };
+      auto issue_qk = [&](int qt, int j, uint32_t k_slot) {
+        const uint32_t d_tmem = tmem + s_buf_col(qt, j);
+        const uint32_t a0 = sQ + qt * C::TILE_BYTES;
+        const uint32_t b0 = sKV + k_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          mma_f16_or_f8<C::FP8>(d_tmem, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(b0 + off, 16, 1024),
+                                C::IDESC_QK, kk > 0);
+        }
+        tc_commit(smem_addr(&bar_s_full[s_buf_idx(qt, j)]));
+      };
+      auto issue_pv = [&](int qt, int j, uint32_t v_slot) {
+        const uint32_t d_tmem = tmem + C::O_COL + qt * C::D;
+        const uint32_t a_tmem = tmem + s_buf_col(qt, j);
+        const uint32_t b0 = sKV + v_slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < C::KSTEPS_PV; ++kk)
+          mma_ts_f16_or_f8<C::FP8>(d_tmem, a_tmem + kk * 8,
+                                   make_sdesc_sw128(b0 + kk * C::PV_ROWS * 128, C::CHUNK_BYTES, 1024), C::IDESC_PV,
+                                   j > 0 || kk > 0);
+        tc_commit(smem_addr(&bar_o_done[qt]));
+      };
+      auto wait_kv = [&](uint32_t pos) -> bool {
+        return mbar_wait(smem_addr(&bar_kv_full[pos % C::NS]), (pos / C::NS) & 1, ctl, SITE_KV_FULL);
+      };
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
+        int n[C::NQ], nmax = 0;
+        for (int qt = 0; qt < C::NQ; ++qt) {
+          n[qt] = kv_tiles_for<C>(tc.mb, qt, p.N);
+          nmax = n[qt] > nmax ? n[qt] : nmax;
+        }
+        if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
+        ++nq_loads;
+        tc_fence_after();
+        const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
+        // Prologue: S_0 for every Q tile.
+        if (!wait_kv(base)) { ok = false; break; }
+        tc_fence_after();
+        for (int qt = 0; qt < C::NQ; ++qt)
+          if (n[qt] > 0) issue_qk(qt, 0, base % C::NS);
+        // Release K_0 before waiting for anything else: with a two-stage ring the producer
+        // needs this slot back to load K_1.
+        tc_commit(smem_addr(&bar_kv_empty[base % C::NS]));
+        if (C::NQ == 1 && nmax > 1) {
+          // One Q tile: the second S buffer lets S_1 run while the softmax works on S_0.
+          if (!wait_kv(base + 2)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk(0, 1, (base + 2) % C::NS);
+          tc_commit(smem_addr(&bar_kv_empty[(base + 2) % C::NS]));
+        }
+        if (nmax == 1 || (C::NQ == 1 && nmax == 2)) tc_commit(smem_addr(&bar_q_empty));
+        for (int j = 0; ok && j < nmax; ++j) {
+          const uint32_t pos_v = base + 2 * j + 1;
+          if (!wait_kv(pos_v)) { ok = false; break; }
+          if (C::NQ == 2) {
+            const bool more = j + 1 < nmax;
+            if (more && !wait_kv(pos_v + 1)) { ok = false; break; }
+            tc_fence_after();
+            for (int qt = 0; qt < C::NQ; ++qt) {
+              if (j >= n[qt]) continue;
+              if (!mbar_wait(smem_addr(&bar_p_full[qt]), p_cnt[qt] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
+              ++p_cnt[qt];
+              tc_fence_after();
+              issue_pv(qt, j, pos_v % C::NS);
+              if (j + 1 < n[qt]) issue_qk(qt, j + 1, (pos_v + 1) % C::NS);
+            }
+            if (!ok) break;
+            tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
+            if (more) {
+              tc_commit(smem_addr(&bar_kv_empty[(pos_v + 1) % C::NS]));
+              if (j + 2 == nmax) tc_commit(smem_addr(&bar_q_empty));
+            }
+          } else {
+            // One Q tile: S_{j+1} was issued a step ahead; issue S_{j+2} into the buffer P_j frees
+            // once PV_j has been issued (the tensor core runs them in issue order).
+            tc_fence_after();
+            if (!mbar_wait(smem_addr(&bar_p_full[0]), p_cnt[0] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
+            ++p_cnt[0];
+            tc_fence_after();
+            issue_pv(0, j, pos_v % C::NS);
+            tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
+            if (j + 2 < nmax) {
+              const uint32_t pos_k = base + 2 * (j + 2);
+              if (!wait_kv(pos_k)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(0, j + 2, pos_k % C::NS);
+              tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
+              if (j + 3 == nmax) tc_commit(smem_addr(&bar_q_empty));
+            }
+          }
+        }
+        ring = base + 2 * nmax;
+      }
+      // Every MMA issued so far must finish before TMEM is released.
+      tc_commit(smem_addr(&bar_drain));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax + epilogue
+    const int qt = warp >> 2;                  // Q tile of this warpgroup
+    const int r = ((warp & 3) << 5) + lane;    // row within the Q tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
+    const float s = p.scale_log2 * (C::FP8 ? __ldg(p.descale_q) * __ldg(p.descale_k) : 1.0f);
+    const float out_scale = C::FP8 ? __ldg(p.descale_v) : 1.0f;
+    uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
+    uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
+    const int n_kv_all = (p.N + C::BN - 1) / C::BN;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
+      const int n = kv_tiles_for<C>(tc.mb, qt, p.N);
+      if (n == 0) continue;
+      const int row0 = (tc.mb * C::NQ + qt) * C::BM;
+      float m = -INFINITY;   // running max of s * x (log2 units), used as the exponent shift
+      float l = 0.0f;        // running sum of exp2(s * x - m)
+      for (int j = 0; j < n; ++j) {
+        const int buf = C::NQ == 2 ? qt : (j & 1);
+        const uint32_t s_col = buf ? C::S_COL1 : C::S_COL0;
+        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), s_cnt[buf] & 1, ctl, SITE_S_FULL);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        ++s_cnt[buf];
+        tc_fence_after();
+        uint32_t sr[128];
+        const uint32_t tS = tmem + lane_base + s_col;
+        tmem_ld_32cols(tS, sr);
+        tmem_ld_32cols(tS + 32, sr + 32);
+        tmem_ld_32cols(tS + 64, sr + 64);
+        tmem_ld_32cols(tS + 96, sr + 96);
+        tmem_ld_wait();
+        reg_fence32(sr);
+        reg_fence32(sr + 32);
+        reg_fence32(sr + 64);
+        reg_fence32(sr + 96);
+        float x[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+        // Masking: keys past N (ragged tail) and, on the diagonal tile, keys after the query row.
+        const bool diag = C::CAUSAL && (j == n - 1);
+        const bool tail = (j == n_kv_all - 1) && (p.N % C::BN != 0);
+        if (diag || tail) {
+          int lim = p.N - j * C::BN;
+          if (diag) lim = min(lim, (row0 + r) - j * C::BN + 1);
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) x[c] = -INFINITY;
+        }
+        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+#pragma unroll
+        for (int c = 4; c < 128; c += 4) {
+          mx0 = fmaxf(mx0, x[c]);
+          mx1 = fmaxf(mx1, x[c + 1]);
+          mx2 = fmaxf(mx2, x[c + 2]);
+          mx3 = fmaxf(mx3, x[c + 3]);
+        }
+        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * s;
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (m_tile > m + 8.0f) {
+          alpha = ex2(m - m_tile);   // 0 on the first tile (m = -inf)
+          m = m_tile;
+          rescale = true;
+        }
+        const float neg_m = -m;
+        float l0 = 0.f, l1 = 0.f;
+        const uint32_t tP = tS;   // P overwrites the first P_COLS columns of the S buffer
+        if (!C::FP8) {
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const float p0 = ex2(fmaf(x[c0 + c], s, neg_m));
+              const float p1 = ex2(fmaf(x[c0 + c + 1], s, neg_m));
+              l0 += p0;
+              l1 += p1;
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_16cols(tP + (c0 >> 1), pk);
+          }
+        } else {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 128; c += 4) {
+            const float p0 = ex2(fmaf(x[c], s, neg_m));
+            const float p1 = ex2(fmaf(x[c + 1], s, neg_m));
+            const float p2 = ex2(fmaf(x[c + 2], s, neg_m));
+            const float p3 = ex2(fmaf(x[c + 3], s, neg_m));
+            l0 += p0 + p2;
+            l1 += p1 + p3;
+            pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+          }
+          tmem_st_32cols(tP, pk);
+        }
+        l = l * alpha + (l0 + l1);
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+          // O (held in TMEM) must not be touched while PV_{j-1} is still accumulating into it.
+          w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
+#pragma unroll 1
+          for (int c0 = 0; c0 < C::D; c0 += 32) {
+            uint32_t ov[32];
+            tmem_ld_32cols(tO + c0, ov);
+            tmem_ld_wait();
+            reg_fence32(ov);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+            tmem_st_32cols(tO + c0, ov);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_p_full[qt]));
+      }
+      if (!ok) break;
+      // Epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2.
+      bool w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + n - 1) & 1, ctl, SITE_O_DONE);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      pv_cnt += n;
+      tc_fence_after();
+      const int row = row0 + r;
+      const bool valid = row < p.N;
+      const float inv_l = out_scale / l;
+      const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
+      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                            ((size_t)(tc.b * p.N + (valid ? row : 0)) * p.H + tc.h) * C::D;
+#pragma unroll 1
+      for (int c0 = 0; c0 < C::D; c0 += 32) {
+        uint32_t ov[32];
+        tmem_ld_32cols(tO + c0, ov);
+        tmem_ld_wait();
+        reg_fence32(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2)
+          pk[c >> 1] = pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        }
+      }
+      if (valid) p.lse[((size_t)tc.b * p.H + tc.h) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace gb300

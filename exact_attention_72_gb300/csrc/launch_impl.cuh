@@ -1,0 +1,19 @@
+// Definition of the per-instance launcher; included by the instantiation units only.
+#pragma once
+#include "launch.h"
+
+namespace gb300 {
+
+template <int D, bool CAUSAL, bool FP8>
+cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
+  using C = AttnCfg<D, CAUSAL, FP8>;
+  auto kernel = attn_fwd_kernel<C>;
+  // The attribute is per device; setting it on every call is cheap and keeps this stateless.
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = a.params.n_tiles < a.num_sms ? a.params.n_tiles : a.num_sms;
+  kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.params);
+  return cudaGetLastError();
+}
+
+}  // namespace gb300

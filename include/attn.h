@@ -1,0 +1,123 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) fused exact-attention forward library
+ * (libattn_gb300.so).
+ *
+ * The operation, from the pages this library follows:
+ *   O = softmax(scale * Q K^T [+ causal mask]) V, plus the per-row log-sum-exp (LSE),
+ *   computed tile by tile with a running (online) softmax so the N x N score matrix is never
+ *   written to memory.
+ *   - Formula: "FlashAttention-3 Deep Dive: WGMMA Async Pipelines, FP8 Tensor Cores & GPU Kernel
+ *     Optimization in 2026" (mojostudio.in), introduction (softmax(Q K^T / sqrt(d_k)) V) and
+ *     section 3 (P_ij = exp(S_ij - m_i)).
+ *   - Tiling + running softmax, no N x N in memory: "flash-attention-3" (ai.thesatyajit.com),
+ *     opening paragraph.
+ *   - Call shape flash_attn_func(q, k, v, causal=True) with q of shape (B, N, H, D):
+ *     "Lecture 9 — Hopper / FlashAttention-3 / FlashAttention-4", "Benchmark task".
+ *   - GQA and FP8 forward with per-tensor descale factors: "flash-attention-3", "What is
+ *     actually in the box" and "FP8 is a different kernel"; "Lecture 9", "FP8".
+ *   - LSE: the "Hopper" tag page (l1-ca0.github.io) names it in its section 4.6 title
+ *     ("rescaling, correction, and LSE"); read here as the natural-log log-sum-exp of the
+ *     scaled, masked scores of the row.
+ *
+ * All entry points are plain C; pointers are raw device or host addresses as stated per call.
+ */
+#ifndef GB300_ATTN_H
+#define GB300_ATTN_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or overlap; nothing was launched   */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement; nothing launched   */
+  ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, copy, sync, no GPU)  */
+  ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (reported by attn_get_status)   */
+} attn_status_t;
+
+typedef enum {
+  ATTN_DTYPE_BF16 = 0,      /* q, k, v are bfloat16                                          */
+  ATTN_DTYPE_FP8_E4M3 = 1   /* q, k, v are float8 e4m3 (OCP "fn": max 448) with fp32 descales */
+} attn_dtype_t;
+
+/*
+ * attn_fwd — fused attention forward on the GPU, asynchronous on `stream`.
+ *
+ * Arguments (all tensors contiguous, row-major, in DEVICE memory owned by the caller):
+ *   q      [B, N, H,   d]  element type `dtype`
+ *   k, v   [B, N, Hkv, d]  element type `dtype`; query head h reads kv head h / (H / Hkv)
+ *   o      [B, N, H,   d]  bfloat16 output
+ *   lse    [B, H, N]       float32 output, LSE_i = ln sum_j exp(scale * q_i . k_j) over the
+ *                          keys row i may see (all keys, or j <= i when causal)
+ *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16, d == 128 for fp8.
+ *   scale  finite float > 0 multiplying the raw dot products (usually 1/sqrt(d)); it does not
+ *          include the fp8 descales. scale <= 0 returns ATTN_ERR_UNSUPPORTED.
+ *   causal nonzero: key j is visible to query i iff j <= i (top-left aligned).
+ *   descale_q/k/v  fp8 only: DEVICE pointers to one float each; the value the kernel uses
+ *          for an element x8 is x8 * descale. Ignored (may be NULL) for bf16.
+ *   stream CUDA stream (0 = legacy default stream).
+ *
+ * Alignment: q, k, v, o must be 16-byte aligned (tensor-memory-accelerator copies and 16-byte
+ * stores); lse 4-byte aligned. o and lse must not overlap q, k, v or each other.
+ *
+ * Errors: argument problems return ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED synchronously
+ * and launch nothing. A failed launch returns ATTN_ERR_CUDA. A kernel that gives up a bounded
+ * internal wait finishes early and records it in a device status word: read it with
+ * attn_get_status. The library allocates no memory in this call and keeps no per-call state.
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Hkv, int N, int d, float scale, int causal,
+                       attn_dtype_t dtype, const float* descale_q, const float* descale_k,
+                       const float* descale_v, cudaStream_t stream);
+
+/*
+ * attn_fwd_host — the same operation on HOST buffers: copies q, k, v (and the three fp8
+ * descales, given here as HOST pointers to one float each) to device buffers owned by the
+ * caller (`workspace`, at least attn_fwd_host_workspace_bytes(...) bytes of device memory,
+ * 256-byte aligned), runs attn_fwd, and copies o and lse back to host memory. All copies and
+ * the kernel are queued on `stream`; the call synchronizes `stream` before returning.
+ * Host buffers may be pageable or pinned (pinned overlaps better). Returns as attn_fwd, plus
+ * ATTN_ERR_INVALID_ARG for a too-small or misaligned workspace.
+ */
+attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                            int B, int H, int Hkv, int N, int d, float scale, int causal,
+                            attn_dtype_t dtype, const float* descale_q, const float* descale_k,
+                            const float* descale_v, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
+/* Device bytes attn_fwd_host needs for one call of this shape (0 for invalid shapes). */
+size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_dtype_t dtype);
+
+/*
+ * attn_get_status — synchronizes `stream`, then returns ATTN_ERR_TIMEOUT if any kernel of this
+ * library on the current device gave up a bounded wait since the last attn_clear_status,
+ * ATTN_ERR_CUDA if the synchronization failed, else ATTN_OK. `detail` (may be NULL) receives
+ * the raw status word (0, or 0x40000000 | wait-site code).
+ */
+attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail);
+
+/* attn_clear_status — resets the current device's status word to 0 (synchronous). */
+attn_status_t attn_clear_status(void);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* attn_status_string(attn_status_t s);
+
+/*
+ * attn_debug_set — test hook for failure handling. timeout_ns: limit for every bounded wait
+ * inside later kernels (0 restores the default of 4 s). skip_load: when nonzero, later launches
+ * make CTA 0 skip one K/V tile copy so a wait runs out on purpose; the kernel then unwinds and
+ * records ATTN_ERR_TIMEOUT. Process-wide, not thread-safe; for tests only.
+ */
+void attn_debug_set(unsigned long long timeout_ns, int skip_load);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GB300_ATTN_H */

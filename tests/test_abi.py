@@ -1,0 +1,82 @@
+"""C-ABI checks that need no GPU: the library builds, loads, exports every declared entry point,
+and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_72_gb300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_host", "attn_get_status", "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, f"declared in attn.h but not exported: {missing}"
+
+
+def test_status_strings_and_version(lib):
+    assert binding.attn_status_string(binding.ATTN_OK) == "ok"
+    assert binding.attn_status_string(binding.ATTN_ERR_TIMEOUT) == "kernel wait timed out"
+    assert binding.attn_status_string(99) == "unknown status"
+    assert binding.attn_version() >= 100
+
+
+def _call(lib, q=4096, k=8192, v=12288, o=16384, lse=1 << 20, B=1, H=2, Hkv=2, N=128, d=128, scale=0.1,
+          causal=0, dtype=0, dq=None, dk=None, dv=None):
+    # Fake, non-dereferenced addresses: every call here must fail validation before any CUDA call.
+    return lib.attn_fwd(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, dtype, dq, dk, dv, None)
+
+
+def test_validation_rejects_bad_arguments(lib):
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+    assert _call(lib, q=0) == INV                         # null pointer
+    assert _call(lib, lse=0) == INV
+    assert _call(lib, B=0) == INV                         # empty batch
+    assert _call(lib, N=0) == INV                         # empty sequence
+    assert _call(lib, H=3, Hkv=2) == INV                  # H not a multiple of Hkv
+    assert _call(lib, scale=float("nan")) == INV
+    assert _call(lib, scale=float("inf")) == INV
+    assert _call(lib, dtype=7) == INV
+    assert _call(lib, d=96) == UNS                        # head dim without an instance
+    assert _call(lib, d=64, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # fp8 only for d=128
+    assert _call(lib, scale=-0.5) == UNS
+    assert _call(lib, scale=0.0) == UNS
+    assert _call(lib, dtype=1) == INV                     # fp8 without descales
+    assert _call(lib, q=4097) == INV                      # misaligned (TMA needs 16 bytes)
+    assert _call(lib, o=16392) == INV
+    assert _call(lib, lse=(1 << 20) + 2) == INV
+    # o overlapping q (q spans 1*128*2*128*2 = 64 KiB from 4096)
+    assert _call(lib, q=1 << 16, k=1 << 24, v=1 << 25, o=(1 << 16) + 4096, lse=1 << 26) == INV
+    # lse overlapping v
+    assert _call(lib, q=1 << 16, k=1 << 24, v=1 << 25, o=1 << 27, lse=(1 << 25) + 64) == INV
+
+
+def test_host_workspace_size(lib):
+    n = binding.attn_fwd_host_workspace_bytes(2, 32, 8, 8192, 128, binding.ATTN_DTYPE_BF16)
+    q = 2 * 8192 * 32 * 128 * 2
+    kv = 2 * 8192 * 8 * 128 * 2
+    assert n >= q + 2 * kv + q + 2 * 32 * 8192 * 4
+    assert binding.attn_fwd_host_workspace_bytes(0, 1, 1, 1, 128, 0) == 0
+    assert binding.attn_fwd_host_workspace_bytes(1, 1, 1, 1, 96, 0) == 0

@@ -1,0 +1,52 @@
+"""Failure handling on the GPU without a GPU fault: a K/V copy is skipped on purpose so a
+bounded wait runs out; the kernel must unwind, report ATTN_ERR_TIMEOUT through the status word,
+and leave the context usable for a correct follow-up call. Also checks the host-buffer entry
+point against the device one."""
+import pytest
+import torch
+
+from exact_attention_72_gb300 import binding, inputs
+from parity_util import all_heads, compare_heads, oracle_heads, run_cuda, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    from exact_attention_72_gb300 import binding, build
+    build.build()
+    binding.attn_debug_set(timeout_ns=1_000_000_000)   # a correct launch never waits this long
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (256, False), (64, False)])
+def test_skipped_copy_times_out_and_context_survives(d, causal):
+    w = inputs.Workload("fault", B=1, H=4, Hkv=2, N=512, d=d, causal=causal, seed=3)
+    x = inputs.make_inputs(w)
+    q, k, v, _ = to_device(x)
+    binding.attn_clear_status()
+    binding.attn_debug_set(timeout_ns=50_000_000, skip_load=True)
+    try:
+        binding.attn_fwd(q, k, v, causal=causal)
+        st, detail = binding.attn_get_status()
+    finally:
+        binding.attn_debug_set(1_000_000_000, False)
+    assert st == binding.ATTN_ERR_TIMEOUT
+    assert detail & 0x40000000
+    binding.attn_clear_status()
+    o, lse = run_cuda(w, x)           # asserts the status is OK again
+    compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_host_entry_point_matches_device_entry_point(dtype):
+    w = inputs.Workload("host", B=1, H=4, Hkv=2, N=384, d=128, causal=True, dtype=dtype, seed=9)
+    x = inputs.make_inputs(w)
+    o_dev, lse_dev = run_cuda(w, x)
+    code = binding.ATTN_DTYPE_FP8_E4M3 if dtype == "fp8_e4m3" else binding.ATTN_DTYPE_BF16
+    ws = torch.empty(binding.attn_fwd_host_workspace_bytes(w.B, w.H, w.Hkv, w.N, w.d, code), dtype=torch.uint8,
+                     device="cuda")
+    o = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16).pin_memory()
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    binding.attn_fwd_host(x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory(), o, lse, w.causal, ws,
+                          descale_q=x.descale_q, descale_k=x.descale_k, descale_v=x.descale_v)
+    assert torch.equal(o, o_dev.cpu()) and torch.equal(lse, lse_dev.cpu())

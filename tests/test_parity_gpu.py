@@ -1,0 +1,105 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs.
+
+Small shapes are compared on every output element; they span several KV tiles, ragged tails
+and all head dims. The full-size workloads are compared on whole sampled heads (every row),
+plus a convex-hull property on every element of every head.
+"""
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_72_gb300 import inputs
+from parity_util import (all_heads, check_convex_hull, compare_heads, oracle_heads, run_cuda)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    from exact_attention_72_gb300 import binding, build
+    build.build()
+    binding.attn_debug_set(timeout_ns=1_000_000_000)   # a correct launch never waits this long
+
+
+def small(name, **kw):
+    base = dict(B=1, H=2, Hkv=2, N=256, d=64, causal=False, seed=77)
+    base.update(kw)
+    return inputs.Workload(name, **base)
+
+
+SMALL = [
+    inputs.WORKLOADS["tiny_bf16_d64"],
+    small("causal_d128_gqa", B=2, H=4, Hkv=2, N=640, d=128, causal=True),
+    small("noncausal_d128", B=1, H=3, Hkv=3, N=512, d=128),
+    small("causal_d64", B=1, H=2, Hkv=1, N=768, d=64, causal=True),
+    small("noncausal_d256", B=1, H=2, Hkv=2, N=384, d=256),
+    small("causal_d256", B=1, H=2, Hkv=1, N=512, d=256, causal=True),
+    small("outliers_causal", B=1, H=4, Hkv=1, N=512, d=128, causal=True, k_outlier_frac=0.005),
+    small("fp8_noncausal", B=1, H=2, Hkv=2, N=512, d=128, dtype="fp8_e4m3"),
+    small("fp8_causal", B=1, H=2, Hkv=1, N=640, d=128, causal=True, dtype="fp8_e4m3"),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_full_parity(w):
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
+
+
+RAGGED_N = [1, 7, 100, 127, 128, 129, 255, 257, 300, 513]
+
+
+@pytest.mark.parametrize("N", RAGGED_N)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_ragged_lengths(N, causal, d):
+    w = small(f"ragged_{N}_{d}_{int(causal)}", B=2, H=2, Hkv=1, N=N, d=d, causal=causal, seed=N * 7 + d)
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
+
+
+@pytest.mark.parametrize("N", [1, 129, 300])
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_lengths_fp8(N, causal):
+    w = small(f"ragged_fp8_{N}", B=1, H=2, Hkv=2, N=N, d=128, causal=causal, dtype="fp8_e4m3", seed=N)
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
+
+
+def test_many_tiles_persistent_loop():
+    """More work tiles than SMs, so each CTA walks several tiles (phase bookkeeping)."""
+    w = small("persistent", B=3, H=40, Hkv=10, N=512, d=128, causal=True, seed=5)
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    heads = [(0, 0), (1, 17), (2, 39), (2, 3), (0, 38)]
+    compare_heads(w, o, lse, oracle_heads(w, x, heads))
+    check_convex_hull(w, x, o)
+
+
+def test_repeatable_bitwise():
+    w = SMALL[1]
+    x = inputs.make_inputs(w)
+    o1, l1 = run_cuda(w, x)
+    o2, l2 = run_cuda(w, x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+FULL = list(inputs.WORKLOADS.values())
+
+
+def sample_heads(w):
+    hs = {(0, 0), (w.B - 1, w.H - 1), (0, w.H // 2), (w.B - 1, min(w.H - 1, w.H // w.Hkv))}
+    return sorted(hs)
+
+
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_full_size_sampled_heads(w):
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    heads = sample_heads(w)
+    stats = compare_heads(w, o, lse, oracle_heads(w, x, heads))
+    check_convex_hull(w, x, o)
+    print(w.name, stats)
