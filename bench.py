@@ -44,6 +44,7 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="name from exact_attention_72_gb300.inputs.WORKLOADS")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiling)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time box")
@@ -386,6 +387,8 @@ def main(argv=None):
     args = parse_args(argv)
     from exact_attention_72_gb300 import inputs
     w = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    if args.batch is not None:
+        w = w.replace(B=args.batch, name=f"{w.name}_b{args.batch}")
     rank, world, _ = rank_info()
     if args.impl == "reference" and rank != 0:
         return 0

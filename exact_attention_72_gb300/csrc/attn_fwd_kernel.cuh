@@ -91,7 +91,7 @@ struct AttnCfg {
 
 // Wait-site codes recorded in the status word when a bounded wait gives up.
 enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
-                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8 };
+                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9 };
 
 struct TileCoord {
   int b, h, mb;
@@ -150,7 +150,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain;
   __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_kv_empty[C::NS];
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[C::NQ], bar_o_done[C::NQ];
+  // o_done: one phase per PV product (rescale waits); o_full: one phase per work tile, after its
+  // last PV (epilogue waits). With one Q tile the S MMAs run a step ahead of the PVs, so at the
+  // epilogue o_done can lag two phases and a parity wait on it would be ambiguous.
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[C::NQ], bar_o_done[C::NQ], bar_o_full[C::NQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
 
@@ -175,6 +178,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int i = 0; i < C::NQ; ++i) {
       mbar_init(smem_addr(&bar_p_full[i]), 128);
       mbar_init(smem_addr(&bar_o_done[i]), 1);
+      mbar_init(smem_addr(&bar_o_full[i]), 1);
     }
     fence_mbar_init();
   }
@@ -278,7 +282,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         tc_commit(smem_addr(&bar_s_full[s_buf_idx(qt, j)]));
       };
-      auto issue_pv = [&](int qt, int j, uint32_t v_slot) {
+      auto issue_pv = [&](int qt, int j, uint32_t v_slot, bool last) {
         const uint32_t d_tmem = tmem + C::O_COL + qt * C::D;
         const uint32_t a_tmem = tmem + s_buf_col(qt, j);
         const uint32_t b0 = sKV + v_slot * C::TILE_BYTES;
@@ -288,6 +292,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    make_sdesc_sw128(b0 + kk * C::PV_ROWS * 128, C::CHUNK_BYTES, 1024), C::IDESC_PV,
                                    j > 0 || kk > 0);
         tc_commit(smem_addr(&bar_o_done[qt]));
+        if (last) tc_commit(smem_addr(&bar_o_full[qt]));
       };
       auto wait_kv = [&](uint32_t pos) -> bool {
         return mbar_wait(smem_addr(&bar_kv_full[pos % C::NS]), (pos / C::NS) & 1, ctl, SITE_KV_FULL);
@@ -331,7 +336,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               if (!mbar_wait(smem_addr(&bar_p_full[qt]), p_cnt[qt] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
               ++p_cnt[qt];
               tc_fence_after();
-              issue_pv(qt, j, pos_v % C::NS);
+              issue_pv(qt, j, pos_v % C::NS, j + 1 == n[qt]);
               if (j + 1 < n[qt]) issue_qk(qt, j + 1, (pos_v + 1) % C::NS);
             }
             if (!ok) break;
@@ -347,7 +352,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!mbar_wait(smem_addr(&bar_p_full[0]), p_cnt[0] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
             ++p_cnt[0];
             tc_fence_after();
-            issue_pv(0, j, pos_v % C::NS);
+            issue_pv(0, j, pos_v % C::NS, j + 1 == nmax);
             tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
             if (j + 2 < nmax) {
               const uint32_t pos_k = base + 2 * (j + 2);
@@ -375,6 +380,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const float out_scale = C::FP8 ? __ldg(p.descale_v) : 1.0f;
     uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
+    uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
     const int n_kv_all = (p.N + C::BN - 1) / C::BN;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
@@ -486,9 +492,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (!ok) break;
       // Epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2.
-      bool w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + n - 1) & 1, ctl, SITE_O_DONE);
+      bool w = mbar_wait(smem_addr(&bar_o_full[qt]), tiles_done & 1, ctl, SITE_O_FULL);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       pv_cnt += n;
+      ++tiles_done;
       tc_fence_after();
       const int row = row0 + r;
       const bool valid = row < p.N;
