@@ -80,7 +80,14 @@ struct AttnCfg {
   static constexpr int O_COL = 256;                       // O tile qt at O_COL + qt * D
   static constexpr int TMEM_COLS = 512;
   static constexpr int WARP_MMA = 4 * NQ, WARP_LOAD = 4 * NQ + 1;
-  static constexpr int THREADS = (4 * NQ + 2) * 32;
+  // Two Q tiles: 12 warps (softmax x8, MMA, load, two idle) so the third warpgroup can hand
+  // registers to the softmax warpgroups with setmaxnreg. The launch gives 384 x 168 = 64,512
+  // registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The host checks the
+  // compiled register count before launching (an over-subscribed increase would never return).
+  static constexpr bool REG_SPLIT = (NQ == 2);
+  static constexpr int THREADS = REG_SPLIT ? 384 : (4 * NQ + 2) * 32;
+  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_OTHER = 96;
+  static constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
   static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, 128, BN, false, false);
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, 128, D, false, true);
@@ -143,6 +150,47 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
+// TMEM column of the S buffer S_j of Q tile qt uses (two Q tiles: one buffer each; one Q tile:
+// the two buffers alternate).
+template <class C>
+__device__ __forceinline__ uint32_t s_buf_col(int qt, int j) {
+  return (C::NQ == 2 ? qt : (j & 1)) ? (uint32_t)C::S_COL1 : (uint32_t)C::S_COL0;
+}
+template <class C>
+__device__ __forceinline__ int s_buf_idx(int qt, int j) {
+  return C::NQ == 2 ? qt : (j & 1);
+}
+
+// S = Q K^T for one 128 x 128 tile: KSTEPS_QK MMAs, each reading 32 bytes of every Q and K row.
+// Descriptors are built once; a k-step only adds its byte offset (>> 4) to the start-address
+// field, which cannot carry out because every shared-memory address is below 2^18.
+template <class C>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+  const uint64_t a0 = make_sdesc_sw128(a_addr, 16, 1024);
+  const uint64_t b0 = make_sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
+    const uint64_t off = (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+    mma_f16_or_f8<C::FP8>(d_tmem, a0 + off, b0 + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Half H of O += P V: the k-steps covering keys [64 H, 64 H + 64) of the tile. P comes from
+// TMEM (8 columns per k-step), V from shared memory (MN-major, PV_ROWS rows per k-step).
+template <class C, int H>
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr,
+                                              bool accumulate_first) {
+  constexpr int KH = C::KSTEPS_PV / 2;
+  const uint64_t b0 = make_sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+#pragma unroll
+  for (int i = 0; i < KH; ++i) {
+    const int kk = H * KH + i;
+    const uint32_t acc = (H > 0 || i > 0) ? 1u : (accumulate_first ? 1u : 0u);
+    mma_ts_f16_or_f8<C::FP8>(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4),
+                             C::IDESC_PV, acc);
+  }
+}
+
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -153,7 +201,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // o_done: one phase per PV product (rescale waits); o_full: one phase per work tile, after its
   // last PV (epilogue waits). With one Q tile the S MMAs run a step ahead of the PVs, so at the
   // epilogue o_done can lag two phases and a parity wait on it would be ambiguous.
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_full[C::NQ], bar_o_done[C::NQ], bar_o_full[C::NQ];
+  // p_half[b][h]: the softmax has written half h of P (keys 64h .. 64h+63) into S buffer b.
+  // One pair per S buffer: with one Q tile the softmax may run a step ahead of the MMA warp,
+  // and per-buffer barriers keep each barrier within one phase of its waiter (a buffer is
+  // reused only after the PV that read it has been issued).
+  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_half[2][2], bar_o_done[C::NQ], bar_o_full[C::NQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
 
@@ -174,9 +226,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_addr(&bar_kv_full[i]), 1);
       mbar_init(smem_addr(&bar_kv_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) mbar_init(smem_addr(&bar_s_full[i]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_addr(&bar_s_full[i]), 1);
+      mbar_init(smem_addr(&bar_p_half[i][0]), 128);
+      mbar_init(smem_addr(&bar_p_half[i][1]), 128);
+    }
     for (int i = 0; i < C::NQ; ++i) {
-      mbar_init(smem_addr(&bar_p_full[i]), 128);
       mbar_init(smem_addr(&bar_o_done[i]), 1);
       mbar_init(smem_addr(&bar_o_full[i]), 1);
     }
@@ -193,6 +248,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
   if (warp == C::WARP_LOAD) {
     // ------------------------------------------------------------------ TMA producer
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -260,42 +316,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
   } else if (warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ tcgen05 issuer
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       uint32_t ring = 0;        // K/V ring position (same sequence as the producer)
       uint32_t nq_loads = 0;
-      uint32_t p_cnt[C::NQ];    // P tiles consumed per Q tile
-      for (int qt = 0; qt < C::NQ; ++qt) p_cnt[qt] = 0;
+      uint32_t p_cnt[2] = {0u, 0u};   // P tiles consumed per S buffer
       bool ok = true;
-      auto s_buf_col = [](int qt, int j) -> uint32_t {
-        return (C::NQ == 2 ? qt : (j & 1)) ? (uint32_t)C::S_COL1 : (uint32_t)C::S_COL0;
-      };
-      auto s_buf_idx = [](int qt, int j) -> int { return C::NQ == 2 ? qt : (j & 1); };
-      auto issue_qk = [&](int qt, int j, uint32_t k_slot) {
-        const uint32_t d_tmem = tmem + s_buf_col(qt, j);
-        const uint32_t a0 = sQ + qt * C::TILE_BYTES;
-        const uint32_t b0 = sKV + k_slot * C::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          mma_f16_or_f8<C::FP8>(d_tmem, make_sdesc_sw128(a0 + off, 16, 1024), make_sdesc_sw128(b0 + off, 16, 1024),
-                                C::IDESC_QK, kk > 0);
-        }
-        tc_commit(smem_addr(&bar_s_full[s_buf_idx(qt, j)]));
-      };
-      auto issue_pv = [&](int qt, int j, uint32_t v_slot, bool last) {
-        const uint32_t d_tmem = tmem + C::O_COL + qt * C::D;
-        const uint32_t a_tmem = tmem + s_buf_col(qt, j);
-        const uint32_t b0 = sKV + v_slot * C::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < C::KSTEPS_PV; ++kk)
-          mma_ts_f16_or_f8<C::FP8>(d_tmem, a_tmem + kk * 8,
-                                   make_sdesc_sw128(b0 + kk * C::PV_ROWS * 128, C::CHUNK_BYTES, 1024), C::IDESC_PV,
-                                   j > 0 || kk > 0);
-        tc_commit(smem_addr(&bar_o_done[qt]));
-        if (last) tc_commit(smem_addr(&bar_o_full[qt]));
-      };
       auto wait_kv = [&](uint32_t pos) -> bool {
         return mbar_wait(smem_addr(&bar_kv_full[pos % C::NS]), (pos / C::NS) & 1, ctl, SITE_KV_FULL);
+      };
+      // S_j of Q tile qt into its S buffer, then signal the softmax.
+      auto qk = [&](int qt, int j, uint32_t k_slot) {
+        issue_qk<C>(tmem + s_buf_col<C>(qt, j), sQ + qt * C::TILE_BYTES, sKV + k_slot * C::TILE_BYTES);
+        tc_commit(smem_addr(&bar_s_full[s_buf_idx<C>(qt, j)]));
+      };
+      // O_qt += P_j V_j, issued in two halves as the softmax hands P over.
+      auto pv = [&](int qt, int j, uint32_t v_slot, bool last) -> bool {
+        const uint32_t d_tmem = tmem + C::O_COL + qt * C::D;
+        const uint32_t a_tmem = tmem + s_buf_col<C>(qt, j);
+        const uint32_t b_addr = sKV + v_slot * C::TILE_BYTES;
+        const int buf = s_buf_idx<C>(qt, j);
+        const uint32_t par = p_cnt[buf] & 1;
+        if (!mbar_wait(smem_addr(&bar_p_half[buf][0]), par, ctl, SITE_P_FULL)) return false;
+        tc_fence_after();
+        issue_pv_half<C, 0>(d_tmem, a_tmem, b_addr, j > 0);
+        if (!mbar_wait(smem_addr(&bar_p_half[buf][1]), par, ctl, SITE_P_FULL)) return false;
+        tc_fence_after();
+        issue_pv_half<C, 1>(d_tmem, a_tmem, b_addr, true);
+        tc_commit(smem_addr(&bar_o_done[qt]));
+        if (last) tc_commit(smem_addr(&bar_o_full[qt]));
+        ++p_cnt[buf];
+        return true;
       };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
@@ -306,13 +357,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
         ++nq_loads;
-        tc_fence_after();
         const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
         // Prologue: S_0 for every Q tile.
         if (!wait_kv(base)) { ok = false; break; }
         tc_fence_after();
         for (int qt = 0; qt < C::NQ; ++qt)
-          if (n[qt] > 0) issue_qk(qt, 0, base % C::NS);
+          if (n[qt] > 0) qk(qt, 0, base % C::NS);
         // Release K_0 before waiting for anything else: with a two-stage ring the producer
         // needs this slot back to load K_1.
         tc_commit(smem_addr(&bar_kv_empty[base % C::NS]));
@@ -320,45 +370,44 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           // One Q tile: the second S buffer lets S_1 run while the softmax works on S_0.
           if (!wait_kv(base + 2)) { ok = false; break; }
           tc_fence_after();
-          issue_qk(0, 1, (base + 2) % C::NS);
+          qk(0, 1, (base + 2) % C::NS);
           tc_commit(smem_addr(&bar_kv_empty[(base + 2) % C::NS]));
         }
         if (nmax == 1 || (C::NQ == 1 && nmax == 2)) tc_commit(smem_addr(&bar_q_empty));
         for (int j = 0; ok && j < nmax; ++j) {
           const uint32_t pos_v = base + 2 * j + 1;
           if (!wait_kv(pos_v)) { ok = false; break; }
+          tc_fence_after();
           if (C::NQ == 2) {
-            const bool more = j + 1 < nmax;
-            if (more && !wait_kv(pos_v + 1)) { ok = false; break; }
-            tc_fence_after();
+            bool k_ready = false;
             for (int qt = 0; qt < C::NQ; ++qt) {
               if (j >= n[qt]) continue;
-              if (!mbar_wait(smem_addr(&bar_p_full[qt]), p_cnt[qt] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
-              ++p_cnt[qt];
-              tc_fence_after();
-              issue_pv(qt, j, pos_v % C::NS, j + 1 == n[qt]);
-              if (j + 1 < n[qt]) issue_qk(qt, j + 1, (pos_v + 1) % C::NS);
+              if (!pv(qt, j, pos_v % C::NS, j + 1 == n[qt])) { ok = false; break; }
+              if (j + 1 < n[qt]) {
+                if (!k_ready) {
+                  if (!wait_kv(pos_v + 1)) { ok = false; break; }
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                qk(qt, j + 1, (pos_v + 1) % C::NS);
+              }
             }
             if (!ok) break;
             tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
-            if (more) {
+            if (j + 1 < nmax) {
               tc_commit(smem_addr(&bar_kv_empty[(pos_v + 1) % C::NS]));
               if (j + 2 == nmax) tc_commit(smem_addr(&bar_q_empty));
             }
           } else {
             // One Q tile: S_{j+1} was issued a step ahead; issue S_{j+2} into the buffer P_j frees
             // once PV_j has been issued (the tensor core runs them in issue order).
-            tc_fence_after();
-            if (!mbar_wait(smem_addr(&bar_p_full[0]), p_cnt[0] & 1, ctl, SITE_P_FULL)) { ok = false; break; }
-            ++p_cnt[0];
-            tc_fence_after();
-            issue_pv(0, j, pos_v % C::NS, j + 1 == nmax);
+            if (!pv(0, j, pos_v % C::NS, j + 1 == nmax)) { ok = false; break; }
             tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
             if (j + 2 < nmax) {
               const uint32_t pos_k = base + 2 * (j + 2);
               if (!wait_kv(pos_k)) { ok = false; break; }
               tc_fence_after();
-              issue_qk(0, j + 2, pos_k % C::NS);
+              qk(0, j + 2, pos_k % C::NS);
               tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
               if (j + 3 == nmax) tc_commit(smem_addr(&bar_q_empty));
             }
@@ -371,8 +420,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else {
+  } else if (warp < 4 * C::NQ) {
     // ------------------------------------------------------------------ softmax + epilogue
+    if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::REGS_SOFTMAX>();
     const int qt = warp >> 2;                  // Q tile of this warpgroup
     const int r = ((warp & 3) << 5) + lane;    // row within the Q tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
@@ -421,15 +471,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int c = 0; c < 128; ++c)
             if (c >= lim) x[c] = -INFINITY;
         }
-        float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+        // Row max: eight independent chains of 3-input max.
+        float a8[8];
 #pragma unroll
-        for (int c = 4; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, x[c]);
-          mx1 = fmaxf(mx1, x[c + 1]);
-          mx2 = fmaxf(mx2, x[c + 2]);
-          mx3 = fmaxf(mx3, x[c + 3]);
-        }
-        const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * s;
+        for (int i = 0; i < 8; ++i) a8[i] = x[i];
+#pragma unroll
+        for (int c = 8; c + 16 <= 128; c += 16)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], x[c + i], x[c + 8 + i]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a8[i] = fmaxf(a8[i], x[120 + i]);
+        const float m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
         float alpha = 1.0f;
         bool rescale = false;
         if (m_tile > m + 8.0f) {
@@ -437,40 +489,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m = m_tile;
           rescale = true;
         }
-        const float neg_m = -m;
-        float l0 = 0.f, l1 = 0.f;
-        const uint32_t tP = tS;   // P overwrites the first P_COLS columns of the S buffer
-        if (!C::FP8) {
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 32; c += 2) {
-              const float p0 = ex2(fmaf(x[c0 + c], s, neg_m));
-              const float p1 = ex2(fmaf(x[c0 + c + 1], s, neg_m));
-              l0 += p0;
-              l1 += p1;
-              pk[c >> 1] = pack_bf16x2(p0, p1);
-            }
-            tmem_st_16cols(tP + (c0 >> 1), pk);
-          }
-        } else {
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 128; c += 4) {
-            const float p0 = ex2(fmaf(x[c], s, neg_m));
-            const float p1 = ex2(fmaf(x[c + 1], s, neg_m));
-            const float p2 = ex2(fmaf(x[c + 2], s, neg_m));
-            const float p3 = ex2(fmaf(x[c + 3], s, neg_m));
-            l0 += p0 + p2;
-            l1 += p1 + p3;
-            pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
-          }
-          tmem_st_32cols(tP, pk);
-        }
-        l = l * alpha + (l0 + l1);
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-          // O (held in TMEM) must not be touched while PV_{j-1} is still accumulating into it.
+          // Rescale O before any half of P_j is released: PV_j must accumulate onto the rescaled
+          // O, and O must not be touched while PV_{j-1} is still accumulating into it.
           w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
           if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
           tc_fence_after();
@@ -486,9 +507,52 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_32cols(tO + c0, ov);
           }
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_addr(&bar_p_full[qt]));
+        // P = exp2(s * x - m) in packed fp32 pairs, in two halves of 64 keys; each half is written
+        // to TMEM (over the first columns of the S buffer) and handed to the MMA warp at once.
+        const uint64_t s2 = f2_pack(s, s);
+        const uint64_t nm2 = f2_pack(-m, -m);
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        const uint32_t tP = tS;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!C::FP8) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              const int cc = h * 64 + c;
+              float t0, t1, t2, t3;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
+              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
+              const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+              acc1 = f2_add(acc1, f2_pack(p2, p3));
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+              pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+            }
+            tmem_st_32cols(tP + h * 32, pk);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              const int cc = h * 64 + c;
+              float t0, t1, t2, t3;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
+              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
+              const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+              acc1 = f2_add(acc1, f2_pack(p2, p3));
+              pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+            }
+            tmem_st_16cols(tP + h * 16, pk);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+        }
+        float l0, l1, l2, l3;
+        f2_unpack(acc0, l0, l1);
+        f2_unpack(acc1, l2, l3);
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
       }
       if (!ok) break;
       // Epilogue: O / l -> bf16, LSE = (m + log2 l) * ln 2.
@@ -522,6 +586,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       }
       if (valid) p.lse[((size_t)tc.b * p.H + tc.h) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
     }
+  }
+  else {
+    // Idle warps of the third warpgroup: give their registers back and wait for teardown.
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
   }
 
   __syncwarp();

@@ -11,6 +11,14 @@ cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
   // The attribute is per device; setting it on every call is cheap and keeps this stateless.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
+  if constexpr (C::REG_SPLIT) {
+    // setmaxnreg redistributes the registers the block was launched with; refuse to launch if the
+    // compiled per-thread count leaves less than the split needs.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kernel);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs * C::THREADS < C::REGS_NEEDED) return cudaErrorInvalidConfiguration;
+  }
   const int grid = a.params.n_tiles < a.num_sms ? a.params.n_tiles : a.num_sms;
   kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.params);
   return cudaGetLastError();

@@ -71,7 +71,7 @@ struct WaitCtl {
   uint64_t timeout_ns;
 };
 
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
+static __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const WaitCtl& ctl,
                                             uint32_t site) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
@@ -275,5 +275,47 @@ __device__ __forceinline__ void mma_ts_f16_or_f8(uint32_t d_tmem, uint32_t a_tme
                                                  uint32_t accumulate) {
   if constexpr (FP8) mma_f8_ts(d_tmem, a_tmem, bdesc, idesc, accumulate);
   else mma_f16_ts(d_tmem, a_tmem, bdesc, idesc, accumulate);
+}
+}  // namespace gb300
+
+// ---------------------------------------------------------------------------------------------
+// Packed fp32 pairs (two lanes of one 64-bit register, sm_100 family) and 3-input max
+// ---------------------------------------------------------------------------------------------
+namespace gb300 {
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+// d = a * b + c, element-wise, round to nearest.
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+}  // namespace gb300
+
+namespace gb300 {
+// Warpgroup register reallocation (every warp of the warpgroup executes the same one).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 }  // namespace gb300
