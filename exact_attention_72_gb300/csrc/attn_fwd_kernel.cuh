@@ -79,15 +79,20 @@ struct AttnCfg {
   static constexpr int S_COL0 = 0, S_COL1 = 128;          // two S buffers
   static constexpr int O_COL = 256;                       // O tile qt at O_COL + qt * D
   static constexpr int TMEM_COLS = 512;
-  static constexpr int WARP_MMA = 4 * NQ, WARP_LOAD = 4 * NQ + 1;
-  // Two Q tiles: 12 warps (softmax x8, MMA, load, two idle) so the third warpgroup can hand
+  // Roles: warps [0, 4 NQ) softmax (one warpgroup per Q tile), then one MMA-issuer warp per Q
+  // tile, then the TMA warp. With two Q tiles each tile has its own issuer, so one issuer's
+  // waits for its softmax never hold up the other tile's MMAs.
+  static constexpr int MMA_WARPS = NQ;
+  static constexpr int SOFTMAX_WARPS = 4 * NQ;            // one warpgroup per Q tile
+  static constexpr int WARP_MMA = SOFTMAX_WARPS, WARP_LOAD = SOFTMAX_WARPS + MMA_WARPS;
+  // Two Q tiles: 12 warps (softmax x8, MMA x2, load, one idle) so the third warpgroup can hand
   // registers to the softmax warpgroups with setmaxnreg. The launch gives 384 x 168 = 64,512
   // registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The host checks the
   // compiled register count before launching (an over-subscribed increase would never return).
   static constexpr bool REG_SPLIT = (NQ == 2);
-  static constexpr int THREADS = REG_SPLIT ? 384 : (4 * NQ + 2) * 32;
+  static constexpr int THREADS = REG_SPLIT ? 384 : (SOFTMAX_WARPS + MMA_WARPS + 1) * 32;
   static constexpr uint32_t REGS_SOFTMAX = 200, REGS_OTHER = 96;
-  static constexpr int REGS_NEEDED = 256 * REGS_SOFTMAX + 128 * REGS_OTHER;
+  static constexpr int REGS_NEEDED = SOFTMAX_WARPS * 32 * REGS_SOFTMAX + 128 * REGS_OTHER;
   static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, 128, BN, false, false);
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, 128, D, false, true);
@@ -98,7 +103,7 @@ struct AttnCfg {
 
 // Wait-site codes recorded in the status word when a bounded wait gives up.
 enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
-                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9 };
+                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9, SITE_S_TURN = 10 };
 
 struct TileCoord {
   int b, h, mb;
@@ -132,6 +137,29 @@ __device__ __forceinline__ int kv_tiles_for(int mb, int qt, int N) {
   const int n_kv = (N + C::BN - 1) / C::BN;
   return C::CAUSAL ? (row0 / C::BN + 1) : n_kv;
 }
+
+// Optional event trace for pipeline analysis (off unless compiled with -DGB300_ATTN_TRACE):
+// in CTA 0, each warp's recording lane appends (event, a, b, clock64) to its own 1024-entry slot.
+#ifdef GB300_ATTN_TRACE
+__device__ unsigned long long g_attn_trace[2 * 32 * 1024];
+#define ATTN_TRACE_DECL uint32_t trace_n_ = 0
+#define ATTN_TRACE(ev, a, b)                                                                          \
+  do {                                                                                               \
+    if (blockIdx.x == 0 && trace_n_ < 1024u && (threadIdx.x >> 5) < 32u) {                           \
+      const uint32_t i_ = (threadIdx.x >> 5) * 1024u + trace_n_++;                                   \
+      g_attn_trace[2 * i_] =                                                                         \
+          ((unsigned long long)(ev) << 48) | ((unsigned long long)(a) << 32) | (unsigned int)(b);    \
+      g_attn_trace[2 * i_ + 1] = clock64();                                                          \
+    }                                                                                                \
+  } while (0)
+#else
+#define ATTN_TRACE_DECL \
+  do {                  \
+  } while (0)
+#define ATTN_TRACE(ev, a, b) \
+  do {                       \
+  } while (0)
+#endif
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -196,7 +224,13 @@ __global__ void __launch_bounds__(C::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain;
+  // kv_empty / q_empty take one arrival per MMA-issuer warp (a tcgen05.commit after the MMAs
+  // that read the stage, or a plain arrive for a stage that warp's Q tile does not need).
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain[C::MMA_WARPS];
+  // s_turn[q]: issuer q may take its next S turn. The two issuers alternate S issues
+  // (S0_j, S1_j, S0_{j+1}, ...), which keeps the two Q tiles' softmax phases staggered so the
+  // tensor core always has the other tile's GEMMs to run.
+  __shared__ __align__(8) uint64_t bar_s_turn[2];
   __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_kv_empty[C::NS];
   // o_done: one phase per PV product (rescale waits); o_full: one phase per work tile, after its
   // last PV (epilogue waits). With one Q tile the S MMAs run a step ahead of the PVs, so at the
@@ -220,11 +254,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (tid == 0) {
     abort_flag = 0u;
     mbar_init(smem_addr(&bar_q_full), 1);
-    mbar_init(smem_addr(&bar_q_empty), 1);
-    mbar_init(smem_addr(&bar_drain), 1);
+    mbar_init(smem_addr(&bar_q_empty), C::MMA_WARPS);
+    for (int i = 0; i < C::MMA_WARPS; ++i) mbar_init(smem_addr(&bar_drain[i]), 1);
+    mbar_init(smem_addr(&bar_s_turn[0]), 1);
+    mbar_init(smem_addr(&bar_s_turn[1]), 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(smem_addr(&bar_kv_full[i]), 1);
-      mbar_init(smem_addr(&bar_kv_empty[i]), 1);
+      mbar_init(smem_addr(&bar_kv_empty[i]), C::MMA_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_addr(&bar_s_full[i]), 1);
@@ -236,6 +272,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       mbar_init(smem_addr(&bar_o_full[i]), 1);
     }
     fence_mbar_init();
+    mbar_arrive(smem_addr(&bar_s_turn[0]));   // issuer 0 takes the first S turn
   }
   if (warp == C::WARP_MMA) {
     tmem_alloc(smem_addr(&tmem_slot), C::TMEM_COLS);
@@ -245,6 +282,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  ATTN_TRACE_DECL;
 
   if (warp == C::WARP_LOAD) {
     // ------------------------------------------------------------------ TMA producer
@@ -314,8 +352,90 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
       }
     }
-  } else if (warp == C::WARP_MMA) {
-    // ------------------------------------------------------------------ tcgen05 issuer
+  } else if (C::NQ == 2 && warp >= C::WARP_MMA && warp < C::WARP_MMA + C::MMA_WARPS) {
+    // ------------------------------------------------------------------ tcgen05 issuer, one per Q tile
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
+    if (lane == 0) {
+      const int myq = warp - C::WARP_MMA;   // Q tile (and S/P buffer) this warp issues for
+      uint32_t ring = 0, nq_loads = 0, p_cnt = 0, turns = 0;
+      bool ok = true;
+
+      auto wait_kv = [&](uint32_t pos) -> bool {
+        return mbar_wait(smem_addr(&bar_kv_full[pos % C::NS]), (pos / C::NS) & 1, ctl, SITE_KV_FULL);
+      };
+      // Release a ring stage: after this warp's MMAs that read it, or at once if none did.
+      auto release = [&](uint64_t* bar, bool used) {
+        if (used) tc_commit(smem_addr(bar));
+        else mbar_arrive(smem_addr(bar));
+      };
+      const uint32_t d_s = tmem + (myq ? C::S_COL1 : C::S_COL0);
+      const uint32_t d_o = tmem + C::O_COL + myq * C::D;
+      const uint32_t a_q = sQ + myq * C::TILE_BYTES;
+      // One S turn: wait for this issuer's turn, issue S (if this Q tile needs it), pass the turn.
+      auto s_turn = [&](bool issue, uint32_t k_addr) -> bool {
+        if (!mbar_wait(smem_addr(&bar_s_turn[myq]), turns & 1, ctl, SITE_S_TURN)) return false;
+        ++turns;
+        if (issue) {
+          tc_fence_after();
+          issue_qk<C>(d_s, a_q, k_addr);
+          tc_commit(smem_addr(&bar_s_full[myq]));
+        }
+        mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
+        return true;
+      };
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
+        const int n = kv_tiles_for<C>(tc.mb, myq, p.N);
+        int nmax = 0;
+        for (int qt = 0; qt < C::NQ; ++qt) {
+          const int nq = kv_tiles_for<C>(tc.mb, qt, p.N);
+          nmax = nq > nmax ? nq : nmax;
+        }
+        if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
+        ++nq_loads;
+        const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
+        if (!wait_kv(base)) { ok = false; break; }
+        if (!s_turn(n > 0, sKV + (base % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+        release(&bar_kv_empty[base % C::NS], n > 0);
+        if (nmax == 1) release(&bar_q_empty, n > 0);
+        for (int j = 0; ok && j < nmax; ++j) {
+          const uint32_t pos_v = base + 2 * j + 1;
+          if (!wait_kv(pos_v)) { ok = false; break; }
+          ATTN_TRACE(15, myq, j);
+          if (j < n) {
+            const uint32_t par = p_cnt & 1;
+            const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
+            if (!mbar_wait(smem_addr(&bar_p_half[myq][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+            ATTN_TRACE(1, myq, j);
+            tc_fence_after();
+            issue_pv_half<C, 0>(d_o, d_s, b_v, j > 0);
+            if (!mbar_wait(smem_addr(&bar_p_half[myq][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+            ATTN_TRACE(3, myq, j);
+            tc_fence_after();
+            issue_pv_half<C, 1>(d_o, d_s, b_v, true);
+            ATTN_TRACE(13, myq, j);
+            ++p_cnt;
+            if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
+          }
+          release(&bar_kv_empty[pos_v % C::NS], j < n);
+          if (j + 1 < nmax) {
+            const uint32_t pos_k = pos_v + 1;
+            if (!wait_kv(pos_k)) { ok = false; break; }
+            if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+            ATTN_TRACE(14, myq, j + 1);
+            release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
+            if (j + 2 == nmax) release(&bar_q_empty, n > 0);
+          }
+        }
+        ring = base + 2 * nmax;
+      }
+      // Every MMA this warp issued must finish before TMEM is released.
+      tc_commit(smem_addr(&bar_drain[myq]));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_addr(&bar_drain[myq]), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else if (C::NQ == 1 && warp == C::WARP_MMA) {
+    // ------------------------------------------------------------------ tcgen05 issuer, one Q tile
     if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       uint32_t ring = 0;        // K/V ring position (same sequence as the producer)
@@ -325,17 +445,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       auto wait_kv = [&](uint32_t pos) -> bool {
         return mbar_wait(smem_addr(&bar_kv_full[pos % C::NS]), (pos / C::NS) & 1, ctl, SITE_KV_FULL);
       };
-      // S_j of Q tile qt into its S buffer, then signal the softmax.
-      auto qk = [&](int qt, int j, uint32_t k_slot) {
-        issue_qk<C>(tmem + s_buf_col<C>(qt, j), sQ + qt * C::TILE_BYTES, sKV + k_slot * C::TILE_BYTES);
-        tc_commit(smem_addr(&bar_s_full[s_buf_idx<C>(qt, j)]));
+      // S_j into S buffer j % 2, then signal the softmax.
+      auto qk = [&](int j, uint32_t k_slot) {
+        issue_qk<C>(tmem + s_buf_col<C>(0, j), sQ, sKV + k_slot * C::TILE_BYTES);
+        tc_commit(smem_addr(&bar_s_full[s_buf_idx<C>(0, j)]));
       };
-      // O_qt += P_j V_j, issued in two halves as the softmax hands P over.
-      auto pv = [&](int qt, int j, uint32_t v_slot, bool last) -> bool {
-        const uint32_t d_tmem = tmem + C::O_COL + qt * C::D;
-        const uint32_t a_tmem = tmem + s_buf_col<C>(qt, j);
+      // O += P_j V_j, issued in two halves as the softmax hands P over.
+      auto pv = [&](int j, uint32_t v_slot, bool last) -> bool {
+        const uint32_t d_tmem = tmem + C::O_COL;
+        const uint32_t a_tmem = tmem + s_buf_col<C>(0, j);
         const uint32_t b_addr = sKV + v_slot * C::TILE_BYTES;
-        const int buf = s_buf_idx<C>(qt, j);
+        const int buf = s_buf_idx<C>(0, j);
         const uint32_t par = p_cnt[buf] & 1;
         if (!mbar_wait(smem_addr(&bar_p_half[buf][0]), par, ctl, SITE_P_FULL)) return false;
         tc_fence_after();
@@ -343,84 +463,56 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (!mbar_wait(smem_addr(&bar_p_half[buf][1]), par, ctl, SITE_P_FULL)) return false;
         tc_fence_after();
         issue_pv_half<C, 1>(d_tmem, a_tmem, b_addr, true);
-        tc_commit(smem_addr(&bar_o_done[qt]));
-        if (last) tc_commit(smem_addr(&bar_o_full[qt]));
+        tc_commit(smem_addr(&bar_o_done[0]));
+        if (last) tc_commit(smem_addr(&bar_o_full[0]));
         ++p_cnt[buf];
         return true;
       };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
-        int n[C::NQ], nmax = 0;
-        for (int qt = 0; qt < C::NQ; ++qt) {
-          n[qt] = kv_tiles_for<C>(tc.mb, qt, p.N);
-          nmax = n[qt] > nmax ? n[qt] : nmax;
-        }
+        const int nmax = kv_tiles_for<C>(tc.mb, 0, p.N);
         if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
         ++nq_loads;
         const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
-        // Prologue: S_0 for every Q tile.
         if (!wait_kv(base)) { ok = false; break; }
         tc_fence_after();
-        for (int qt = 0; qt < C::NQ; ++qt)
-          if (n[qt] > 0) qk(qt, 0, base % C::NS);
+        qk(0, base % C::NS);
         // Release K_0 before waiting for anything else: with a two-stage ring the producer
         // needs this slot back to load K_1.
         tc_commit(smem_addr(&bar_kv_empty[base % C::NS]));
-        if (C::NQ == 1 && nmax > 1) {
-          // One Q tile: the second S buffer lets S_1 run while the softmax works on S_0.
+        if (nmax > 1) {
+          // The second S buffer lets S_1 run while the softmax works on S_0.
           if (!wait_kv(base + 2)) { ok = false; break; }
           tc_fence_after();
-          qk(0, 1, (base + 2) % C::NS);
+          qk(1, (base + 2) % C::NS);
           tc_commit(smem_addr(&bar_kv_empty[(base + 2) % C::NS]));
         }
-        if (nmax == 1 || (C::NQ == 1 && nmax == 2)) tc_commit(smem_addr(&bar_q_empty));
+        if (nmax <= 2) tc_commit(smem_addr(&bar_q_empty));
         for (int j = 0; ok && j < nmax; ++j) {
           const uint32_t pos_v = base + 2 * j + 1;
           if (!wait_kv(pos_v)) { ok = false; break; }
           tc_fence_after();
-          if (C::NQ == 2) {
-            bool k_ready = false;
-            for (int qt = 0; qt < C::NQ; ++qt) {
-              if (j >= n[qt]) continue;
-              if (!pv(qt, j, pos_v % C::NS, j + 1 == n[qt])) { ok = false; break; }
-              if (j + 1 < n[qt]) {
-                if (!k_ready) {
-                  if (!wait_kv(pos_v + 1)) { ok = false; break; }
-                  tc_fence_after();
-                  k_ready = true;
-                }
-                qk(qt, j + 1, (pos_v + 1) % C::NS);
-              }
-            }
-            if (!ok) break;
-            tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
-            if (j + 1 < nmax) {
-              tc_commit(smem_addr(&bar_kv_empty[(pos_v + 1) % C::NS]));
-              if (j + 2 == nmax) tc_commit(smem_addr(&bar_q_empty));
-            }
-          } else {
-            // One Q tile: S_{j+1} was issued a step ahead; issue S_{j+2} into the buffer P_j frees
-            // once PV_j has been issued (the tensor core runs them in issue order).
-            if (!pv(0, j, pos_v % C::NS, j + 1 == nmax)) { ok = false; break; }
-            tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
-            if (j + 2 < nmax) {
-              const uint32_t pos_k = base + 2 * (j + 2);
-              if (!wait_kv(pos_k)) { ok = false; break; }
-              tc_fence_after();
-              qk(0, j + 2, pos_k % C::NS);
-              tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
-              if (j + 3 == nmax) tc_commit(smem_addr(&bar_q_empty));
-            }
+          // S_{j+1} was issued a step ahead; issue S_{j+2} into the buffer P_j frees once PV_j
+          // has been issued (one thread's MMAs run in issue order).
+          if (!pv(j, pos_v % C::NS, j + 1 == nmax)) { ok = false; break; }
+          tc_commit(smem_addr(&bar_kv_empty[pos_v % C::NS]));
+          if (j + 2 < nmax) {
+            const uint32_t pos_k = base + 2 * (j + 2);
+            if (!wait_kv(pos_k)) { ok = false; break; }
+            tc_fence_after();
+            qk(j + 2, pos_k % C::NS);
+            tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
+            if (j + 3 == nmax) tc_commit(smem_addr(&bar_q_empty));
           }
         }
         ring = base + 2 * nmax;
       }
       // Every MMA issued so far must finish before TMEM is released.
-      tc_commit(smem_addr(&bar_drain));
+      tc_commit(smem_addr(&bar_drain[0]));
       const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+      while (!mbar_try_wait(smem_addr(&bar_drain[0]), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else if (warp < 4 * C::NQ) {
+  } else if (warp < C::SOFTMAX_WARPS) {
     // ------------------------------------------------------------------ softmax + epilogue
     if constexpr (C::REG_SPLIT) setmaxnreg_inc<C::REGS_SOFTMAX>();
     const int qt = warp >> 2;                  // Q tile of this warpgroup
@@ -445,6 +537,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t s_col = buf ? C::S_COL1 : C::S_COL0;
         bool w = mbar_wait(smem_addr(&bar_s_full[buf]), s_cnt[buf] & 1, ctl, SITE_S_FULL);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        if (r == 0) ATTN_TRACE(4, qt, j);
         ++s_cnt[buf];
         tc_fence_after();
         uint32_t sr[128];
@@ -458,6 +551,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         reg_fence32(sr + 32);
         reg_fence32(sr + 64);
         reg_fence32(sr + 96);
+        if (r == 0) ATTN_TRACE(5, qt, j);
         float x[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
@@ -482,6 +576,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int i = 0; i < 8; ++i) a8[i] = fmaxf(a8[i], x[120 + i]);
         const float m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
+        if (r == 0) ATTN_TRACE(6, qt, j);
         float alpha = 1.0f;
         bool rescale = false;
         if (m_tile > m + 8.0f) {
@@ -492,8 +587,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
           // Rescale O before any half of P_j is released: PV_j must accumulate onto the rescaled
           // O, and O must not be touched while PV_{j-1} is still accumulating into it.
-          w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
-          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          // Two Q tiles: S_j's commit already covered PV_{j-1} (same issuing thread), so O is
+          // settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV.
+          if constexpr (C::NQ == 1) {
+            w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          }
           tc_fence_after();
           const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
 #pragma unroll 1
@@ -548,6 +647,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+          if (r == 0) ATTN_TRACE(7 + h, qt, j);
         }
         float l0, l1, l2, l3;
         f2_unpack(acc0, l0, l1);
