@@ -565,6 +565,42 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int c = 0; c < 128; ++c)
             if (c >= lim) x[c] = -INFINITY;
         }
+        // P = exp2(s * x - m) in packed fp32 pairs, in two halves of 64 keys; each half is written
+        // to TMEM (over the first columns of the S buffer) and handed to the MMA warp at once.
+        // The first half is computed speculatively with the row's current shift m while the row
+        // max of this tile is taken alongside it; only if some row's max moved by more than 8
+        // (always on the first tile) is that half recomputed with the new shift.
+        const uint64_t s2 = f2_pack(s, s);
+        constexpr int PKN = C::FP8 ? 16 : 32;   // packed 32-bit P words per half
+        auto exp_half = [&](int h, uint64_t nm2, uint32_t* pk, uint64_t& acc0, uint64_t& acc1) {
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const int cc = h * 64 + c;
+            float t0, t1, t2, t3;
+            f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
+            f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
+            const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+            acc0 = f2_add(acc0, f2_pack(p0, p1));
+            acc1 = f2_add(acc1, f2_pack(p2, p3));
+            if (C::FP8) {
+              pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
+            } else {
+              pk[c >> 1] = pack_bf16x2(p0, p1);
+              pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+            }
+          }
+        };
+        auto store_half = [&](int h, const uint32_t* pk) {
+          if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
+          else tmem_st_32cols(tS + h * 32, pk);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+          if (r == 0) ATTN_TRACE(7 + h, qt, j);
+        };
+        uint32_t pk[PKN];
+        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+        exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
         // Row max: eight independent chains of 3-input max.
         float a8[8];
 #pragma unroll
@@ -584,71 +620,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m = m_tile;
           rescale = true;
         }
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-          // Rescale O before any half of P_j is released: PV_j must accumulate onto the rescaled
-          // O, and O must not be touched while PV_{j-1} is still accumulating into it.
-          // Two Q tiles: S_j's commit already covered PV_{j-1} (same issuing thread), so O is
-          // settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV.
-          if constexpr (C::NQ == 1) {
-            w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-          }
-          tc_fence_after();
-          const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
+        if (__any_sync(0xffffffffu, rescale)) {
+          if (j > 0) {
+            // Rescale O before any half of P_j is released: PV_j must accumulate onto the
+            // rescaled O, and O must not be touched while PV_{j-1} is still accumulating into
+            // it. Two Q tiles: S_j's commit already covered PV_{j-1} (same issuing thread), so O
+            // is settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV.
+            if constexpr (C::NQ == 1) {
+              w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            }
+            tc_fence_after();
+            const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
 #pragma unroll 1
-          for (int c0 = 0; c0 < C::D; c0 += 32) {
-            uint32_t ov[32];
-            tmem_ld_32cols(tO + c0, ov);
-            tmem_ld_wait();
-            reg_fence32(ov);
+            for (int c0 = 0; c0 < C::D; c0 += 32) {
+              uint32_t ov[32];
+              tmem_ld_32cols(tO + c0, ov);
+              tmem_ld_wait();
+              reg_fence32(ov);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
-            tmem_st_32cols(tO + c0, ov);
-          }
-        }
-        // P = exp2(s * x - m) in packed fp32 pairs, in two halves of 64 keys; each half is written
-        // to TMEM (over the first columns of the S buffer) and handed to the MMA warp at once.
-        const uint64_t s2 = f2_pack(s, s);
-        const uint64_t nm2 = f2_pack(-m, -m);
-        uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
-        const uint32_t tP = tS;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!C::FP8) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const int cc = h * 64 + c;
-              float t0, t1, t2, t3;
-              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
-              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
-              const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-              acc0 = f2_add(acc0, f2_pack(p0, p1));
-              acc1 = f2_add(acc1, f2_pack(p2, p3));
-              pk[c >> 1] = pack_bf16x2(p0, p1);
-              pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
+              for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+              tmem_st_32cols(tO + c0, ov);
             }
-            tmem_st_32cols(tP + h * 32, pk);
-          } else {
-            uint32_t pk[16];
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-              const int cc = h * 64 + c;
-              float t0, t1, t2, t3;
-              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
-              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
-              const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-              acc0 = f2_add(acc0, f2_pack(p0, p1));
-              acc1 = f2_add(acc1, f2_pack(p2, p3));
-              pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
-            }
-            tmem_st_16cols(tP + h * 16, pk);
           }
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(smem_addr(&bar_p_half[buf][h]));
-          if (r == 0) ATTN_TRACE(7 + h, qt, j);
+          // The speculative half used the old shift: redo it with the new one.
+          acc0 = f2_pack(0.f, 0.f);
+          acc1 = acc0;
+          exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
         }
+        store_half(0, pk);
+        exp_half(1, f2_pack(-m, -m), pk, acc0, acc1);
+        store_half(1, pk);
         float l0, l1, l2, l3;
         f2_unpack(acc0, l0, l1);
         f2_unpack(acc1, l2, l3);
