@@ -220,7 +220,7 @@ def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
         steps += 1
     desc = (f"{steps} blocks of {block_rows} query rows (full score rows, fp64) from heads of the "
             f"{w.name} workload; FLOPs credited by the metric's convention")
-    return flops / elapsed / 1e12, desc, elapsed, steps
+    return (flops / elapsed / 1e12 if elapsed > 0 else 0.0), desc, elapsed, steps
 
 
 def cores_used() -> int:
@@ -237,7 +237,8 @@ def run_reference(args, w, x):
         return
     block = 256
     # warm-up steps (untimed), then K timed steps, each one oracle row block
-    cpu_oracle_sample(w, x, seconds=1e9, block_rows=block, max_steps=args.warmup)
+    if args.warmup > 0:
+        cpu_oracle_sample(w, x, seconds=1e9, block_rows=block, max_steps=args.warmup)
     tflops, desc, secs, steps = cpu_oracle_sample(w, x, seconds=1e9, block_rows=block, max_steps=args.steps)
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
