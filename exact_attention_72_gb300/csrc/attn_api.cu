@@ -1,5 +1,6 @@
 // C ABI of the attention forward library: argument checks, tensor-map encoding, dispatch to
 // the kernel instance for (head dim, causal, dtype), device status word, host-buffer variant.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -15,6 +16,8 @@
 static __device__ uint32_t g_attn_status;
 
 namespace {
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr unsigned long long kDefaultTimeoutNs = 4000000000ull;
 constexpr int kMaxDevices = 64;
@@ -40,11 +43,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+constexpr int kMaxChunks = 8;
+
 struct DeviceInfo {
   std::once_flag once;
   int num_sms = 0;
   uint32_t* status = nullptr;
   bool ok = false;
+  // Host-buffer pipeline (attn_fwd_host): created once per device on first use.
+  std::once_flag pipe_once;
+  bool pipe_ok = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr, s_comp[2] = {nullptr, nullptr};
+  cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[kMaxChunks] = {}, ev_k[kMaxChunks] = {};
+  std::mutex pipe_mutex;   // one host-buffer call at a time per device (shared streams/events)
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -59,6 +70,65 @@ DeviceInfo* device_info() {
     di->status = static_cast<uint32_t*>(p);
   });
   return di->ok ? di : nullptr;
+}
+
+bool pipeline_ready(DeviceInfo* di) {
+  std::call_once(di->pipe_once, [di] {
+    bool ok = true;
+    ok = ok && cudaStreamCreateWithFlags(&di->s_in, cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaStreamCreateWithFlags(&di->s_out, cudaStreamNonBlocking) == cudaSuccess;
+    for (int i = 0; i < 2; ++i) ok = ok && cudaStreamCreateWithFlags(&di->s_comp[i], cudaStreamNonBlocking) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&di->ev_start, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&di->ev_end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < kMaxChunks; ++i) {
+      ok = ok && cudaEventCreateWithFlags(&di->ev_in[i], cudaEventDisableTiming) == cudaSuccess;
+      ok = ok && cudaEventCreateWithFlags(&di->ev_k[i], cudaEventDisableTiming) == cudaSuccess;
+    }
+    di->pipe_ok = ok;
+  });
+  return di->pipe_ok;
+}
+
+// attn_fwd_host work split: chunks of whole batches (B >= 4) or, for B < 4, one batch and a
+// contiguous range of KV heads (with their query heads), so each chunk is a self-contained
+// attention problem whose copies can overlap another chunk's kernel. At most four chunks.
+struct HostChunk {
+  int b0, nb;      // batches [b0, b0 + nb)
+  int g0, ng;      // kv heads [g0, g0 + ng); query heads [g0 G, (g0 + ng) G)
+  size_t off_q, off_k, off_v, off_o, off_lse;   // workspace offsets
+};
+
+int plan_host_chunks(int B, int H, int Hkv, int N, int d, size_t elt, HostChunk* ch, size_t* total) {
+  const int G = H / Hkv;
+  int nc = 0;
+  auto add = [&](int b0, int nb, int g0, int ng) {
+    HostChunk& c = ch[nc++];
+    c.b0 = b0; c.nb = nb; c.g0 = g0; c.ng = ng;
+    const size_t rows = (size_t)nb * N;
+    size_t off = *total;
+    c.off_q = off;   off += round_up(rows * ng * G * d * elt, 256);
+    c.off_k = off;   off += round_up(rows * ng * d * elt, 256);
+    c.off_v = off;   off += round_up(rows * ng * d * elt, 256);
+    c.off_o = off;   off += round_up(rows * ng * G * d * 2, 256);
+    c.off_lse = off; off += round_up(rows * ng * G * 4, 256);
+    *total = off;
+  };
+  *total = 0;
+  if (B >= 4) {
+    for (int i = 0; i < 4; ++i) {
+      const int b0 = (int)((long long)B * i / 4), b1 = (int)((long long)B * (i + 1) / 4);
+      if (b1 > b0) add(b0, b1 - b0, 0, Hkv);
+    }
+  } else {
+    const int S = std::min(Hkv, (4 + B - 1) / B);
+    for (int b = 0; b < B; ++b)
+      for (int i = 0; i < S; ++i) {
+        const int g0 = (int)((long long)Hkv * i / S), g1 = (int)((long long)Hkv * (i + 1) / S);
+        if (g1 > g0) add(b, 1, g0, g1 - g0);
+      }
+  }
+  *total += 256;   // fp8 descales
+  return nc;
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -113,8 +183,6 @@ cudaError_t dispatch_d(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t
   }
   return causal ? gb300::launch_attn_fwd<D, true, false>(a, s) : gb300::launch_attn_fwd<D, false, false>(a, s);
 }
-
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
@@ -176,10 +244,10 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
 
 size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_dtype_t dtype) {
   if (check_shape(B, H, Hkv, N, d, 1.0f, dtype) != ATTN_OK) return 0;
-  const size_t elt = dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2;
-  const size_t nq = (size_t)B * N * H * d, nkv = (size_t)B * N * Hkv * d;
-  return round_up(nq * elt, 256) + 2 * round_up(nkv * elt, 256) + round_up(nq * 2, 256) +
-         round_up((size_t)B * H * N * 4, 256) + 256;
+  HostChunk ch[kMaxChunks];
+  size_t total = 0;
+  plan_host_chunks(B, H, Hkv, N, d, dtype == ATTN_DTYPE_FP8_E4M3 ? 1 : 2, ch, &total);
+  return total;
 }
 
 attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
@@ -193,31 +261,73 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   if (fp8 && (!descale_q || !descale_k || !descale_v)) return ATTN_ERR_INVALID_ARG;
   if (!aligned(workspace, 256) || workspace_bytes < attn_fwd_host_workspace_bytes(B, H, Hkv, N, d, dtype))
     return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info();
+  if (!di || !pipeline_ready(di)) return ATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(di->pipe_mutex);
   const size_t elt = fp8 ? 1 : 2;
-  const size_t nq = (size_t)B * N * H * d, nkv = (size_t)B * N * Hkv * d;
+  const int G = H / Hkv;
+  HostChunk ch[kMaxChunks];
+  size_t total = 0;
+  const int nc = plan_host_chunks(B, H, Hkv, N, d, elt, ch, &total);
   uint8_t* w = static_cast<uint8_t*>(workspace);
-  uint8_t* dq = w;
-  uint8_t* dk = dq + round_up(nq * elt, 256);
-  uint8_t* dv = dk + round_up(nkv * elt, 256);
-  uint8_t* d_o = dv + round_up(nkv * elt, 256);
-  uint8_t* d_lse = d_o + round_up(nq * 2, 256);
-  float* d_desc = reinterpret_cast<float*>(d_lse + round_up((size_t)B * H * N * 4, 256));
-  if (cudaMemcpyAsync(dq, q, nq * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dk, k, nkv * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(dv, v, nkv * elt, cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (fp8) {
+  float* d_desc = reinterpret_cast<float*>(w + total - 256);
+  const uint8_t* hq = static_cast<const uint8_t*>(q);
+  const uint8_t* hk = static_cast<const uint8_t*>(k);
+  const uint8_t* hv = static_cast<const uint8_t*>(v);
+  uint8_t* ho = static_cast<uint8_t*>(o);
+  uint8_t* hl = reinterpret_cast<uint8_t*>(lse);
+  const size_t q_pitch = (size_t)H * d * elt, kv_pitch = (size_t)Hkv * d * elt, o_pitch = (size_t)H * d * 2;
+  bool ok = cudaEventRecord(di->ev_start, stream) == cudaSuccess;
+  for (cudaStream_t s : {di->s_in, di->s_out, di->s_comp[0], di->s_comp[1]})
+    ok = ok && cudaStreamWaitEvent(s, di->ev_start, 0) == cudaSuccess;
+  if (ok && fp8) {
     const float desc[3] = {*descale_q, *descale_k, *descale_v};
-    if (cudaMemcpyAsync(d_desc, desc, sizeof(desc), cudaMemcpyHostToDevice, stream) != cudaSuccess)
-      return ATTN_ERR_CUDA;
+    ok = cudaMemcpyAsync(d_desc, desc, sizeof(desc), cudaMemcpyHostToDevice, di->s_in) == cudaSuccess;
   }
-  st = attn_fwd(dq, dk, dv, d_o, reinterpret_cast<float*>(d_lse), B, H, Hkv, N, d, scale, causal, dtype,
-                fp8 ? d_desc : nullptr, fp8 ? d_desc + 1 : nullptr, fp8 ? d_desc + 2 : nullptr, stream);
+  // Uploads: rows [b0 N, (b0 + nb) N) of the [B N, heads, d] views, a head range of each row.
+  for (int c = 0; ok && c < nc; ++c) {
+    const HostChunk& x = ch[c];
+    const size_t rows = (size_t)x.nb * N, row0 = (size_t)x.b0 * N;
+    ok = cudaMemcpy2DAsync(w + x.off_q, (size_t)x.ng * G * d * elt, hq + row0 * q_pitch + (size_t)x.g0 * G * d * elt,
+                           q_pitch, (size_t)x.ng * G * d * elt, rows, cudaMemcpyHostToDevice, di->s_in) == cudaSuccess &&
+         cudaMemcpy2DAsync(w + x.off_k, (size_t)x.ng * d * elt, hk + row0 * kv_pitch + (size_t)x.g0 * d * elt,
+                           kv_pitch, (size_t)x.ng * d * elt, rows, cudaMemcpyHostToDevice, di->s_in) == cudaSuccess &&
+         cudaMemcpy2DAsync(w + x.off_v, (size_t)x.ng * d * elt, hv + row0 * kv_pitch + (size_t)x.g0 * d * elt,
+                           kv_pitch, (size_t)x.ng * d * elt, rows, cudaMemcpyHostToDevice, di->s_in) == cudaSuccess &&
+         cudaEventRecord(di->ev_in[c], di->s_in) == cudaSuccess;
+  }
+  // Kernels: each chunk is a [nb, N, ng G, d] problem, alternating between two streams so one
+  // chunk's tail overlaps the next chunk's start.
+  for (int c = 0; ok && c < nc; ++c) {
+    const HostChunk& x = ch[c];
+    cudaStream_t sc = di->s_comp[c & 1];
+    ok = cudaStreamWaitEvent(sc, di->ev_in[c], 0) == cudaSuccess;
+    if (!ok) break;
+    st = attn_fwd(w + x.off_q, w + x.off_k, w + x.off_v, w + x.off_o, reinterpret_cast<float*>(w + x.off_lse), x.nb,
+                  x.ng * G, x.ng, N, d, scale, causal, dtype, fp8 ? d_desc : nullptr, fp8 ? d_desc + 1 : nullptr,
+                  fp8 ? d_desc + 2 : nullptr, sc);
+    if (st != ATTN_OK) { ok = false; break; }
+    ok = cudaEventRecord(di->ev_k[c], sc) == cudaSuccess;
+  }
+  // Downloads: O head ranges back into the strided host rows; LSE [B, H, N] rows are contiguous.
+  for (int c = 0; ok && c < nc; ++c) {
+    const HostChunk& x = ch[c];
+    const size_t rows = (size_t)x.nb * N, row0 = (size_t)x.b0 * N;
+    ok = cudaStreamWaitEvent(di->s_out, di->ev_k[c], 0) == cudaSuccess &&
+         cudaMemcpy2DAsync(ho + row0 * o_pitch + (size_t)x.g0 * G * d * 2, o_pitch, w + x.off_o,
+                           (size_t)x.ng * G * d * 2, (size_t)x.ng * G * d * 2, rows, cudaMemcpyDeviceToHost,
+                           di->s_out) == cudaSuccess;
+    for (int b = 0; ok && b < x.nb; ++b)
+      ok = cudaMemcpyAsync(hl + (((size_t)(x.b0 + b) * H + (size_t)x.g0 * G) * N) * 4,
+                           w + x.off_lse + (size_t)b * x.ng * G * N * 4, (size_t)x.ng * G * N * 4,
+                           cudaMemcpyDeviceToHost, di->s_out) == cudaSuccess;
+  }
+  // The caller's stream resumes after the last download; the call returns when it is done.
+  const bool joined = cudaEventRecord(di->ev_end, di->s_out) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, di->ev_end, 0) == cudaSuccess;
+  const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
   if (st != ATTN_OK) return st;
-  if (cudaMemcpyAsync(o, d_o, nq * 2, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaMemcpyAsync(lse, d_lse, (size_t)B * H * N * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return cudaStreamSynchronize(stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return (ok && joined && synced) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {

@@ -78,10 +78,15 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * attn_fwd_host — the same operation on HOST buffers: copies q, k, v (and the three fp8
  * descales, given here as HOST pointers to one float each) to device buffers owned by the
  * caller (`workspace`, at least attn_fwd_host_workspace_bytes(...) bytes of device memory,
- * 256-byte aligned), runs attn_fwd, and copies o and lse back to host memory. All copies and
- * the kernel are queued on `stream`; the call synchronizes `stream` before returning.
- * Host buffers may be pageable or pinned (pinned overlaps better). Returns as attn_fwd, plus
- * ATTN_ERR_INVALID_ARG for a too-small or misaligned workspace.
+ * 256-byte aligned), runs the forward, and copies o and lse back to host memory.
+ * The work is split into up to four chunks (whole batches when B >= 4, otherwise one batch and a
+ * range of KV heads with their query heads); the upload of one chunk, the kernel of another and
+ * the download of a third run concurrently on internal streams (created once per device, never
+ * on later calls; the call allocates no memory). The call starts after the work already queued
+ * on `stream` and returns after synchronizing `stream`, with o and lse in host memory. Host
+ * buffers may be pageable or pinned; only pinned buffers let the copies overlap. Calls on the
+ * same device are serialized. Returns as attn_fwd, plus ATTN_ERR_INVALID_ARG for a too-small or
+ * misaligned workspace.
  */
 attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
                             int B, int H, int Hkv, int N, int d, float scale, int causal,

@@ -37,9 +37,20 @@ def test_skipped_copy_times_out_and_context_survives(d, causal):
     compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
 
 
+HOST_SHAPES = [
+    dict(B=1, H=4, Hkv=2, N=384, d=128, causal=True),      # one batch, two KV-head chunks
+    dict(B=2, H=8, Hkv=4, N=300, d=128, causal=False),     # two batches x two KV-head chunks, ragged N
+    dict(B=5, H=2, Hkv=1, N=256, d=64, causal=True),       # uneven batch chunks
+    dict(B=1, H=6, Hkv=3, N=200, d=256, causal=False),     # three KV-head chunks
+]
+
+
+@pytest.mark.parametrize("shape", HOST_SHAPES, ids=lambda s: "B{B}_H{H}_Hkv{Hkv}_N{N}_d{d}".format(**s))
 @pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
-def test_host_entry_point_matches_device_entry_point(dtype):
-    w = inputs.Workload("host", B=1, H=4, Hkv=2, N=384, d=128, causal=True, dtype=dtype, seed=9)
+def test_host_entry_point_matches_device_entry_point(dtype, shape):
+    if dtype == "fp8_e4m3" and shape["d"] != 128:
+        pytest.skip("fp8 instances are d=128")
+    w = inputs.Workload("host", dtype=dtype, seed=9, **shape)
     x = inputs.make_inputs(w)
     o_dev, lse_dev = run_cuda(w, x)
     code = binding.ATTN_DTYPE_FP8_E4M3 if dtype == "fp8_e4m3" else binding.ATTN_DTYPE_BF16
