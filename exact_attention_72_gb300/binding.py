@@ -45,6 +45,10 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
+    L.attn_fwd_splitkv.restype = i
+    L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
+    L.attn_fwd_splitkv_workspace_bytes.restype = sz
+    L.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_fwd_host_workspace_bytes.restype = sz
     L.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
     L.attn_get_status.restype = i
@@ -114,6 +118,49 @@ def attn_fwd(q, k, v, causal: bool, scale: Optional[float] = None, descale_q=Non
                         float(scale), int(bool(causal)), code, ptrs[0], ptrs[1], ptrs[2], _stream_handle(stream))
     _check(st, "attn_fwd")
     return out, lse
+
+
+def attn_fwd_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, descale_q=None, descale_k=None,
+                     descale_v=None, workspace=None, out=None, lse=None, stream=None):
+    """Split-KV decode forward: q [B,Nq,H,d] attends to all keys of k/v [B,Nk,Hkv,d] (no mask).
+
+    ``workspace`` (CUDA uint8, at least attn_fwd_splitkv_workspace_bytes(...) bytes) is allocated
+    here with torch if not given. Returns (out [B,Nq,H,d] bf16, lse [B,H,Nq] fp32).
+    """
+    import torch
+    B, Nq, H, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.shape != (B, Nk, Hkv, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must be [B, Nk, Hkv, d] with q's dtype")
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, Nq, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ptrs = [0, 0, 0]
+    if code == ATTN_DTYPE_FP8_E4M3:
+        for idx, t in enumerate((descale_q, descale_k, descale_v)):
+            if t is None or t.dtype != torch.float32 or not t.is_cuda:
+                raise ValueError("fp8 needs descale_q/k/v as float32 CUDA tensors")
+            ptrs[idx] = t.data_ptr()
+    st = lib().attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv,
+                                Nq, Nk, d, float(scale), int(num_splits), code, ptrs[0], ptrs[1], ptrs[2],
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(stream))
+    _check(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attn_fwd_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(lib().attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
 
 
 def attn_fwd_host(q, k, v, out, lse, causal: bool, workspace, scale: Optional[float] = None,

@@ -140,17 +140,48 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 // [B, N, heads, d] tensor -> 4-D map (d, N, heads, B), box (128-byte row, 128 rows, 1, 1),
 // 128-byte swizzle; rows past N read as zeros.
-bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int heads, int B) {
+bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int heads, int B, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t elt = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)heads * d * elt, (cuuint64_t)d * elt, (cuuint64_t)N * heads * d * elt};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), 128, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
              dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Packed GQA view of q [B, Nq, H, d] for split-KV decode: 5-D map (d, G, Nq, Hkv, B) so one box
+// (128-byte row, G heads, 128 / G positions, 1, 1) is 128 query rows of one kv head's group.
+bool make_map_q_packed(CUtensorMap* m, const void* base, bool fp8, int d, int Nq, int H, int Hkv, int B) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t elt = fp8 ? 1 : 2;
+  const int G = H / Hkv;
+  cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)G, (cuuint64_t)Nq, (cuuint64_t)Hkv, (cuuint64_t)B};
+  cuuint64_t strides[4] = {(cuuint64_t)d * elt, (cuuint64_t)H * d * elt, (cuuint64_t)G * d * elt,
+                           (cuuint64_t)Nq * H * d * elt};
+  cuuint32_t box[5] = {(cuuint32_t)(128 / elt), (cuuint32_t)G, (cuuint32_t)(128 / G), 1, 1};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t dispatch_split(gb300::LaunchArgs& a, bool fp8, cudaStream_t s) {
+  if constexpr (D == 128) {
+    if (fp8) return gb300::launch_attn_fwd<128, false, true, true>(a, s);
+  }
+  return gb300::launch_attn_fwd<D, false, false, true>(a, s);
+}
+
+constexpr int kMaxSplits = 128;
+
+size_t splitkv_part_o_bytes(int B, int H, int Nq, int d, int S) {
+  return round_up((size_t)S * B * H * Nq * d * 4, 256);
 }
 
 bool supported_dim(int d, attn_dtype_t dtype) {
@@ -229,6 +260,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.scale_log2 = scale * 1.4426950408889634f;
   p.n_mb = (N + rows - 1) / rows;
   p.n_tiles = B * H * p.n_mb;
+  p.Nk = N;
+  p.G = H / Hkv;
+  p.n_splits = 1;
+  p.n_kvt = (N + 127) / 128;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
   p.status = di->status;
   p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
   p.debug_skip_load = g_skip_load;
@@ -328,6 +365,89 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
   if (st != ATTN_OK) return st;
   return (ok && joined && synced) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_part_o_bytes(B, H, Nq, d, num_splits) + round_up((size_t)num_splits * B * H * Nq * 4, 256);
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                               int Hkv, int Nq, int Nk, int d, float scale, int num_splits, attn_dtype_t dtype,
+                               const float* descale_q, const float* descale_k, const float* descale_v,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (Nq < 1 || Nk < 1 || num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_shape(B, H, Hkv, Nk, d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  st = check_shape(B, H, Hkv, Nq, d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  const int G = H / Hkv;
+  if (G > 128 || (128 % G) != 0) return ATTN_ERR_UNSUPPORTED;   // G packed rows must tile 128
+  const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
+  if (!q || !k || !v || !o || !lse || !workspace) return ATTN_ERR_INVALID_ARG;
+  if (fp8 && (!descale_q || !descale_k || !descale_v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(workspace, 256))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits)) return ATTN_ERR_INVALID_ARG;
+  const size_t elt = fp8 ? 1 : 2;
+  const size_t nq = (size_t)B * Nq * H * d, nkv = (size_t)B * Nk * Hkv * d;
+  const size_t o_bytes = nq * 2, lse_bytes = (size_t)B * H * Nq * 4;
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {nq * elt, nkv * elt, nkv * elt};
+  for (int i = 0; i < 3; ++i)
+    if (ranges_overlap(o, o_bytes, ins[i], in_bytes[i]) || ranges_overlap(lse, lse_bytes, ins[i], in_bytes[i]) ||
+        ranges_overlap(workspace, workspace_bytes, ins[i], in_bytes[i]))
+      return ATTN_ERR_INVALID_ARG;
+  if (ranges_overlap(o, o_bytes, lse, lse_bytes) || ranges_overlap(workspace, workspace_bytes, o, o_bytes) ||
+      ranges_overlap(workspace, workspace_bytes, lse, lse_bytes))
+    return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  gb300::LaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map_q_packed(&a.tm_q, q, fp8, d, Nq, H, Hkv, B) || !make_map(&a.tm_k, k, fp8, d, Nk, Hkv, B, 128) ||
+      !make_map(&a.tm_v, v, fp8, d, Nk, Hkv, B, 128))
+    return ATTN_ERR_CUDA;
+  const int n_kvt = (Nk + 127) / 128;
+  const int S = num_splits < n_kvt ? num_splits : n_kvt;   // every split gets at least one KV tile
+  const int rows = gb300::rows_per_work_tile(d);
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + splitkv_part_o_bytes(B, H, Nq, d, num_splits));
+  gb300::AttnParams& p = a.params;
+  p.o = o;
+  p.lse = lse;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = Nq;
+  p.Nk = Nk;
+  p.G = G;
+  p.n_splits = S;
+  p.n_kvt = n_kvt;
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.n_mb = (int)(((long long)Nq * G + rows - 1) / rows);
+  const long long tiles = (long long)B * Hkv * S * p.n_mb;
+  if (tiles >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.n_tiles = (int)tiles;
+  p.status = di->status;
+  p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
+  p.debug_skip_load = g_skip_load;
+  a.num_sms = di->num_sms;
+  cudaError_t e;
+  switch (d) {
+    case 64: e = dispatch_split<64>(a, fp8, stream); break;
+    case 128: e = dispatch_split<128>(a, fp8, stream); break;
+    default: e = dispatch_split<256>(a, fp8, stream); break;
+  }
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  e = gb300::launch_splitkv_combine(part_o, part_lse, o, lse, S, B, H, Nq, d, di->num_sms, stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {

@@ -45,20 +45,28 @@ struct AttnParams {
   const float* descale_q;   // fp8 only: one fp32 each (device)
   const float* descale_k;
   const float* descale_v;
-  int B, H, Hkv, N;
+  int B, H, Hkv, N;         // N: query rows per (batch, head) (prefill: also the key count)
   float scale_log2;         // scale * log2(e)
-  int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head)
-  int n_tiles;              // B * H * n_mb
+  int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head) / per (batch, kv head)
+  int n_tiles;              // work tiles in the launch
+  // Split-KV (decode) mode: Nk keys in n_kvt tiles of 128, split into n_splits ranges; query
+  // rows of a GQA group are packed G per position into the 128-row tiles; the normalized partial
+  // O (fp32 [n_splits, B, H, N, D]) and LSE ([n_splits, B, H, N]) go to part_o / part_lse.
+  int Nk, G, n_splits, n_kvt;
+  float* part_o;
+  float* part_lse;
   uint32_t* status;         // device status word (first failure)
   unsigned long long timeout_ns;
   int debug_skip_load;      // fault injection: CTA 0 never loads V_0 of its first tile
 };
 
-template <int D_, bool CAUSAL_, bool FP8_>
+template <int D_, bool CAUSAL_, bool FP8_, bool SPLIT_ = false>
 struct AttnCfg {
   static constexpr int D = D_;
   static constexpr bool CAUSAL = CAUSAL_;
   static constexpr bool FP8 = FP8_;
+  static constexpr bool SPLIT = SPLIT_;                   // split-KV decode mode (no mask)
+  static_assert(!(SPLIT && CAUSAL), "split-KV mode has no causal mask");
   static constexpr int ELT = FP8 ? 1 : 2;                 // bytes per q/k/v element
   static constexpr int NQ = (D <= 128) ? 2 : 1;           // 128-row Q tiles per CTA
   static constexpr int BM = 128, BN = 128;                // query rows per Q tile, keys per KV tile
@@ -106,18 +114,34 @@ enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_
                   SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9, SITE_S_TURN = 10 };
 
 struct TileCoord {
-  int b, h, mb;
+  int b, h, mb;     // h: query head (prefill) or kv head (split-KV)
+  int s, j0, j1;    // split index and its KV tile range [j0, j1)
 };
 
 // Work tile t -> (batch, head, query block). Causal tiles go longest first: every head's last
 // query block, then every head's second-to-last, and so on. Non-causal tiles keep a head's
 // blocks together so concurrently running CTAs share K/V in L2.
-template <bool CAUSAL>
+template <class C>
 __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
   TileCoord c;
+  if (C::SPLIT) {
+    // Split-KV: the query blocks of one (batch, kv head, split) are consecutive.
+    c.mb = t % p.n_mb;
+    const int rest = t / p.n_mb;
+    c.s = rest % p.n_splits;
+    const int bk = rest / p.n_splits;
+    c.b = bk / p.Hkv;
+    c.h = bk % p.Hkv;
+    c.j0 = (int)((long long)c.s * p.n_kvt / p.n_splits);
+    c.j1 = (int)((long long)(c.s + 1) * p.n_kvt / p.n_splits);
+    return c;
+  }
+  c.s = 0;
+  c.j0 = 0;
+  c.j1 = p.n_kvt;
   const int BH = p.B * p.H;
   int bh;
-  if (CAUSAL) {
+  if (C::CAUSAL) {
     c.mb = p.n_mb - 1 - t / BH;
     bh = t % BH;
   } else {
@@ -129,13 +153,20 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
   return c;
 }
 
-// Number of KV tiles Q tile `qt` of query block `mb` visits (0 if all its rows are past N).
+// First query position of Q tile qt (split-KV: G packed rows per position).
 template <class C>
-__device__ __forceinline__ int kv_tiles_for(int mb, int qt, int N) {
-  const int row0 = (mb * C::NQ + qt) * C::BM;
-  if (row0 >= N) return 0;
-  const int n_kv = (N + C::BN - 1) / C::BN;
-  return C::CAUSAL ? (row0 / C::BN + 1) : n_kv;
+__device__ __forceinline__ int q_tile_pos0(const TileCoord& tc, int qt, const AttnParams& p) {
+  const int row0 = (tc.mb * C::NQ + qt) * C::BM;
+  return C::SPLIT ? row0 / p.G : row0;
+}
+
+// Number of KV tiles Q tile `qt` visits (0 if all its rows are past N), starting at tile tc.j0.
+template <class C>
+__device__ __forceinline__ int kv_tiles_for(const TileCoord& tc, int qt, const AttnParams& p) {
+  const int pos0 = q_tile_pos0<C>(tc, qt, p);
+  if (pos0 >= p.N) return 0;
+  if (C::SPLIT) return tc.j1 - tc.j0;
+  return C::CAUSAL ? (pos0 / C::BN + 1) : p.n_kvt;
 }
 
 // Optional event trace for pipeline analysis (off unless compiled with -DGB300_ATTN_TRACE):
@@ -296,11 +327,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       bool ok = true;
       int iter = 0;
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++iter) {
-        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
-        const int kvh = tc.h / (p.H / p.Hkv);
+        const TileCoord tc = decode_tile<C>(t, p);
+        const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
         for (int qt = 0; qt < C::NQ; ++qt) {
-          const int n = kv_tiles_for<C>(tc.mb, qt, p.N);
+          const int n = kv_tiles_for<C>(tc, qt, p);
           nmax = n > nmax ? n : nmax;
           nq_valid += (n > 0);
         }
@@ -311,11 +342,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         mbar_arrive_expect_tx(smem_addr(&bar_q_full), nq_valid * C::TILE_BYTES);
         for (int qt = 0; qt < C::NQ; ++qt) {
-          const int row0 = (tc.mb * C::NQ + qt) * C::BM;
-          if (row0 >= p.N) continue;
-          for (int ch = 0; ch < C::NCH; ++ch)
-            tma_load_4d(sQ + (qt * C::NCH + ch) * C::CHUNK_BYTES, &tm_q, smem_addr(&bar_q_full), ch * C::CE,
-                        row0, tc.h, tc.b);
+          const int pos0 = q_tile_pos0<C>(tc, qt, p);
+          if (pos0 >= p.N) continue;
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            const uint32_t dst = sQ + (qt * C::NCH + ch) * C::CHUNK_BYTES;
+            if (C::SPLIT)   // (d, head in group, position, kv head, batch): G x 128/G packed rows
+              tma_load_5d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, 0, pos0, tc.h, tc.b);
+            else
+              tma_load_4d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, pos0, tc.h, tc.b);
+          }
         }
         ++nq_loads;
         for (int j = 0; ok && j < nmax; ++j) {
@@ -332,7 +367,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               mbar_arrive_expect_tx(smem_addr(&bar_kv_full[slot]), C::TILE_BYTES);
               for (int ch = 0; ch < C::NCH; ++ch)
                 tma_load_4d(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES, tm, smem_addr(&bar_kv_full[slot]),
-                            ch * C::CE, j * C::BN, kvh, tc.b);
+                            ch * C::CE, (tc.j0 + j) * C::BN, kvh, tc.b);
             }
             ++ring;
           }
@@ -384,11 +419,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return true;
       };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
-        const int n = kv_tiles_for<C>(tc.mb, myq, p.N);
+        const TileCoord tc = decode_tile<C>(t, p);
+        const int n = kv_tiles_for<C>(tc, myq, p);
         int nmax = 0;
         for (int qt = 0; qt < C::NQ; ++qt) {
-          const int nq = kv_tiles_for<C>(tc.mb, qt, p.N);
+          const int nq = kv_tiles_for<C>(tc, qt, p);
           nmax = nq > nmax ? nq : nmax;
         }
         if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
@@ -469,8 +504,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         return true;
       };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
-        const int nmax = kv_tiles_for<C>(tc.mb, 0, p.N);
+        const TileCoord tc = decode_tile<C>(t, p);
+        const int nmax = kv_tiles_for<C>(tc, 0, p);
+        if (nmax == 0) continue;
         if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
         ++nq_loads;
         const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
@@ -523,13 +559,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
-    const int n_kv_all = (p.N + C::BN - 1) / C::BN;
+    const int Nk = C::SPLIT ? p.Nk : p.N;   // keys per (batch, head)
     bool ok = true;
     for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
-      const TileCoord tc = decode_tile<C::CAUSAL>(t, p);
-      const int n = kv_tiles_for<C>(tc.mb, qt, p.N);
+      const TileCoord tc = decode_tile<C>(t, p);
+      const int n = kv_tiles_for<C>(tc, qt, p);
       if (n == 0) continue;
-      const int row0 = (tc.mb * C::NQ + qt) * C::BM;
+      const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
       float m = -INFINITY;   // running max of s * x (log2 units), used as the exponent shift
       float l = 0.0f;        // running sum of exp2(s * x - m)
       for (int j = 0; j < n; ++j) {
@@ -557,9 +593,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
         // Masking: keys past N (ragged tail) and, on the diagonal tile, keys after the query row.
         const bool diag = C::CAUSAL && (j == n - 1);
-        const bool tail = (j == n_kv_all - 1) && (p.N % C::BN != 0);
+        const int jk = tc.j0 + j;   // KV tile index within the sequence
+        const bool tail = (jk == p.n_kvt - 1) && (Nk % C::BN != 0);
         if (diag || tail) {
-          int lim = p.N - j * C::BN;
+          int lim = Nk - jk * C::BN;
           if (diag) lim = min(lim, (row0 + r) - j * C::BN + 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -663,30 +700,56 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       pv_cnt += n;
       ++tiles_done;
       tc_fence_after();
-      const int row = row0 + r;
-      const bool valid = row < p.N;
-      const float inv_l = out_scale / l;
       const uint32_t tO = tmem + lane_base + C::O_COL + qt * C::D;
-      __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                            ((size_t)(tc.b * p.N + (valid ? row : 0)) * p.H + tc.h) * C::D;
+      const float lse_row = (m + log2f(l)) * 0.69314718055994531f;
+      if constexpr (C::SPLIT) {
+        // Partial result of this KV range: normalized O in fp32 and its LSE, row (position, head).
+        const int pos = row0 + r / p.G;
+        const int h = tc.h * p.G + r % p.G;
+        const bool valid = pos < p.N;
+        const float inv_l = out_scale / l;
+        const size_t prow = (((size_t)tc.s * p.B + tc.b) * p.H + h) * p.N + (valid ? pos : 0);
+        float* orow = p.part_o + prow * C::D;
 #pragma unroll 1
-      for (int c0 = 0; c0 < C::D; c0 += 32) {
-        uint32_t ov[32];
-        tmem_ld_32cols(tO + c0, ov);
-        tmem_ld_wait();
-        reg_fence32(ov);
-        uint32_t pk[16];
+        for (int c0 = 0; c0 < C::D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld_32cols(tO + c0, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+          if (valid) {
+            float4* dst = reinterpret_cast<float4*>(orow + c0);
 #pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          pk[c >> 1] = pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
+                                    __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
+          }
         }
+        if (valid) p.part_lse[prow] = lse_row;
+      } else {
+        const int row = row0 + r;
+        const bool valid = row < p.N;
+        const float inv_l = out_scale / l;
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                              ((size_t)(tc.b * p.N + (valid ? row : 0)) * p.H + tc.h) * C::D;
+#pragma unroll 1
+        for (int c0 = 0; c0 < C::D; c0 += 32) {
+          uint32_t ov[32];
+          tmem_ld_32cols(tO + c0, ov);
+          tmem_ld_wait();
+          reg_fence32(ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2)
+            pk[c >> 1] = pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid) p.lse[((size_t)tc.b * p.H + tc.h) * p.N + row] = lse_row;
       }
-      if (valid) p.lse[((size_t)tc.b * p.H + tc.h) * p.N + row] = (m + log2f(l)) * 0.69314718055994531f;
     }
   }
   else {

@@ -1,0 +1,9 @@
+// Split-KV (decode) instances of the attention forward: bf16 d = 64, 128, 256 and e4m3 d = 128.
+#include "launch_impl.cuh"
+
+namespace gb300 {
+template cudaError_t launch_attn_fwd<64, false, false, true>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<128, false, false, true>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<256, false, false, true>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<128, false, true, true>(LaunchArgs&, cudaStream_t);
+}  // namespace gb300

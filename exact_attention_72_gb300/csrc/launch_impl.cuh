@@ -4,9 +4,9 @@
 
 namespace gb300 {
 
-template <int D, bool CAUSAL, bool FP8>
+template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
-  using C = AttnCfg<D, CAUSAL, FP8>;
+  using C = AttnCfg<D, CAUSAL, FP8, SPLIT>;
   auto kernel = attn_fwd_kernel<C>;
   // The attribute is per device; setting it on every call is cheap and keeps this stateless.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);

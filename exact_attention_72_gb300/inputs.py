@@ -49,6 +49,12 @@ class Workload:
     seed: int = 1000
     k_outlier_frac: float = 0.0    # fraction of K entries replaced by +-k_outlier_mag
     k_outlier_mag: float = 8.0
+    Nk: Optional[int] = None       # keys per sequence when it differs from N (decode shapes)
+    splits: int = 1                # split-KV ranges (decode shapes)
+
+    @property
+    def n_keys(self) -> int:
+        return self.N if self.Nk is None else self.Nk
 
     @property
     def scale(self) -> float:
@@ -56,8 +62,8 @@ class Workload:
 
     @property
     def flops(self) -> float:
-        """4*B*H*N^2*d, halved for causal (the benchmark's counting convention)."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        """4*B*H*Nq*Nk*d, halved for causal (the benchmark's counting convention)."""
+        f = 4.0 * self.B * self.H * self.N * self.n_keys * self.d
         return f / 2.0 if self.causal else f
 
     @property
@@ -68,7 +74,7 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Read q, k, v once; write o (bf16) and lse (fp32) once."""
         q = self.B * self.N * self.H * self.d * self.elt_bytes
-        kv = 2 * self.B * self.N * self.Hkv * self.d * self.elt_bytes
+        kv = 2 * self.B * self.n_keys * self.Hkv * self.d * self.elt_bytes
         o = self.B * self.N * self.H * self.d * 2
         lse = self.B * self.H * self.N * 4
         return q + kv + o + lse
@@ -94,6 +100,14 @@ WORKLOADS = {
 
 # The headline workload the benchmark times.
 HEADLINE = "causal_gqa_bf16_n8192_d128"
+
+# Decode-shaped workloads for the split-KV path (few queries, long KV sequence, no mask).
+DECODE_WORKLOADS = {
+    "decode_gqa_bf16_nq1_nk16384_d128": Workload("decode_gqa_bf16_nq1_nk16384_d128", B=8, H=32, Hkv=8, N=1,
+                                                 d=128, causal=False, seed=1101, Nk=16384, splits=16),
+    "decode_gqa_bf16_nq16_nk8192_d128": Workload("decode_gqa_bf16_nq16_nk8192_d128", B=4, H=32, Hkv=8, N=16,
+                                                 d=128, causal=False, seed=1102, Nk=8192, splits=8),
+}
 
 
 @dataclasses.dataclass
@@ -131,8 +145,8 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> AttnInputs:
     g = torch.Generator(device="cpu")
     g.manual_seed(w.seed if seed is None else seed)
     q = torch.randn((w.B, w.N, w.H, w.d), generator=g, dtype=torch.float32)
-    k = torch.randn((w.B, w.N, w.Hkv, w.d), generator=g, dtype=torch.float32)
-    v = torch.randn((w.B, w.N, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.n_keys, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.n_keys, w.Hkv, w.d), generator=g, dtype=torch.float32)
     if w.k_outlier_frac > 0:
         n_out = int(round(w.k_outlier_frac * k.numel()))
         idx = torch.randperm(k.numel(), generator=g)[:n_out]

@@ -98,6 +98,35 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
 size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_dtype_t dtype);
 
 /*
+ * attn_fwd_splitkv — split-KV ("flash-decoding") forward for decode-shaped problems: Nq query
+ * rows per (batch, head) attend to all Nk keys (no mask: each query sees the whole KV sequence,
+ * as a newly generated token sees its cache). The key sequence is cut into
+ * min(num_splits, ceil(Nk / 128)) ranges that are processed in parallel, each producing a
+ * normalized partial output and its log-sum-exp; a second kernel merges them with
+ * LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.
+ *   Source: "flash-attention-3" (ai.thesatyajit.com), "What is actually in the box" (split-KV
+ *   with a separate combine kernel); "Hopper" tag page (l1-ca0.github.io), section 10 titles
+ *   ("Flash-Decoding: Split-KV and the Combine Kernel", 10.2.1 "The combine math") and
+ *   section 11 ("PackGQA": query heads of a GQA group are packed into the 128-row tile).
+ *
+ *   q [B, Nq, H, d], k/v [B, Nk, Hkv, d], o [B, Nq, H, d] bf16, lse [B, H, Nq] fp32: DEVICE
+ *   memory, same element types, alignment and descale rules as attn_fwd. H / Hkv must divide
+ *   128. 1 <= num_splits <= 128.
+ *   workspace: caller-owned DEVICE memory of at least
+ *   attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes, 256-byte aligned, not
+ *   overlapping the other buffers; it holds the partial results and needs no initialization.
+ * Asynchronous on `stream`; allocates nothing. Errors as attn_fwd.
+ */
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               int B, int H, int Hkv, int Nq, int Nk, int d, float scale,
+                               int num_splits, attn_dtype_t dtype, const float* descale_q,
+                               const float* descale_k, const float* descale_v, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream);
+
+/* Device bytes attn_fwd_splitkv needs for its partial results (0 for invalid arguments). */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
  * attn_get_status — synchronizes `stream`, then returns ATTN_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded wait since the last attn_clear_status,
  * ATTN_ERR_CUDA if the synchronization failed, else ATTN_OK. `detail` (may be NULL) receives

@@ -80,3 +80,25 @@ def test_host_workspace_size(lib):
     assert n >= q + 2 * kv + q + 2 * 32 * 8192 * 4
     assert binding.attn_fwd_host_workspace_bytes(0, 1, 1, 1, 128, 0) == 0
     assert binding.attn_fwd_host_workspace_bytes(1, 1, 1, 1, 96, 0) == 0
+
+
+def test_splitkv_validation(lib):
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+
+    def call(Nq=1, Nk=512, B=1, H=8, Hkv=2, d=128, splits=4, ws=1 << 28, ws_bytes=1 << 20, scale=0.1, dtype=0,
+             q=1 << 16, k=1 << 20, v=1 << 24, o=1 << 26, lse=1 << 27):
+        return lib.attn_fwd_splitkv(q, k, v, o, lse, B, H, Hkv, Nq, Nk, d, scale, splits, dtype, None, None, None,
+                                    ws, ws_bytes, None)
+
+    assert call(Nq=0) == INV
+    assert call(Nk=0) == INV
+    assert call(splits=0) == INV
+    assert call(splits=129) == INV
+    assert call(H=6, Hkv=2) == UNS                 # group of 3 heads cannot tile 128 rows
+    assert call(d=96) == UNS
+    assert call(ws_bytes=16) == INV                 # workspace too small
+    assert call(ws=(1 << 28) + 8) == INV            # workspace misaligned
+    assert call(ws=(1 << 16)) == INV                # workspace overlaps q
+    need = binding.attn_fwd_splitkv_workspace_bytes(2, 32, 1, 128, 16)
+    assert need >= 16 * 2 * 32 * 1 * (128 + 1) * 4
+    assert binding.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 128, 0) == 0

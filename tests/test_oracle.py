@@ -299,3 +299,49 @@ def test_planted_mistakes_are_caught(kind):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"no pin caught the planted mistake {kind!r}"
+
+
+# ----------------------------------------------------------------------------------------------
+# Decode shape: fewer queries than keys, every query sees every key (no mask)
+# ----------------------------------------------------------------------------------------------
+
+def test_oracle_more_keys_than_queries_brute_force():
+    """Nq != Nk (decode / split-KV shape): pure-Python brute force, no numpy arithmetic."""
+    rng = np.random.default_rng(31)
+    B, Nq, Nk, H, Hkv, d = 2, 3, 11, 4, 2, 5
+    q = rng.standard_normal((B, Nq, H, d))
+    k = rng.standard_normal((B, Nk, Hkv, d))
+    v = rng.standard_normal((B, Nk, Hkv, d))
+    o, lse = oracle.attention_forward(q, k, v, 0.45, False)
+    assert o.shape == (B, Nq, H, d) and lse.shape == (B, H, Nq)
+    for b in range(B):
+        for h in range(H):
+            kh = h // (H // Hkv)
+            for i in range(Nq):
+                s = [0.45 * math.fsum(q[b, i, h, t] * k[b, j, kh, t] for t in range(d)) for j in range(Nk)]
+                mx = max(s)
+                w = [math.exp(x - mx) for x in s]
+                tot = math.fsum(w)
+                assert abs(lse[b, h, i] - (mx + math.log(tot))) < 1e-12
+                for t in range(d):
+                    ref = math.fsum(w[j] * v[b, j, kh, t] for j in range(Nk)) / tot
+                    assert abs(o[b, i, h, t] - ref) < 1e-12
+
+
+def test_oracle_key_partition_merge_identity():
+    """Splitting the keys into ranges and merging the per-range (O, LSE) by exp(LSE_s - LSE)
+    reproduces the full result: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s. This
+    is a property of the definition (the split-KV combine), checked here on the oracle itself."""
+    rng = np.random.default_rng(32)
+    B, Nq, Nk, H, d = 1, 4, 23, 2, 6
+    q = rng.standard_normal((B, Nq, H, d)) * 2
+    k = rng.standard_normal((B, Nk, H, d))
+    v = rng.standard_normal((B, Nk, H, d))
+    o, lse = oracle.attention_forward(q, k, v, 0.5, False)
+    cuts = [0, 5, 6, 17, 23]
+    parts = [oracle.attention_forward(q, k[:, a:b], v[:, a:b], 0.5, False) for a, b in zip(cuts, cuts[1:])]
+    lse_all = np.logaddexp.reduce(np.stack([p[1] for p in parts]), axis=0)
+    np.testing.assert_allclose(lse_all, lse, rtol=0, atol=1e-12)
+    w = [np.exp(p[1] - lse_all) for p in parts]          # [B, H, Nq]
+    o_m = sum(np.transpose(wi, (0, 2, 1))[..., None] * p[0] for wi, p in zip(w, parts))
+    np.testing.assert_allclose(o_m, o, rtol=0, atol=1e-12)
