@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
     L.attn_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
+    L.attn_fwd_splitkv_static.restype = i
+    L.attn_fwd_splitkv_static.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
     L.attn_fwd_splitkv_workspace_bytes.restype = sz
     L.attn_fwd_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_fwd_host_workspace_bytes.restype = sz
@@ -156,6 +158,27 @@ def attn_fwd_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, de
                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                 _stream_handle(stream))
     _check(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def attn_fwd_splitkv_static(q, k, v, num_splits: int, scale: Optional[float] = None, out=None, lse=None,
+                            stream=None):
+    """attn_fwd_splitkv without a workspace: the library's fixed 16 MiB device scratch holds the
+    partial results (for callers that cannot allocate device memory). bf16 inputs; calls that
+    overlap on the GPU share that scratch and must be serialized."""
+    import torch
+    B, Nq, H, d = q.shape
+    Nk, Hkv = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Nq, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd_splitkv_static(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                                       H, Hkv, Nq, Nk, d, float(scale), int(num_splits), _dtype_code(q), None, None,
+                                       None, _stream_handle(stream))
+    _check(st, "attn_fwd_splitkv_static")
     return out, lse
 
 

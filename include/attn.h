@@ -126,6 +126,33 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
 /* Device bytes attn_fwd_splitkv needs for its partial results (0 for invalid arguments). */
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 
+/* Size of the fixed device scratch used by attn_fwd_splitkv_static (16 MiB). */
+#define ATTN_SPLITKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * attn_fwd_splitkv_static — attn_fwd_splitkv for callers that cannot allocate device memory
+ * (a plugin whose host framework owns every device allocation, a server that has already
+ * committed its memory budget, a latency-critical path that must not risk the device
+ * synchronization an allocation can bring). Instead of a caller workspace, the partial results
+ * go to a fixed 16 MiB device array that is part of the library (ATTN_SPLITKV_STATIC_SCRATCH_BYTES;
+ * every GPU that loads the library holds it until the process exits). The pages have no
+ * counterpart to this entry point: it exists for callers of this library.
+ *   Arguments, layouts and errors as attn_fwd_splitkv, without workspace arguments. Returns
+ *   ATTN_ERR_UNSUPPORTED when attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits) exceeds
+ *   ATTN_SPLITKV_STATIC_SCRATCH_BYTES. Allocates nothing, on the device or elsewhere.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress with
+ *   that device current); make that first call before any stream capture.
+ *   All calls share the one array, and each call overwrites it: calls whose kernels overlap on
+ *   the GPU (different streams, or different host threads) race and corrupt each other's results.
+ *   Serialize them, e.g. by using one stream. Nothing in the array needs to start at zero: each
+ *   call writes every partial result it reads.
+ */
+attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o,
+                                      float* lse, int B, int H, int Hkv, int Nq, int Nk, int d,
+                                      float scale, int num_splits, attn_dtype_t dtype,
+                                      const float* descale_q, const float* descale_k,
+                                      const float* descale_v, cudaStream_t stream);
+
 /*
  * attn_get_status — synchronizes `stream`, then returns ATTN_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded wait since the last attn_clear_status,
