@@ -35,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "attn fwd TFLOP/s (bf16, causal, N=8192, d=128) and % of GB300 dense peak"
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
+DECODE_NAMES = {"decode_gqa_bf16_nq1_nk16384_d128", "decode_gqa_bf16_nq16_nk8192_d128"}
 
 
 def parse_args(argv=None):
@@ -156,6 +157,15 @@ def peaks():
         return FALLBACK_BF16_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)"
 
 
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", "*"))):
@@ -215,7 +225,7 @@ def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
         t0 = time.perf_counter()
         oracle.attention_head(q, k, v, w.scale, w.causal, rows=rows)
         elapsed += time.perf_counter() - t0
-        flops += credited_flops(w, rows, w.N)
+        flops += credited_flops(w, rows, w.n_keys)
         blocks_done.append((b, h, int(r0)))
         steps += 1
     desc = (f"{steps} blocks of {block_rows} query rows (full score rows, fp64) from heads of the "
@@ -254,7 +264,8 @@ def run_reference(args, w, x):
 
 
 def config_of(w):
-    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal,
+    extra = {"Nk": w.n_keys, "splits": w.splits} if w.name in DECODE_NAMES else {}
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal, **extra,
             "qkv_dtype": w.dtype, "k_outliers": w.k_outlier_frac,
             "l2": "flushed before every step (256 MiB write, outside the timed events)",
             "parallelism": "replicas (one full workload per GPU)"}
@@ -279,9 +290,16 @@ def run_ours(args, w, x):
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    decode = w.name in DECODE_NAMES
+    if decode:
+        ws = torch.empty(binding.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.N, w.d, w.splits), dtype=torch.uint8,
+                         device=dev)
 
     def step():
-        binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, **kw)
+        if decode:
+            binding.attn_fwd_splitkv(q, k, v, w.splits, scale=w.scale, workspace=ws, out=o, lse=lse, **kw)
+        else:
+            binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, **kw)
 
     for i in range(max(args.warmup, 0)):
         flush.fill_(i & 0xFF)
@@ -321,9 +339,22 @@ def run_ours(args, w, x):
     peak = peak_bf16 * (2.0 if fp8 else 1.0)
     if fp8:
         peak_src += " x2 (e4m3/bf16 nominal dense ratio)"
+    if decode:
+        # Few query rows against a long KV sequence: bound by reading K and V once from HBM.
+        gbs = w.algorithmic_bytes / (mean_ms * 1e-3) / 1e9
+        hbm, hbm_src = hbm_peak()
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                    "traffic": None, "kernel": "attn_fwd_kernel (split-KV) + splitkv_combine_kernel",
+                    "peak_source": hbm_src, "algorithmic_bytes": w.algorithmic_bytes,
+                    "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}}
+    else:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": measured_traffic(w.name),
+                    "kernel": "attn_fwd_kernel", "peak_source": peak_src,
+                    "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}}
 
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not decode:
         e2e = measure_e2e(args, w, x, dev, dist, world)
 
     clocks = sampler.summary(t_host0, t_host1)
@@ -338,11 +369,8 @@ def run_ours(args, w, x):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
             "config": config_of(w),
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": measured_traffic(w.name),
-                         "kernel": "attn_fwd_kernel", "peak_source": peak_src,
-                         "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}},
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks,
+            "roofline": roofline,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (2 if decode else 1), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -387,7 +415,8 @@ def measure_e2e(args, w, x, dev, dist, world):
 def main(argv=None):
     args = parse_args(argv)
     from exact_attention_72_gb300 import inputs
-    w = inputs.WORKLOADS[args.workload or inputs.HEADLINE]
+    name = args.workload or inputs.HEADLINE
+    w = inputs.WORKLOADS[name] if name in inputs.WORKLOADS else inputs.DECODE_WORKLOADS[name]
     if args.batch is not None:
         w = w.replace(B=args.batch, name=f"{w.name}_b{args.batch}")
     rank, world, _ = rank_info()
