@@ -43,6 +43,8 @@ def lib() -> ctypes.CDLL:
     vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.attn_fwd.restype = i
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
+    L.attn_fwd_fp8_scaled.restype = i
+    L.attn_fwd_fp8_scaled.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, i, vp, vp, i, i, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -119,6 +121,44 @@ def attn_fwd(q, k, v, causal: bool, scale: Optional[float] = None, descale_q=Non
     st = lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, N, d,
                         float(scale), int(bool(causal)), code, ptrs[0], ptrs[1], ptrs[2], _stream_handle(stream))
     _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_fp8_scaled(q, k, v, causal: bool, descale_q, descale_k, descale_v, scale: Optional[float] = None,
+                        out=None, lse=None, stream=None):
+    """attn_fwd for e4m3 q/k/v with descale factors per (batch, head).
+
+    ``descale_q`` is a float32 CUDA tensor of shape [B, H] (or any shape broadcastable to it by
+    strides, e.g. [1, H] expanded); ``descale_k`` and ``descale_v`` are [B, Hkv] with the SAME
+    strides as each other. Strides are taken from the tensors (a stride of 0 repeats a value).
+    """
+    import torch
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float8_e4m3fn:
+            raise ValueError(f"{name} must be a contiguous float8_e4m3fn CUDA tensor")
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d]")
+    dq = descale_q.expand(B, H)
+    dk = descale_k.expand(B, Hkv)
+    dv = descale_v.expand(B, Hkv)
+    for name, t in (("descale_q", dq), ("descale_k", dk), ("descale_v", dv)):
+        if t.dtype != torch.float32 or not t.is_cuda:
+            raise ValueError(f"{name} must be a float32 CUDA tensor")
+    if dk.stride() != dv.stride():
+        raise ValueError("descale_k and descale_v must share strides")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd_fp8_scaled(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                                   Hkv, N, d, float(scale), int(bool(causal)), dq.data_ptr(), dq.stride(0),
+                                   dq.stride(1), dk.data_ptr(), dv.data_ptr(), dk.stride(0), dk.stride(1),
+                                   _stream_handle(stream))
+    _check(st, "attn_fwd_fp8_scaled")
     return out, lse
 
 

@@ -219,9 +219,15 @@ cudaError_t dispatch_d(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t
 
 extern "C" {
 
-attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
-                       int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
-                       const float* descale_k, const float* descale_v, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The prefill forward behind attn_fwd and attn_fwd_fp8_scaled. ds: descale element strides
+// (q by batch, q by head, k by batch, k by kv head, v by batch, v by kv head); all 0 = per tensor.
+attn_status_t prefill_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                              int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
+                              const float* descale_k, const float* descale_v, const int* ds, cudaStream_t stream) {
   attn_status_t st = check_shape(B, H, Hkv, N, d, scale, dtype);
   if (st != ATTN_OK) return st;
   const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
@@ -253,6 +259,12 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
   p.descale_q = descale_q;
   p.descale_k = descale_k;
   p.descale_v = descale_v;
+  p.dq_sb = ds[0];
+  p.dq_sh = ds[1];
+  p.dk_sb = ds[2];
+  p.dk_sh = ds[3];
+  p.dv_sb = ds[4];
+  p.dv_sh = ds[5];
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
@@ -277,6 +289,28 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
     default: e = dispatch_d<256>(a, causal != 0, fp8, stream); break;
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
+                       int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
+                       const float* descale_k, const float* descale_v, cudaStream_t stream) {
+  static const int per_tensor[6] = {0, 0, 0, 0, 0, 0};
+  return prefill_forward(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, dtype, descale_q, descale_k, descale_v,
+                         per_tensor, stream);
+}
+
+attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                  int Hkv, int N, int d, float scale, int causal, const float* descale_q,
+                                  int q_stride_b, int q_stride_h, const float* descale_k, const float* descale_v,
+                                  int kv_stride_b, int kv_stride_h, cudaStream_t stream) {
+  if (q_stride_b < 0 || q_stride_h < 0 || kv_stride_b < 0 || kv_stride_h < 0) return ATTN_ERR_INVALID_ARG;
+  const int ds[6] = {q_stride_b, q_stride_h, kv_stride_b, kv_stride_h, kv_stride_b, kv_stride_h};
+  return prefill_forward(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, ATTN_DTYPE_FP8_E4M3, descale_q, descale_k,
+                         descale_v, ds, stream);
 }
 
 size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_dtype_t dtype) {

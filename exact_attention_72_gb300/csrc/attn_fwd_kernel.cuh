@@ -42,9 +42,10 @@ namespace gb300 {
 struct AttnParams {
   void* o;                  // bf16 [B, N, H, D]
   float* lse;               // fp32 [B, H, N]
-  const float* descale_q;   // fp8 only: one fp32 each (device)
-  const float* descale_k;
-  const float* descale_v;
+  const float* descale_q;   // fp8 only: descale of q at [b * dq_sb + h * dq_sh] (h: query head)
+  const float* descale_k;   // fp8 only: descale of k at [b * dk_sb + kvh * dk_sh]
+  const float* descale_v;   // fp8 only: descale of v at [b * dv_sb + kvh * dv_sh]
+  int dq_sb, dq_sh, dk_sb, dk_sh, dv_sb, dv_sh;   // element strides; all 0 = one value per tensor
   int B, H, Hkv, N;         // N: query rows per (batch, head) (prefill: also the key count)
   float scale_log2;         // scale * log2(e)
   int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head) / per (batch, kv head)
@@ -554,8 +555,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qt = warp >> 2;                  // Q tile of this warpgroup
     const int r = ((warp & 3) << 5) + lane;    // row within the Q tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    const float s = p.scale_log2 * (C::FP8 ? __ldg(p.descale_q) * __ldg(p.descale_k) : 1.0f);
-    const float out_scale = C::FP8 ? __ldg(p.descale_v) : 1.0f;
     uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
@@ -566,6 +565,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int n = kv_tiles_for<C>(tc, qt, p);
       if (n == 0) continue;
       const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
+      // Score scale (log2 units) and output scale of this row's head (FP8: descales per tensor or
+      // per head; split-KV rows of one tile belong to different query heads of the group).
+      const int h_row = C::SPLIT ? tc.h * p.G + r % p.G : tc.h;
+      const int kvh_row = C::SPLIT ? tc.h : tc.h / p.G;
+      float s = p.scale_log2;
+      float out_scale = 1.0f;
+      if (C::FP8) {
+        s *= __ldg(p.descale_q + tc.b * p.dq_sb + h_row * p.dq_sh) * __ldg(p.descale_k + tc.b * p.dk_sb + kvh_row * p.dk_sh);
+        out_scale = __ldg(p.descale_v + tc.b * p.dv_sb + kvh_row * p.dv_sh);
+      }
       float m = -INFINITY;   // running max of s * x (log2 units), used as the exponent shift
       float l = 0.0f;        // running sum of exp2(s * x - m)
       for (int j = 0; j < n; ++j) {

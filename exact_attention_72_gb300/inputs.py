@@ -140,6 +140,16 @@ def quantize_e4m3(x: torch.Tensor):
     return y.to(torch.float8_e4m3fn), float(descale)
 
 
+def quantize_e4m3_per_head(x: torch.Tensor):
+    """Per-(batch, head) e4m3 quantisation of x [B, N, H, d]: returns (x8, descale [B, H]) with
+    x[b, :, h, :] ~= x8[b, :, h, :] * descale[b, h]."""
+    x = x.to(torch.float32)
+    amax = x.abs().amax(dim=(1, 3))                                   # [B, H]
+    descale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax)).to(torch.float32)
+    y = (x / descale[:, None, :, None]).clamp_(-E4M3_MAX, E4M3_MAX)
+    return y.to(torch.float8_e4m3fn), descale
+
+
 def make_inputs(w: Workload, seed: Optional[int] = None) -> AttnInputs:
     """Draw the seeded inputs of workload ``w`` on the CPU."""
     g = torch.Generator(device="cpu")

@@ -75,6 +75,23 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        const float* descale_v, cudaStream_t stream);
 
 /*
+ * attn_fwd_fp8_scaled — attn_fwd for e4m3 q, k, v with descale factors that vary by batch and
+ * head instead of one per tensor. The value used for an element of q in batch b, query head h
+ * is x8 * descale_q[b * q_stride_b + h * q_stride_h]; for k and v in batch b, kv head g it is
+ * x8 * descale_{k,v}[b * kv_stride_b + g * kv_stride_h]. Strides are in elements (>= 0); all 0
+ * reproduces the per-tensor attn_fwd. Per-head scales keep more of e4m3's few mantissa bits when
+ * heads differ in magnitude: "flash-attention-3" (ai.thesatyajit.com), "FP8 is a different
+ * kernel" (descale pointers with strides).
+ *   descale arrays: DEVICE fp32, large enough for every (b, head) the strides address.
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128).
+ */
+attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, void* o,
+                                  float* lse, int B, int H, int Hkv, int N, int d, float scale,
+                                  int causal, const float* descale_q, int q_stride_b,
+                                  int q_stride_h, const float* descale_k, const float* descale_v,
+                                  int kv_stride_b, int kv_stride_h, cudaStream_t stream);
+
+/*
  * attn_fwd_host — the same operation on HOST buffers: copies q, k, v (and the three fp8
  * descales, given here as HOST pointers to one float each) to device buffers owned by the
  * caller (`workspace`, at least attn_fwd_host_workspace_bytes(...) bytes of device memory,

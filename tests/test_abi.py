@@ -102,3 +102,18 @@ def test_splitkv_validation(lib):
     need = binding.attn_fwd_splitkv_workspace_bytes(2, 32, 1, 128, 16)
     assert need >= 16 * 2 * 32 * 1 * (128 + 1) * 4
     assert binding.attn_fwd_splitkv_workspace_bytes(1, 1, 1, 128, 0) == 0
+
+
+def test_fp8_scaled_validation(lib):
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+
+    def call(B=1, H=4, Hkv=2, N=256, d=128, sqb=0, sqh=1, skb=0, skh=1, dq=1 << 12, dk=1 << 13, dv=1 << 14):
+        return lib.attn_fwd_fp8_scaled(1 << 16, 1 << 20, 1 << 24, 1 << 26, 1 << 27, B, H, Hkv, N, d, 0.1, 1,
+                                       dq, sqb, sqh, dk, dv, skb, skh, None)
+
+    assert call(sqh=-1) == INV
+    assert call(skb=-4) == INV
+    assert call(dq=0) == INV                         # descale pointers are required
+    assert call(dv=0) == INV
+    assert call(N=0) == INV
+    assert call(d=64) == UNS                         # e4m3 is built for d = 128 only
