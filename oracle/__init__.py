@@ -4,9 +4,11 @@ TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke entry point and by th
 benchmark's CPU-baseline leg, never by the library. It shares no code with the
 CUDA path. ``attention`` is the two-pass definition; ``online_softmax`` is an
 independently written tiled recurrence used to cross-check it on tiny inputs.
+``fp8_quant`` holds the e4m3 block quantisation and Hadamard rotation.
 """
 from .attention import attention_forward, attention_head, kv_head, probabilities, scores, softmax_two_pass
 from .online_softmax import attention_online
+from . import fp8_quant
 
 __all__ = ["attention_forward", "attention_head", "kv_head", "probabilities", "scores",
-           "softmax_two_pass", "attention_online"]
+           "softmax_two_pass", "attention_online", "fp8_quant"]
