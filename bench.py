@@ -217,10 +217,24 @@ def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
         key = (b, h)
         if key not in cache:
             cache.clear()
-            def f64(t, hh, s):
-                a = t[b, :, hh, :].float().double().numpy()
-                return a * np.float64(np.float32(s)) if t.element_size() == 1 else a
-            cache[key] = (f64(x.q, h, x.descale_q), f64(x.k, h // g, x.descale_k), f64(x.v, h // g, x.descale_v))
+            if w.dtype == "fp8_block":
+                # the oracle's own block quantisation of this head (q, k rotated), then attention of
+                # the dequantised values: the rotated q' k'^T equals the scores of the rotation's inputs
+                from oracle import fp8_quant as fq
+                signs = fp8_block_signs(w).double().numpy()
+
+                def blocks(t, hh, rows, sg):
+                    a = t[b:b + 1, :, hh:hh + 1, :].float().double().numpy()
+                    c, ds = fq.quantize_blocks(a, rows, sg)
+                    return fq.dequantize_blocks(c, ds, rows)[0, :, 0, :]
+                cache[key] = (blocks(x.q, h, 128, signs), blocks(x.k, h // g, 64, signs),
+                              blocks(x.v, h // g, w.n_keys, None))
+            else:
+                def f64(t, hh, s):
+                    a = t[b, :, hh, :].float().double().numpy()
+                    return a * np.float64(np.float32(s)) if t.element_size() == 1 else a
+                cache[key] = (f64(x.q, h, x.descale_q), f64(x.k, h // g, x.descale_k),
+                              f64(x.v, h // g, x.descale_v))
         q, k, v = cache[key]
         t0 = time.perf_counter()
         oracle.attention_head(q, k, v, w.scale, w.causal, rows=rows)
@@ -231,6 +245,12 @@ def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
     desc = (f"{steps} blocks of {block_rows} query rows (full score rows, fp64) from heads of the "
             f"{w.name} workload; FLOPs credited by the metric's convention")
     return (flops / elapsed / 1e12 if elapsed > 0 else 0.0), desc, elapsed, steps
+
+
+def fp8_block_signs(w):
+    """Random signs of the Hadamard rotation of the block-scaled e4m3 workload."""
+    from exact_attention_72_gb300 import inputs
+    return inputs.hadamard_signs(w.d, w.seed + 7)
 
 
 def cores_used() -> int:
@@ -265,6 +285,9 @@ def run_reference(args, w, x):
 
 def config_of(w):
     extra = {"Nk": w.n_keys, "splits": w.splits} if w.name in DECODE_NAMES else {}
+    if w.dtype == "fp8_block":
+        extra = {"quantisation": "per step on the GPU: q e4m3 blocks of 128 rows and k of 64 rows after a "
+                                 "random Hadamard rotation, v one descale per head"}
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal, **extra,
             "qkv_dtype": w.dtype, "k_outliers": w.k_outlier_frac,
             "l2": "flushed before every step (256 MiB write, outside the timed events)",
@@ -280,10 +303,11 @@ def run_ours(args, w, x):
     binding.lib()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    fp8 = w.dtype == "fp8_e4m3"
+    fp8 = w.dtype in ("fp8_e4m3", "fp8_block")
+    block = w.dtype == "fp8_block"
     q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
     kw = {}
-    if fp8:
+    if w.dtype == "fp8_e4m3":
         kw = {n: torch.tensor([s], dtype=torch.float32, device=dev)
               for n, s in (("descale_q", x.descale_q), ("descale_k", x.descale_k), ("descale_v", x.descale_v))}
     o = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16, device=dev)
@@ -295,9 +319,25 @@ def run_ours(args, w, x):
         ws = torch.empty(binding.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.N, w.d, w.splits), dtype=torch.uint8,
                          device=dev)
 
-    def step():
+    if block:
+        signs = fp8_block_signs(w).to(dev)
+        q8, k8, v8 = (torch.empty(t.shape, dtype=torch.float8_e4m3fn, device=dev) for t in (q, k, v))
+        dq = torch.empty((w.B, w.H, -(-w.N // 128)), dtype=torch.float32, device=dev)
+        dk = torch.empty((w.B, w.Hkv, -(-w.N // 64)), dtype=torch.float32, device=dev)
+        dv = torch.empty((w.B, w.Hkv, 1), dtype=torch.float32, device=dev)
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if block else None
+
+    def step(i=None):
         if decode:
             binding.attn_fwd_splitkv(q, k, v, w.splits, scale=w.scale, workspace=ws, out=o, lse=lse, **kw)
+        elif block:
+            binding.quantize_e4m3(q, 128, signs, out=q8, descale=dq)
+            binding.quantize_e4m3(k, 64, signs, out=k8, descale=dk)
+            binding.quantize_e4m3(v, w.N, out=v8, descale=dv)
+            if i is not None:
+                mids[i].record(stream)
+            binding.attn_fwd_fp8_blockscaled(q8, k8, v8, w.causal, dq, dk, dv.view(w.B, w.Hkv), scale=w.scale,
+                                             out=o, lse=lse)
         else:
             binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, **kw)
 
@@ -319,21 +359,33 @@ def run_ours(args, w, x):
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
-        step()
+        step(i)
         ends[i].record(stream)
     torch.cuda.synchronize()
     barrier(dist)
     t_host1 = time.time()
     time.sleep(0.12)
     sampler.stop()
-    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms per launch
+    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms per step
+    prepass = None
+    if block:
+        # the attention launch alone (the roofline's kernel), and the quantisation before it
+        pre = [s.elapsed_time(m) for s, m in zip(starts, mids)]
+        durs_attn = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+        pre_ms = statistics.fmean(pre)
+        qkv_bytes = (w.B * w.N * (w.H + 2 * w.Hkv) * w.d) * 3 + 4 * (dq.numel() + dk.numel() + dv.numel())
+        hbm, hbm_src = hbm_peak()
+        prepass = {"kernel": "quantize_kernel (q, k rotated; v per head)", "ms": pre_ms,
+                   "algorithmic_bytes": qkv_bytes, "GB/s": qkv_bytes / (pre_ms * 1e-3) / 1e9,
+                   "frac_hbm": qkv_bytes / (pre_ms * 1e-3) / 1e9 / hbm, "peak_source": hbm_src}
     st, detail = binding.attn_get_status()
     if st != binding.ATTN_OK:
         raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
     local_ms = sum(durs)
     total_ms = max_over_ranks(dist, local_ms)
     value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
-    mean_ms = statistics.fmean(durs)
+    kdurs = durs_attn if block else durs
+    mean_ms = statistics.fmean(kdurs)
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
     peak_bf16, peak_src = peaks()
     peak = peak_bf16 * (2.0 if fp8 else 1.0)
@@ -351,11 +403,13 @@ def run_ours(args, w, x):
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                     "frac": achieved / peak, "traffic": measured_traffic(w.name),
                     "kernel": "attn_fwd_kernel", "peak_source": peak_src,
-                    "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}}
+                    "kernel_ms": {"mean": mean_ms, "min": min(kdurs), "max": max(kdurs)}}
+        if prepass is not None:
+            roofline["prepass"] = prepass
 
     e2e = None
     if not args.no_e2e and not decode:
-        e2e = measure_e2e(args, w, x, dev, dist, world)
+        e2e = (measure_e2e_block if block else measure_e2e)(args, w, x, dev, dist, world)
 
     clocks = sampler.summary(t_host0, t_host1)
     cpu = None
@@ -370,11 +424,65 @@ def run_ours(args, w, x):
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
             "config": config_of(w),
             "roofline": roofline,
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * (2 if decode else 1), "clocks": clocks,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * launches_per_step(w), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def launches_per_step(w):
+    """Kernels of this library launched by one step."""
+    if w.name in DECODE_NAMES:
+        return 2                                  # split-KV forward + combine
+    if w.dtype == "fp8_block":
+        v_launches = 1 if w.N <= 128 else 3       # one block per head: maxima, codes, descales
+        return 1 + 1 + v_launches + 1             # quantise q, k, v; block-scaled forward
+    return 1
+
+
+def measure_e2e_block(args, w, x, dev, dist, world):
+    """Block-scaled e4m3 chain end to end: pinned bf16 q/k/v copied in, quantised and attended on
+    the GPU through the public binding, o and lse copied back to pinned host memory."""
+    import torch
+    from exact_attention_72_gb300 import binding
+    qh, kh, vh = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
+    oh = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (qh, kh, vh))
+    signs = fp8_block_signs(w).to(dev)
+    o = torch.empty(oh.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(lh.shape, dtype=torch.float32, device=dev)
+
+    def step():
+        for d_, h_ in ((qd, qh), (kd, kh), (vd, vh)):
+            d_.copy_(h_, non_blocking=True)
+        q8, dq = binding.quantize_e4m3(qd, 128, signs)
+        k8, dk = binding.quantize_e4m3(kd, 64, signs)
+        v8, dv = binding.quantize_e4m3(vd, w.N)
+        binding.attn_fwd_fp8_blockscaled(q8, k8, v8, w.causal, dq, dk, dv.view(w.B, w.Hkv), scale=w.scale, out=o,
+                                         lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(dist)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    return {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+            "entry_point": "quantize_e4m3 + attn_fwd_fp8_blockscaled on pinned host buffers"}
 
 
 def measure_e2e(args, w, x, dev, dist, world):
@@ -416,7 +524,8 @@ def main(argv=None):
     args = parse_args(argv)
     from exact_attention_72_gb300 import inputs
     name = args.workload or inputs.HEADLINE
-    w = inputs.WORKLOADS[name] if name in inputs.WORKLOADS else inputs.DECODE_WORKLOADS[name]
+    table = {**inputs.WORKLOADS, **inputs.DECODE_WORKLOADS, **inputs.FP8_BLOCK_WORKLOADS}
+    w = table[name]
     if args.batch is not None:
         w = w.replace(B=args.batch, name=f"{w.name}_b{args.batch}")
     rank, world, _ = rank_info()

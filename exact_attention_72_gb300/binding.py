@@ -45,6 +45,12 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
     L.attn_fwd_fp8_scaled.restype = i
     L.attn_fwd_fp8_scaled.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, i, i, vp, vp, i, i, vp]
+    L.attn_fwd_fp8_blockscaled.restype = i
+    L.attn_fwd_fp8_blockscaled.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, vp, vp, vp]
+    L.attn_quantize_e4m3.restype = i
+    L.attn_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp]
+    L.attn_quantize_e4m3_descale_count.restype = sz
+    L.attn_quantize_e4m3_descale_count.argtypes = [i, i, i, i]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -160,6 +166,68 @@ def attn_fwd_fp8_scaled(q, k, v, causal: bool, descale_q, descale_k, descale_v, 
                                    _stream_handle(stream))
     _check(st, "attn_fwd_fp8_scaled")
     return out, lse
+
+
+ATTN_FP8_Q_BLOCK = 128   # query rows per q descale block (attn_fwd_fp8_blockscaled)
+ATTN_FP8_K_BLOCK = 64    # keys per k descale block
+
+
+def attn_fwd_fp8_blockscaled(q, k, v, causal: bool, descale_q, descale_k, descale_v, scale: Optional[float] = None,
+                             out=None, lse=None, stream=None):
+    """attn_fwd for e4m3 q/k/v with block descales: descale_q [B, H, ceil(N/128)], descale_k
+    [B, Hkv, ceil(N/64)], descale_v [B, Hkv] (contiguous float32 CUDA tensors)."""
+    import torch
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.float8_e4m3fn:
+            raise ValueError(f"{name} must be a contiguous float8_e4m3fn CUDA tensor")
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, N, Hkv, d]")
+    want = {"descale_q": (B, H, -(-N // ATTN_FP8_Q_BLOCK)), "descale_k": (B, Hkv, -(-N // ATTN_FP8_K_BLOCK)),
+            "descale_v": (B, Hkv)}
+    for (name, shape), t in zip(want.items(), (descale_q, descale_k, descale_v)):
+        if tuple(t.shape) != shape or t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape {shape}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    st = lib().attn_fwd_fp8_blockscaled(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                                        H, Hkv, N, d, float(scale), int(bool(causal)), descale_q.data_ptr(),
+                                        descale_k.data_ptr(), descale_v.data_ptr(), _stream_handle(stream))
+    _check(st, "attn_fwd_fp8_blockscaled")
+    return out, lse
+
+
+def quantize_e4m3(x, block_rows: int, signs=None, out=None, descale=None, stream=None):
+    """e4m3 codes of bf16 x [B, N, Hx, d] with a descale per block of ``block_rows`` rows of one
+    (batch, head), optionally after the rotation diag(signs) H_d / sqrt(d). Returns (x8, descale)
+    with descale float32 [B, Hx, ceil(N / block_rows)]."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous() or x.dtype != torch.bfloat16 or x.dim() != 4:
+        raise ValueError("x must be a contiguous bfloat16 CUDA tensor [B, N, Hx, d]")
+    B, N, Hx, d = x.shape
+    nblk = -(-N // block_rows) if block_rows > 0 else 0
+    if out is None:
+        out = torch.empty((B, N, Hx, d), dtype=torch.float8_e4m3fn, device=x.device)
+    if descale is None:
+        descale = torch.empty((B, Hx, nblk), dtype=torch.float32, device=x.device)
+    sp = 0
+    if signs is not None:
+        if not signs.is_cuda or signs.dtype != torch.float32 or signs.numel() != d or not signs.is_contiguous():
+            raise ValueError("signs must be a contiguous float32 CUDA tensor of d values")
+        sp = signs.data_ptr()
+    st = lib().attn_quantize_e4m3(x.data_ptr(), out.data_ptr(), descale.data_ptr(), B, N, Hx, d, int(block_rows),
+                                  sp or None, _stream_handle(stream))
+    _check(st, "attn_quantize_e4m3")
+    return out, descale
+
+
+def attn_quantize_e4m3_descale_count(B: int, N: int, Hx: int, block_rows: int) -> int:
+    return int(lib().attn_quantize_e4m3_descale_count(B, N, Hx, block_rows))
 
 
 def attn_fwd_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, descale_q=None, descale_k=None,

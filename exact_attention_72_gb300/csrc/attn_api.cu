@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -153,6 +154,21 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int head
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 [B, N, heads, d] tensor -> 4-D map (d, N, heads, B) whose box is 64 columns of box_rows
+// rows of one (batch, head) with the 128-byte swizzle: the e4m3 quantiser's input, loaded as d/64
+// boxes per chunk. Rows past N read as zeros.
+bool make_rows_map(CUtensorMap* m, const void* base, int d, int N, int heads, int B, int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)heads * d * 2, (cuuint64_t)d * 2, (cuuint64_t)N * heads * d * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Packed GQA view of q [B, Nq, H, d] for split-KV decode: 5-D map (d, G, Nq, Hkv, B) so one box
 // (128-byte row, G heads, 128 / G positions, 1, 1) is 128 query rows of one kv head's group.
 bool make_map_q_packed(CUtensorMap* m, const void* base, bool fp8, int d, int Nq, int H, int Hkv, int B) {
@@ -223,8 +239,9 @@ extern "C" {
 
 namespace {
 
-// The prefill forward behind attn_fwd and attn_fwd_fp8_scaled. ds: descale element strides
-// (q by batch, q by head, k by batch, k by kv head, v by batch, v by kv head); all 0 = per tensor.
+// The prefill forward behind attn_fwd and the fp8 entries with finer descales. ds: descale
+// element strides (q by batch, q by head, q by 128-row block, k by batch, k by kv head, k by
+// 64-key block, v by batch, v by kv head); all 0 = one descale per tensor.
 attn_status_t prefill_forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
                               int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
                               const float* descale_k, const float* descale_v, const int* ds, cudaStream_t stream) {
@@ -261,10 +278,12 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   p.descale_v = descale_v;
   p.dq_sb = ds[0];
   p.dq_sh = ds[1];
-  p.dk_sb = ds[2];
-  p.dk_sh = ds[3];
-  p.dv_sb = ds[4];
-  p.dv_sh = ds[5];
+  p.dq_sm = ds[2];
+  p.dk_sb = ds[3];
+  p.dk_sh = ds[4];
+  p.dk_sn = ds[5];
+  p.dv_sb = ds[6];
+  p.dv_sh = ds[7];
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;
@@ -298,7 +317,7 @@ extern "C" {
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Hkv,
                        int N, int d, float scale, int causal, attn_dtype_t dtype, const float* descale_q,
                        const float* descale_k, const float* descale_v, cudaStream_t stream) {
-  static const int per_tensor[6] = {0, 0, 0, 0, 0, 0};
+  static const int per_tensor[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   return prefill_forward(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, dtype, descale_q, descale_k, descale_v,
                          per_tensor, stream);
 }
@@ -308,7 +327,20 @@ attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, v
                                   int q_stride_b, int q_stride_h, const float* descale_k, const float* descale_v,
                                   int kv_stride_b, int kv_stride_h, cudaStream_t stream) {
   if (q_stride_b < 0 || q_stride_h < 0 || kv_stride_b < 0 || kv_stride_h < 0) return ATTN_ERR_INVALID_ARG;
-  const int ds[6] = {q_stride_b, q_stride_h, kv_stride_b, kv_stride_h, kv_stride_b, kv_stride_h};
+  const int ds[8] = {q_stride_b, q_stride_h, 0, kv_stride_b, kv_stride_h, 0, kv_stride_b, kv_stride_h};
+  return prefill_forward(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, ATTN_DTYPE_FP8_E4M3, descale_q, descale_k,
+                         descale_v, ds, stream);
+}
+
+attn_status_t attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                       int H, int Hkv, int N, int d, float scale, int causal,
+                                       const float* descale_q, const float* descale_k, const float* descale_v,
+                                       cudaStream_t stream) {
+  if (N < 1 || H < 1 || Hkv < 1) return ATTN_ERR_INVALID_ARG;
+  const long long nqb = (N + ATTN_FP8_Q_BLOCK - 1) / ATTN_FP8_Q_BLOCK;
+  const long long nkb = (N + ATTN_FP8_K_BLOCK - 1) / ATTN_FP8_K_BLOCK;
+  if ((long long)B * H * nqb > INT_MAX || (long long)B * Hkv * nkb > INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const int ds[8] = {(int)(H * nqb), (int)nqb, 1, (int)(Hkv * nkb), (int)nkb, 1, Hkv, 1};
   return prefill_forward(q, k, v, o, lse, B, H, Hkv, N, d, scale, causal, ATTN_DTYPE_FP8_E4M3, descale_q, descale_k,
                          descale_v, ds, stream);
 }
@@ -482,6 +514,67 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   if (e != cudaSuccess) return ATTN_ERR_CUDA;
   e = gb300::launch_splitkv_combine(part_o, part_lse, o, lse, S, B, H, Nq, d, di->num_sms, stream);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_quantize_e4m3_descale_count(int B, int N, int Hx, int block_rows) {
+  if (B < 1 || N < 1 || Hx < 1 || block_rows < 1) return 0;
+  return (size_t)B * Hx * (size_t)((N + (long long)block_rows - 1) / block_rows);
+}
+
+attn_status_t attn_quantize_e4m3(const void* x, void* x8, float* descale, int B, int N, int Hx, int d,
+                                 int block_rows, const float* signs, cudaStream_t stream) {
+  if (!x || !x8 || !descale) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || N < 1 || Hx < 1 || block_rows < 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(descale, 4) || (signs && !aligned(signs, 4)))
+    return ATTN_ERR_INVALID_ARG;
+  const long long nblk = (N + (long long)block_rows - 1) / block_rows;
+  // Chunks (one TMA load each, at most 128 rows of one batch and head): 128 rows holding whole
+  // blocks when the block size is a power of two from 8 to 128; one block when it is another size
+  // below 128; 128-row pieces of longer blocks. Rows split into spans of whole chunks.
+  int chunk_rows, span, cps;
+  if (block_rows <= 128) {
+    chunk_rows = (block_rows >= 8 && 128 % block_rows == 0) ? 128 : block_rows;
+    span = chunk_rows;
+    cps = 1;
+  } else {
+    chunk_rows = 128;
+    span = block_rows;
+    cps = (block_rows + 127) / 128;
+  }
+  const long long nspan = (N + (long long)span - 1) / span;
+  if ((long long)B * Hx * nspan * cps > INT_MAX || (long long)B * N * Hx > INT_MAX ||
+      (long long)B * Hx * nblk > INT_MAX)
+    return ATTN_ERR_UNSUPPORTED;
+  // The codes and descales must not overlap x: other CTAs may still be reading it.
+  const size_t elems = (size_t)B * N * Hx * d;
+  const uintptr_t xb = (uintptr_t)x, xe = xb + elems * 2;
+  const uintptr_t qb = (uintptr_t)x8, qe = qb + elems;
+  const uintptr_t db = (uintptr_t)descale, de = db + (size_t)(B * Hx * nblk) * 4;
+  if ((qb < xe && xb < qe) || (db < xe && xb < de) || (db < qe && qb < de)) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  gb300::QuantLaunch q;
+  memset(&q, 0, sizeof(q));
+  if (!make_rows_map(&q.tm_x, x, d, N, Hx, B, chunk_rows)) return ATTN_ERR_CUDA;
+  q.x8 = static_cast<uint8_t*>(x8);
+  q.descale = descale;
+  q.signs = signs;
+  q.B = B;
+  q.N = N;
+  q.Hx = Hx;
+  q.d = d;
+  q.block_rows = block_rows;
+  q.nblk = (int)nblk;
+  q.span = span;
+  q.cps = cps;
+  q.nspan = (int)nspan;
+  q.chunk_rows = chunk_rows;
+  q.grp_rows = std::min(block_rows, chunk_rows);
+  q.status = di->status;
+  q.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
+  q.num_sms = di->num_sms;
+  return gb300::launch_quantize_e4m3(q, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {

@@ -42,10 +42,14 @@ namespace gb300 {
 struct AttnParams {
   void* o;                  // bf16 [B, N, H, D]
   float* lse;               // fp32 [B, H, N]
-  const float* descale_q;   // fp8 only: descale of q at [b * dq_sb + h * dq_sh] (h: query head)
-  const float* descale_k;   // fp8 only: descale of k at [b * dk_sb + kvh * dk_sh]
-  const float* descale_v;   // fp8 only: descale of v at [b * dv_sb + kvh * dv_sh]
-  int dq_sb, dq_sh, dk_sb, dk_sh, dv_sb, dv_sh;   // element strides; all 0 = one value per tensor
+  // fp8 only. Descales are read at element offsets (all strides 0 = one value per tensor):
+  //   q: b * dq_sb + h * dq_sh + (pos / 128) * dq_sm      (h query head, pos query position)
+  //   k: b * dk_sb + kvh * dk_sh + (key / 64) * dk_sn     (kvh kv head, key key position)
+  //   v: b * dv_sb + kvh * dv_sh
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
+  int dq_sb, dq_sh, dq_sm, dk_sb, dk_sh, dk_sn, dv_sb, dv_sh;
   int B, H, Hkv, N;         // N: query rows per (batch, head) (prefill: also the key count)
   float scale_log2;         // scale * log2(e)
   int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head) / per (batch, kv head)
@@ -565,21 +569,35 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const int n = kv_tiles_for<C>(tc, qt, p);
       if (n == 0) continue;
       const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
-      // Score scale (log2 units) and output scale of this row's head (FP8: descales per tensor or
-      // per head; split-KV rows of one tile belong to different query heads of the group).
+      // Score scale (log2 units) and output scale of this row (FP8: descales per tensor, per head
+      // or per block; split-KV rows of one tile belong to different query heads of the group).
       const int h_row = C::SPLIT ? tc.h * p.G + r % p.G : tc.h;
       const int kvh_row = C::SPLIT ? tc.h : tc.h / p.G;
-      float s = p.scale_log2;
+      float s = p.scale_log2;        // bf16: the score scale; fp8: times the q (and k) descales
+      float s_q = s;                 // fp8 with K blocks: scale_log2 * descale_q of this row
       float out_scale = 1.0f;
+      const float* dk_row = nullptr;
       if (C::FP8) {
-        s *= __ldg(p.descale_q + tc.b * p.dq_sb + h_row * p.dq_sh) * __ldg(p.descale_k + tc.b * p.dk_sb + kvh_row * p.dk_sh);
+        const int pos = C::SPLIT ? min(row0 + r / p.G, p.N - 1) : row0;
+        s_q = s * __ldg(p.descale_q + tc.b * p.dq_sb + h_row * p.dq_sh + (pos >> 7) * p.dq_sm);
+        dk_row = p.descale_k + tc.b * p.dk_sb + kvh_row * p.dk_sh;
+        s = p.dk_sn ? s_q : s_q * __ldg(dk_row);
         out_scale = __ldg(p.descale_v + tc.b * p.dv_sb + kvh_row * p.dv_sh);
       }
+      const int n_kblk = (Nk + 63) >> 6;   // 64-key descale blocks
       float m = -INFINITY;   // running max of s * x (log2 units), used as the exponent shift
       float l = 0.0f;        // running sum of exp2(s * x - m)
       for (int j = 0; j < n; ++j) {
         const int buf = C::NQ == 2 ? qt : (j & 1);
         const uint32_t s_col = buf ? C::S_COL1 : C::S_COL0;
+        // Scales of the two 64-key halves of this tile (they differ only with K block descales;
+        // read before the wait so the load latency hides behind it).
+        float s_lo = s, s_hi = s;
+        if (C::FP8 && p.dk_sn) {
+          const int kb = 2 * (tc.j0 + j);
+          s_lo = s_q * __ldg(dk_row + kb * p.dk_sn);
+          s_hi = s_q * __ldg(dk_row + min(kb + 1, n_kblk - 1) * p.dk_sn);
+        }
         bool w = mbar_wait(smem_addr(&bar_s_full[buf]), s_cnt[buf] & 1, ctl, SITE_S_FULL);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (r == 0) ATTN_TRACE(4, qt, j);
@@ -616,9 +634,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // The first half is computed speculatively with the row's current shift m while the row
         // max of this tile is taken alongside it; only if some row's max moved by more than 8
         // (always on the first tile) is that half recomputed with the new shift.
-        const uint64_t s2 = f2_pack(s, s);
+        const uint64_t s2_lo = f2_pack(s_lo, s_lo), s2_hi = f2_pack(s_hi, s_hi);
         constexpr int PKN = C::FP8 ? 16 : 32;   // packed 32-bit P words per half
         auto exp_half = [&](int h, uint64_t nm2, uint32_t* pk, uint64_t& acc0, uint64_t& acc1) {
+          const uint64_t s2 = h ? s2_hi : s2_lo;
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
             const int cc = h * 64 + c;
@@ -647,17 +666,37 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t pk[PKN];
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
-        // Row max: eight independent chains of 3-input max.
-        float a8[8];
+        // Row max: eight independent chains of 3-input max (per 64-key half for fp8, whose halves
+        // may carry different K descales; the scales are positive, so max commutes with them).
+        float m_tile;
+        if constexpr (C::FP8) {
+          float mh[2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a8[i] = x[i];
+          for (int h = 0; h < 2; ++h) {
+            float a8[8];
 #pragma unroll
-        for (int c = 8; c + 16 <= 128; c += 16)
+            for (int i = 0; i < 8; ++i) a8[i] = x[h * 64 + i];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], x[c + i], x[c + 8 + i]);
+            for (int c = 8; c + 16 <= 64; c += 16)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a8[i] = fmaxf(a8[i], x[120 + i]);
-        const float m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
+              for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], x[h * 64 + c + i], x[h * 64 + c + 8 + i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a8[i] = fmaxf(a8[i], x[h * 64 + 56 + i]);
+            mh[h] = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7]));
+          }
+          m_tile = fmaxf(mh[0] * s_lo, mh[1] * s_hi);
+        } else {
+          float a8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a8[i] = x[i];
+#pragma unroll
+          for (int c = 8; c + 16 <= 128; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a8[i] = fmax3(a8[i], x[c + i], x[c + 8 + i]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a8[i] = fmaxf(a8[i], x[120 + i]);
+          m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
+        }
         if (r == 0) ATTN_TRACE(6, qt, j);
         float alpha = 1.0f;
         bool rescale = false;

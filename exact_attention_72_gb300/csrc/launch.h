@@ -22,6 +22,24 @@ cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream);
 cudaError_t launch_splitkv_combine(const float* part_o, const float* part_lse, void* o, float* lse, int S, int B,
                                    int H, int Nq, int D, int num_sms, cudaStream_t stream);
 
+// e4m3 block quantisation of bf16 rows (fp8_quantize.cu). Rows of one (batch, head) are cut into
+// spans of span rows (span = chunk_rows when blocks have at most 128 rows, else block_rows), and
+// each span into cps chunks of up to chunk_rows rows; one chunk is one TMA load. A chunk holds
+// chunk_rows / grp_rows groups of rows, each inside one block. tm_x: 4-D map of x (d, N, Hx, B),
+// box (64, chunk_rows, 1, 1), 128-byte swizzle.
+struct QuantLaunch {
+  CUtensorMap tm_x;
+  uint8_t* x8;              // [B, N, Hx, d] codes
+  float* descale;           // [B, Hx, nblk]
+  const float* signs;       // d values or null
+  int B, N, Hx, d, block_rows, nblk;
+  int span, cps, nspan, chunk_rows, grp_rows;
+  uint32_t* status;
+  unsigned long long timeout_ns;
+  int num_sms;
+};
+cudaError_t launch_quantize_e4m3(const QuantLaunch& q, cudaStream_t stream);
+
 // Rows of queries one CTA work tile covers for head dim d (two 128-row tiles for d <= 128).
 inline int rows_per_work_tile(int d) { return d <= 128 ? 256 : 128; }
 

@@ -45,7 +45,8 @@ class Workload:
     N: int
     d: int
     causal: bool
-    dtype: str = "bf16"            # "bf16" or "fp8_e4m3" (storage type of q, k, v)
+    dtype: str = "bf16"            # "bf16", "fp8_e4m3" (storage type of q, k, v), or "fp8_block":
+                                   # stored bf16, quantised on the GPU into e4m3 blocks each step
     seed: int = 1000
     k_outlier_frac: float = 0.0    # fraction of K entries replaced by +-k_outlier_mag
     k_outlier_mag: float = 8.0
@@ -110,6 +111,16 @@ DECODE_WORKLOADS = {
 }
 
 
+# Block-scaled e4m3 workload: bf16 inputs (K with outliers) quantised on the GPU every step (q in
+# blocks of 128 rows and k in blocks of 64 rows, both after the random Hadamard rotation; v with
+# one descale per head), then the block-scaled e4m3 forward. Same shape as the fp8 configuration.
+FP8_BLOCK_WORKLOADS = {
+    "fp8_block_hadamard_noncausal_n8192_d128": Workload("fp8_block_hadamard_noncausal_n8192_d128", B=1, H=16,
+                                                        Hkv=16, N=8192, d=128, causal=False, dtype="fp8_block",
+                                                        seed=1201, k_outlier_frac=0.005),
+}
+
+
 @dataclasses.dataclass
 class AttnInputs:
     """Stored inputs (what the kernel reads) plus their exact fp64 values."""
@@ -150,6 +161,13 @@ def quantize_e4m3_per_head(x: torch.Tensor):
     return y.to(torch.float8_e4m3fn), descale
 
 
+def hadamard_signs(d: int, seed: int) -> torch.Tensor:
+    """The d random signs (+-1, float32) of a random Hadamard rotation, drawn from ``seed``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    return torch.randint(0, 2, (d,), generator=g).to(torch.float32) * 2.0 - 1.0
+
+
 def make_inputs(w: Workload, seed: Optional[int] = None) -> AttnInputs:
     """Draw the seeded inputs of workload ``w`` on the CPU."""
     g = torch.Generator(device="cpu")
@@ -162,7 +180,7 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> AttnInputs:
         idx = torch.randperm(k.numel(), generator=g)[:n_out]
         sign = torch.randint(0, 2, (n_out,), generator=g).to(torch.float32) * 2.0 - 1.0
         k.view(-1)[idx] = sign * w.k_outlier_mag
-    if w.dtype == "bf16":
+    if w.dtype in ("bf16", "fp8_block"):
         return AttnInputs(q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
     if w.dtype == "fp8_e4m3":
         q8, sq = quantize_e4m3(q)

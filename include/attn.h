@@ -91,6 +91,60 @@ attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, v
                                   int q_stride_h, const float* descale_k, const float* descale_v,
                                   int kv_stride_b, int kv_stride_h, cudaStream_t stream);
 
+/* Rows per descale block of the block-scaled e4m3 forward: q in blocks of 128 query positions,
+ * k in blocks of 64 key positions, both within one (batch, head). */
+#define ATTN_FP8_Q_BLOCK 128
+#define ATTN_FP8_K_BLOCK 64
+
+/*
+ * attn_fwd_fp8_blockscaled — attn_fwd for e4m3 q, k, v with one descale per block: the score
+ * matrix is tiled into 128 x 64 blocks (128 query rows by 64 keys), q carries a descale per
+ * 128-row block and k one per 64-row block, so every block of scores has its own scale.
+ * "FlashAttention-3 Deep Dive" (mojostudio.in), section 4 "FP8 Block Quantization & Numerical
+ * Incoherence Elimination", per-block scaling.
+ *   descale_q: DEVICE fp32 [B, H, ceil(N / 128)]; the q value at (b, n, h, :) is
+ *              q8 * descale_q[b, h, n / 128].
+ *   descale_k: DEVICE fp32 [B, Hkv, ceil(N / 64)]; k at (b, n, g, :) is k8 * descale_k[b, g, n / 64].
+ *   descale_v: DEVICE fp32 [B, Hkv]; v at (b, n, g, :) is v8 * descale_v[b, g].
+ *   Descales must be positive and finite. attn_quantize_e4m3 writes codes and descales in these
+ *   layouts (block_rows 128 for q, 64 for k, N for v). q and k may both be rotated by the same
+ *   orthogonal matrix: the scores do not change.
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128).
+ */
+attn_status_t attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
+                                       float* lse, int B, int H, int Hkv, int N, int d,
+                                       float scale, int causal, const float* descale_q,
+                                       const float* descale_k, const float* descale_v,
+                                       cudaStream_t stream);
+
+/*
+ * attn_quantize_e4m3 — bf16 x [B, N, Hx, d] to e4m3 codes x8 [B, N, Hx, d] with one fp32
+ * descale per block of block_rows consecutive rows of one (batch, head) (the last block of a
+ * head may be shorter): descale = max |x'| / 448 over the block (1 if the block is all zero),
+ * x8 = e4m3(x' / descale), rounded to nearest even and saturated to +-448. x' is x, or, when
+ * signs is given, x R with R = diag(signs) H_d / sqrt(d), H_d the Sylvester Hadamard matrix:
+ * a random orthogonal rotation that spreads outliers across the row. Codes come from the
+ * unnormalised product x diag(signs) H_d; the 1/sqrt(d) factor goes into the stored descale.
+ * "FlashAttention-3 Deep Dive" (mojostudio.in), section 4: per-block scaling and Hadamard
+ * incoherence processing.
+ *   x:        DEVICE bf16, 16-byte aligned. Values must be finite.
+ *   x8:       DEVICE, 16-byte aligned, B*N*Hx*d bytes; must not overlap x.
+ *   descale:  DEVICE fp32 [B, Hx, ceil(N / block_rows)] (attn_quantize_e4m3_descale_count
+ *             entries); must not overlap x or x8.
+ *   signs:    DEVICE fp32 [d] of +-1 values, or NULL for no rotation. Other values are used as
+ *             given (the transform is then not orthogonal).
+ *   d in {64, 128, 256}; block_rows >= 1. Blocks of up to 128 rows take one launch; longer
+ *   blocks take a memset and three launches on the stream.
+ * Asynchronous on stream; allocates nothing. INVALID_ARG for null or misaligned pointers,
+ * non-positive sizes or overlapping buffers; UNSUPPORTED for other d or sizes past 32-bit
+ * indexing; ATTN_ERR_CUDA if a launch fails.
+ */
+attn_status_t attn_quantize_e4m3(const void* x, void* x8, float* descale, int B, int N, int Hx,
+                                 int d, int block_rows, const float* signs, cudaStream_t stream);
+
+/* Number of descales attn_quantize_e4m3 writes: B * Hx * ceil(N / block_rows) (0 if invalid). */
+size_t attn_quantize_e4m3_descale_count(int B, int N, int Hx, int block_rows);
+
 /*
  * attn_fwd_host — the same operation on HOST buffers: copies q, k, v (and the three fp8
  * descales, given here as HOST pointers to one float each) to device buffers owned by the

@@ -117,3 +117,27 @@ def test_fp8_scaled_validation(lib):
     assert call(dv=0) == INV
     assert call(N=0) == INV
     assert call(d=64) == UNS                         # e4m3 is built for d = 128 only
+
+
+def test_quantize_and_blockscaled_validation(lib):
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+
+    def q(x=1 << 20, x8=1 << 26, ds=1 << 28, B=1, N=256, Hx=2, d=128, R=64, signs=None):
+        return lib.attn_quantize_e4m3(x, x8, ds, B, N, Hx, d, R, signs, None)
+
+    assert q(x=0) == INV and q(x8=0) == INV and q(ds=0) == INV
+    assert q(R=0) == INV and q(N=0) == INV and q(Hx=0) == INV
+    assert q(d=96) == UNS and q(d=32) == UNS
+    assert q(x=(1 << 20) + 8) == INV                    # x not 16-byte aligned
+    assert q(ds=(1 << 28) + 2) == INV                   # descale not 4-byte aligned
+    assert q(x8=(1 << 20) + 1024) == INV                # codes overlap x
+    assert q(ds=(1 << 26) + 64) == INV                  # descales overlap the codes
+    assert binding.attn_quantize_e4m3_descale_count(2, 300, 3, 128) == 2 * 3 * 3
+    assert binding.attn_quantize_e4m3_descale_count(1, 300, 1, 0) == 0
+
+    def f(N=256, d=128, H=4, Hkv=2):
+        return lib.attn_fwd_fp8_blockscaled(1 << 16, 1 << 20, 1 << 24, 1 << 26, 1 << 27, 1, H, Hkv, N, d, 0.1, 1,
+                                            1 << 12, 1 << 13, 1 << 14, None)
+
+    assert f(N=0) == INV and f(H=0) == INV
+    assert f(d=64) == UNS
