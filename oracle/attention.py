@@ -44,10 +44,11 @@ def kv_head(h: int, H: int, Hkv: int) -> int:
 
 
 def scores(q_bh: np.ndarray, k_bh: np.ndarray, scale: float, causal: bool,
-           rows: np.ndarray | None = None) -> np.ndarray:
+           rows: np.ndarray | None = None, causal_offset: int = 0) -> np.ndarray:
     """Scaled, masked score rows S[i, :] for query rows ``rows`` (default: all).
 
-    q_bh: [Nq, d], k_bh: [Nk, d]. Causal masks keys j > i (top-left alignment).
+    q_bh: [Nq, d], k_bh: [Nk, d]. Causal masks keys j > i + causal_offset (offset 0: top-left
+    alignment; offset Nk - Nq: bottom-right alignment, used for ragged batches).
     """
     q_bh = np.asarray(q_bh, dtype=np.float64)
     k_bh = np.asarray(k_bh, dtype=np.float64)
@@ -56,7 +57,7 @@ def scores(q_bh: np.ndarray, k_bh: np.ndarray, scale: float, causal: bool,
     s = np.float64(scale) * (q_bh[rows] @ k_bh.T)
     if causal:
         j = np.arange(k_bh.shape[0])[None, :]
-        s = np.where(j > np.asarray(rows)[:, None], -np.inf, s)
+        s = np.where(j > np.asarray(rows)[:, None] + causal_offset, -np.inf, s)
     return s
 
 
@@ -72,11 +73,12 @@ def softmax_two_pass(s: np.ndarray):
 
 
 def attention_head(q_bh, k_bh, v_bh, scale: float, causal: bool,
-                   rows: np.ndarray | None = None, row_chunk: int = 1024):
+                   rows: np.ndarray | None = None, row_chunk: int = 1024, causal_offset: int = 0):
     """O and LSE for one (batch, head): q_bh [Nq, d], k_bh/v_bh [Nk, d].
 
     Rows are processed in chunks of ``row_chunk`` only to bound memory; every
-    score row is still materialised in full.
+    score row is still materialised in full. A row whose keys are all masked
+    (or with no keys at all) has O = 0 and LSE = -inf.
     """
     q_bh = np.asarray(q_bh, dtype=np.float64)
     k_bh = np.asarray(k_bh, dtype=np.float64)
@@ -88,7 +90,7 @@ def attention_head(q_bh, k_bh, v_bh, scale: float, causal: bool,
     lse = np.empty(rows.size, dtype=np.float64)
     for c0 in range(0, rows.size, row_chunk):
         r = rows[c0:c0 + row_chunk]
-        s = scores(q_bh, k_bh, scale, causal, rows=r)
+        s = scores(q_bh, k_bh, scale, causal, rows=r, causal_offset=causal_offset)
         p, m, l = softmax_two_pass(s)
         o[c0:c0 + r.size] = p @ v_bh
         with np.errstate(divide="ignore"):
