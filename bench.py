@@ -520,10 +520,204 @@ def measure_e2e(args, w, x, dev, dist, world):
             "entry_point": "attn_fwd_host"}
 
 
+# ------------------------------------------------------------------------------------ ragged batch
+def varlen_config(w):
+    return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "d": w.d, "causal": w.causal,
+            "lengths_q": list(w.lengths_q), "lengths_k": list(w.lk), "total_q": w.total_q, "qkv_dtype": w.dtype,
+            "plan": "attn_varlen_plan built once before timing and reused by every step",
+            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "parallelism": "replicas (one full workload per GPU)"}
+
+
+def varlen_cpu_sample(w, x, seconds: float, block_rows=512, max_steps=None):
+    """The oracle on row blocks of successive (sequence, head) pairs of the ragged batch."""
+    import numpy as np
+    import oracle
+    g = w.H // w.Hkv
+    pairs = [(b, h) for b in range(w.B) if w.lengths_q[b] > 0 for h in range(w.H)]
+    flops = elapsed = 0.0
+    steps = i = 0
+    cache = {}
+    while elapsed < seconds and (max_steps is None or steps < max_steps):
+        b, h = pairs[i % len(pairs)]
+        nq, nk = w.lengths_q[b], w.lk[b]
+        nblk = max(1, -(-nq // block_rows))
+        blk = (i * 7) % nblk
+        i += 1
+        if (b, h) not in cache:
+            cache.clear()
+            q0, k0 = int(w.cu_q[b]), int(w.cu_k[b])
+
+            def up(t, r0, n, hh, sc):
+                a = t[r0:r0 + n, hh, :].float().double().numpy()
+                return a * np.float64(np.float32(sc)) if t.element_size() == 1 else a
+            cache[(b, h)] = (up(x.q, q0, nq, h, x.descale_q), up(x.k, k0, nk, h // g, x.descale_k),
+                             up(x.v, k0, nk, h // g, x.descale_v))
+        q, k, v = cache[(b, h)]
+        rows = np.arange(blk * block_rows, min(nq, (blk + 1) * block_rows))
+        t0 = time.perf_counter()
+        oracle.attention_head(q, k, v, w.scale, w.causal, rows=rows, causal_offset=nk - nq)
+        elapsed += time.perf_counter() - t0
+        if w.causal:   # the metric's convention: half the rectangle for a causal sequence
+            flops += 4.0 * w.d * nk * len(rows) / 2.0
+        else:
+            flops += 4.0 * w.d * nk * len(rows)
+        steps += 1
+    desc = (f"{steps} blocks of up to {block_rows} query rows (full score rows, fp64) from (sequence, head) "
+            f"pairs of the {w.name} ragged batch; FLOPs credited by the metric's convention")
+    return (flops / elapsed / 1e12 if elapsed > 0 else 0.0), desc, elapsed, steps
+
+
+def run_varlen_reference(args, w, x):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    if args.warmup > 0:
+        varlen_cpu_sample(w, x, seconds=1e9, block_rows=256, max_steps=args.warmup)
+    tflops, desc, secs, steps = varlen_cpu_sample(w, x, seconds=1e9, block_rows=256, max_steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": varlen_config(w),
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_varlen_ours(args, w, x):
+    import torch
+    from exact_attention_72_gb300 import binding, build
+    rank, world, local = rank_info()
+    dist = init_dist(world)
+    build.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fp8 = w.dtype == "fp8_e4m3"
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    kw = {}
+    if fp8:
+        kw = {n: torch.tensor([s], dtype=torch.float32, device=dev)
+              for n, s in (("descale_q", x.descale_q), ("descale_k", x.descale_k), ("descale_v", x.descale_v))}
+    cu_q = torch.tensor(w.cu_q, dtype=torch.int32, device=dev)
+    cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device=dev)
+    o = torch.empty((w.total_q, w.H, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.H, w.total_q), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    # the plan: built once, like a serving loop reusing it across layers; its build time is reported
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    plan = binding.attn_varlen_plan(cu_q, cu_k, w.H, w.total_q, w.total_k, w.d, w.causal)
+    p1.record(stream)
+
+    def step():
+        binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, plan, w.causal, scale=w.scale, out=o, lse=lse, **kw)
+
+    for i in range(max(args.warmup, 0)):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    plan_ms = p0.elapsed_time(p1)
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+    sampler = ClockSampler(local)
+    sampler.wait_first()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_host1 = time.time()
+    time.sleep(0.12)
+    sampler.stop()
+    durs = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+    total_ms = max_over_ranks(dist, sum(durs))
+    value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    mean_ms = statistics.fmean(durs)
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    peak_bf16, peak_src = peaks()
+    peak = peak_bf16 * (2.0 if fp8 else 1.0)
+    if fp8:
+        peak_src += " x2 (e4m3/bf16 nominal dense ratio)"
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": measured_traffic(w.name), "kernel": "attn_fwd_kernel (varlen)", "peak_source": peak_src,
+                "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}, "plan_build_ms": plan_ms}
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = x.q.pin_memory(), x.k.pin_memory(), x.v.pin_memory()
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+        def e2e_step():
+            for d_, h_ in ((q, qh), (k, kh), (v, vh)):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            oh.copy_(o, non_blocking=True)
+            lh.copy_(lse, non_blocking=True)
+
+        for _ in range(max(args.warmup, 0)):
+            e2e_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        ms = max_over_ranks(dist, e0.elapsed_time(e1))
+        e2e = {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (qh, kh, vh)),
+               "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size(),
+               "ms_per_step": ms / args.steps, "entry_point": "attn_fwd_varlen on pinned host copies"}
+    clocks = sampler.summary(t_host0, t_host1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops, desc, secs, _ = varlen_cpu_sample(w, x, args.cpu_seconds)
+        cpu = {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": desc + f"; {secs:.1f} s of CPU work"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+            "config": varlen_config(w), "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
     from exact_attention_72_gb300 import inputs
     name = args.workload or inputs.HEADLINE
+    if name in inputs.VARLEN_WORKLOADS:
+        w = inputs.VARLEN_WORKLOADS[name]
+        rank, world, _ = rank_info()
+        if args.impl == "reference" and rank != 0:
+            return 0
+        x = inputs.make_varlen_inputs(w)
+        (run_varlen_reference if args.impl == "reference" else run_varlen_ours)(args, w, x)
+        return 0
     table = {**inputs.WORKLOADS, **inputs.DECODE_WORKLOADS, **inputs.FP8_BLOCK_WORKLOADS}
     w = table[name]
     if args.batch is not None:

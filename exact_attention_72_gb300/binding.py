@@ -51,6 +51,12 @@ def lib() -> ctypes.CDLL:
     L.attn_quantize_e4m3.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp]
     L.attn_quantize_e4m3_descale_count.restype = sz
     L.attn_quantize_e4m3_descale_count.argtypes = [i, i, i, i]
+    L.attn_varlen_plan_bytes.restype = sz
+    L.attn_varlen_plan_bytes.argtypes = [i, i, i, i]
+    L.attn_varlen_plan.restype = i
+    L.attn_varlen_plan.argtypes = [vp, vp, i, i, i, i, i, i, vp, sz, vp]
+    L.attn_fwd_varlen.restype = i
+    L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -165,6 +171,75 @@ def attn_fwd_fp8_scaled(q, k, v, causal: bool, descale_q, descale_k, descale_v, 
                                    dq.stride(1), dk.data_ptr(), dv.data_ptr(), dk.stride(0), dk.stride(1),
                                    _stream_handle(stream))
     _check(st, "attn_fwd_fp8_scaled")
+    return out, lse
+
+
+def attn_varlen_plan_bytes(B: int, H: int, total_q: int, d: int) -> int:
+    return int(lib().attn_varlen_plan_bytes(B, H, total_q, d))
+
+
+def _check_offsets(name, cu):
+    import torch
+    if not cu.is_cuda or cu.dtype != torch.int32 or cu.dim() != 1 or not cu.is_contiguous() or cu.numel() < 2:
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor of B + 1 offsets")
+
+
+def attn_varlen_plan(cu_seqlens_q, cu_seqlens_k, H: int, total_q: int, total_k: int, d: int, causal: bool,
+                     plan=None, stream=None):
+    """Work-tile plan of a ragged batch (uint8 CUDA tensor), reusable across forward calls."""
+    import torch
+    _check_offsets("cu_seqlens_q", cu_seqlens_q)
+    _check_offsets("cu_seqlens_k", cu_seqlens_k)
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    need = attn_varlen_plan_bytes(B, H, total_q, d)
+    if plan is None:
+        plan = torch.empty(max(need, 16), dtype=torch.uint8, device=cu_seqlens_q.device)
+    st = lib().attn_varlen_plan(cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H, total_q, total_k, d,
+                                int(bool(causal)), plan.data_ptr(), plan.numel() * plan.element_size(),
+                                _stream_handle(stream))
+    _check(st, "attn_varlen_plan")
+    return plan
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, plan, causal: bool, scale: Optional[float] = None,
+                    descale_q=None, descale_k=None, descale_v=None, out=None, lse=None, stream=None):
+    """Ragged-batch forward: q [total_q, H, d], k/v [total_k, Hkv, d] packed along rows.
+
+    Returns (out bf16 [total_q, H, d], lse float32 [H, total_q]). ``plan`` comes from
+    attn_varlen_plan with the same offsets, H, d, causal and totals.
+    """
+    import torch
+    total_q, H, d = q.shape
+    total_k, Hkv = k.shape[0], k.shape[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous 3-D CUDA tensor")
+    if k.shape != (total_k, Hkv, d) or v.shape != k.shape or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("k and v must be [total_k, Hkv, d] with q's dtype")
+    _check_offsets("cu_seqlens_q", cu_seqlens_q)
+    _check_offsets("cu_seqlens_k", cu_seqlens_k)
+    B = cu_seqlens_q.numel() - 1
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((total_q, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    ptrs = [0, 0, 0]
+    if code == ATTN_DTYPE_FP8_E4M3:
+        for idx, t in enumerate((descale_q, descale_k, descale_v)):
+            if t is None or t.dtype != torch.float32 or not t.is_cuda:
+                raise ValueError("fp8 needs descale_q/k/v as float32 CUDA tensors")
+            ptrs[idx] = t.data_ptr()
+    st = lib().attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                               cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), plan.data_ptr(),
+                               plan.numel() * plan.element_size(), B, H, Hkv,
+                               total_q, total_k, d, float(scale), int(bool(causal)), code, ptrs[0] or None,
+                               ptrs[1] or None, ptrs[2] or None, _stream_handle(stream))
+    _check(st, "attn_fwd_varlen")
     return out, lse
 
 

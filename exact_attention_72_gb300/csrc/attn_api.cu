@@ -239,6 +239,23 @@ extern "C" {
 
 namespace {
 
+template <int D>
+cudaError_t dispatch_varlen(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
+  if constexpr (D == 128) {
+    if (fp8)
+      return causal ? gb300::launch_attn_fwd<128, true, true, false, true>(a, s)
+                    : gb300::launch_attn_fwd<128, false, true, false, true>(a, s);
+  }
+  return causal ? gb300::launch_attn_fwd<D, true, false, false, true>(a, s)
+                : gb300::launch_attn_fwd<D, false, false, false, true>(a, s);
+}
+
+// Work tiles a ragged batch can have at most: sum_b ceil(Nq_b / R) <= total_q / R + B, per head.
+long long varlen_tile_bound(int B, int H, int total_q, int d) {
+  const long long R = gb300::rows_per_work_tile(d);
+  return (long long)H * ((total_q + R - 1) / R + B);
+}
+
 // The prefill forward behind attn_fwd and the fp8 entries with finer descales. ds: descale
 // element strides (q by batch, q by head, q by 128-row block, k by batch, k by kv head, k by
 // 64-key block, v by batch, v by kv head); all 0 = one descale per tensor.
@@ -516,6 +533,101 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+size_t attn_varlen_plan_bytes(int B, int H, int total_q, int d) {
+  if (B < 1 || H < 1 || total_q < 0 || (d != 64 && d != 128 && d != 256)) return 0;
+  const long long tiles = varlen_tile_bound(B, H, total_q, d);
+  if (tiles >= INT_MAX || B >= INT_MAX / 2) return 0;
+  return (size_t)gb300::plan_tiles_offset(B) * 4 + (size_t)tiles * 8;
+}
+
+attn_status_t attn_varlen_plan(const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H, int total_q,
+                               int total_k, int d, int causal, void* plan, size_t plan_bytes, cudaStream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k || !plan) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || total_q < 0 || total_k < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(plan, 16) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_varlen_plan_bytes(B, H, total_q, d);
+  if (need == 0) return ATTN_ERR_UNSUPPORTED;
+  if (plan_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const size_t head = (size_t)gb300::plan_tiles_offset(B) * 4;
+  const size_t cap = (plan_bytes - head) / 8;
+  const int capacity = cap > (size_t)INT_MAX ? INT_MAX : (int)cap;
+  const cudaError_t e = gb300::launch_varlen_plan(cu_seqlens_q, cu_seqlens_k, B, H, gb300::rows_per_work_tile(d),
+                                                  causal != 0, total_q, total_k, capacity, static_cast<int*>(plan),
+                                                  stream);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, const void* plan, size_t plan_bytes,
+                              int B, int H, int Hkv, int total_q, int total_k, int d, float scale, int causal,
+                              attn_dtype_t dtype, const float* descale_q, const float* descale_k,
+                              const float* descale_v, cudaStream_t stream) {
+  if (total_q < 0 || total_k < 0 || B < 1) return ATTN_ERR_INVALID_ARG;
+  attn_status_t st = check_shape(1, H, Hkv, total_q > 0 ? total_q : 1, d, scale, dtype);
+  if (st != ATTN_OK) return st;
+  if (varlen_tile_bound(B, H, total_q, d) >= INT_MAX) return ATTN_ERR_UNSUPPORTED;
+  const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
+  if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || !plan) return ATTN_ERR_INVALID_ARG;
+  if (fp8 && (!descale_q || !descale_k || !descale_v)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(plan, 16) || !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return ATTN_ERR_INVALID_ARG;
+  if (plan_bytes < (size_t)gb300::plan_tiles_offset(B) * 4) return ATTN_ERR_INVALID_ARG;
+  if (total_q == 0) return ATTN_OK;   // no query rows: nothing to write
+  const size_t elt = fp8 ? 1 : 2;
+  const size_t nq = (size_t)total_q * H * d, nkv = (size_t)total_k * Hkv * d;
+  const size_t o_bytes = nq * 2, lse_bytes = (size_t)H * total_q * 4;
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {nq * elt, nkv * elt, nkv * elt};
+  for (int i = 0; i < 3; ++i)
+    if (ranges_overlap(o, o_bytes, ins[i], in_bytes[i]) || ranges_overlap(lse, lse_bytes, ins[i], in_bytes[i]))
+      return ATTN_ERR_INVALID_ARG;
+  if (ranges_overlap(o, o_bytes, lse, lse_bytes)) return ATTN_ERR_INVALID_ARG;
+  DeviceInfo* di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  gb300::LaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  // Packed tensors as one batch of total rows. With no keys at all the k/v maps are never read.
+  const int kv_rows = total_k > 0 ? total_k : 1;
+  if (!make_map(&a.tm_q, q, fp8, d, total_q, H, 1) || !make_map(&a.tm_k, k, fp8, d, kv_rows, Hkv, 1) ||
+      !make_map(&a.tm_v, v, fp8, d, kv_rows, Hkv, 1))
+    return ATTN_ERR_CUDA;
+  gb300::AttnParams& p = a.params;
+  p.o = o;
+  p.lse = lse;
+  p.descale_q = descale_q;
+  p.descale_k = descale_k;
+  p.descale_v = descale_v;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.N = total_q;
+  p.Nk = total_k;
+  p.G = H / Hkv;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  // Launch bound and read limit: the tiles a valid plan can hold, and no more than the buffer has.
+  const size_t held = (plan_bytes - (size_t)gb300::plan_tiles_offset(B) * 4) / 8;
+  const long long bound = varlen_tile_bound(B, H, total_q, d);
+  p.n_tiles = (int)std::min<long long>(bound, (long long)std::min<size_t>(held, (size_t)INT_MAX));
+  if (p.n_tiles < 1) p.n_tiles = 1;
+  p.n_splits = 1;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.plan = static_cast<const int*>(plan);
+  p.status = di->status;
+  p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
+  p.debug_skip_load = 0;
+  a.num_sms = di->num_sms;
+  cudaError_t e;
+  switch (d) {
+    case 64: e = dispatch_varlen<64>(a, causal != 0, fp8, stream); break;
+    case 128: e = dispatch_varlen<128>(a, causal != 0, fp8, stream); break;
+    default: e = dispatch_varlen<256>(a, causal != 0, fp8, stream); break;
+  }
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_quantize_e4m3_descale_count(int B, int N, int Hx, int block_rows) {
   if (B < 1 || N < 1 || Hx < 1 || block_rows < 1) return 0;
   return (size_t)B * Hx * (size_t)((N + (long long)block_rows - 1) / block_rows);
@@ -583,7 +695,8 @@ attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {
   uint32_t v = 0;
   if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v)) != cudaSuccess) return ATTN_ERR_CUDA;
   if (detail) *detail = v;
-  return v ? ATTN_ERR_TIMEOUT : ATTN_OK;
+  if (!v) return ATTN_OK;
+  return (v & 0x40000000u) ? ATTN_ERR_TIMEOUT : ATTN_ERR_INVALID_ARG;   // 0x20000000: bad varlen plan
 }
 
 attn_status_t attn_clear_status(void) {

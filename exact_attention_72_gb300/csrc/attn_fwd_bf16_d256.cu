@@ -2,6 +2,6 @@
 #include "launch_impl.cuh"
 
 namespace gb300 {
-template cudaError_t launch_attn_fwd<256, false, false, false>(LaunchArgs&, cudaStream_t);
-template cudaError_t launch_attn_fwd<256, true, false, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<256, false, false, false, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<256, true, false, false, false>(LaunchArgs&, cudaStream_t);
 }  // namespace gb300

@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include "ptx.cuh"
+#include "varlen.cuh"
 
 namespace gb300 {
 
@@ -60,18 +61,25 @@ struct AttnParams {
   int Nk, G, n_splits, n_kvt;
   float* part_o;
   float* part_lse;
+  // Varlen mode (ragged batch): sequence b owns rows cu_q[b] .. cu_q[b+1]-1 of the packed q (the
+  // maps and B = 1, N = total rows) and rows cu_k[b] .. of k and v; work tiles come from the plan.
+  const int* cu_q;
+  const int* cu_k;
+  const int* plan;
   uint32_t* status;         // device status word (first failure)
   unsigned long long timeout_ns;
   int debug_skip_load;      // fault injection: CTA 0 never loads V_0 of its first tile
 };
 
-template <int D_, bool CAUSAL_, bool FP8_, bool SPLIT_ = false>
+template <int D_, bool CAUSAL_, bool FP8_, bool SPLIT_ = false, bool VARLEN_ = false>
 struct AttnCfg {
   static constexpr int D = D_;
   static constexpr bool CAUSAL = CAUSAL_;
   static constexpr bool FP8 = FP8_;
   static constexpr bool SPLIT = SPLIT_;                   // split-KV decode mode (no mask)
+  static constexpr bool VARLEN = VARLEN_;                 // ragged batch from a tile plan
   static_assert(!(SPLIT && CAUSAL), "split-KV mode has no causal mask");
+  static_assert(!(SPLIT && VARLEN), "split-KV and varlen modes are separate");
   static constexpr int ELT = FP8 ? 1 : 2;                 // bytes per q/k/v element
   static constexpr int NQ = (D <= 128) ? 2 : 1;           // 128-row Q tiles per CTA
   static constexpr int BM = 128, BN = 128;                // query rows per Q tile, keys per KV tile
@@ -121,6 +129,9 @@ enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_
 struct TileCoord {
   int b, h, mb;     // h: query head (prefill) or kv head (split-KV)
   int s, j0, j1;    // split index and its KV tile range [j0, j1)
+  int bo;           // batch coordinate of the maps and outputs (0 in varlen mode)
+  int q_base, k_base;   // first q / k row of the sequence in the packed tensors (varlen)
+  int nq, nk, n_kvt;    // query rows, keys and 128-key tiles of this sequence
 };
 
 // Work tile t -> (batch, head, query block). Causal tiles go longest first: every head's last
@@ -129,6 +140,37 @@ struct TileCoord {
 template <class C>
 __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
   TileCoord c;
+  if constexpr (C::VARLEN) {
+    // Plan entry: (sequence, head << 16 | query block), longest first.
+    const int2 e = reinterpret_cast<const int2*>(p.plan + p.plan[5])[t];
+    c.b = e.x;
+    c.h = e.y >> 16;
+    c.mb = e.y & 0xFFFF;
+    c.bo = 0;
+    const bool b_ok = c.b >= 0 && c.b < p.B;
+    c.q_base = b_ok ? __ldg(p.cu_q + c.b) : 0;
+    c.nq = b_ok ? __ldg(p.cu_q + c.b + 1) - c.q_base : 0;
+    c.k_base = b_ok ? __ldg(p.cu_k + c.b) : 0;
+    c.nk = b_ok ? __ldg(p.cu_k + c.b + 1) - c.k_base : 0;
+    // Rows outside the packed tensors (offsets that changed since the plan was built) make the
+    // tile empty for every role, so nothing is read or written out of bounds.
+    if (!(b_ok && c.h < p.H && c.q_base >= 0 && c.nq >= 0 && c.q_base + c.nq <= p.N && c.k_base >= 0 && c.nk >= 0 &&
+          c.k_base + c.nk <= p.Nk)) {
+      atomicCAS(p.status, 0u, kStatusBadPlan);
+      c.b = c.h = 0;
+      c.q_base = c.k_base = c.nq = c.nk = 0;
+    }
+    c.n_kvt = (c.nk + C::BN - 1) / C::BN;
+    c.s = 0;
+    c.j0 = 0;
+    c.j1 = c.n_kvt;
+    return c;
+  }
+  c.q_base = 0;
+  c.k_base = 0;
+  c.nq = p.N;
+  c.nk = C::SPLIT ? p.Nk : p.N;
+  c.n_kvt = p.n_kvt;
   if (C::SPLIT) {
     // Split-KV: the query blocks of one (batch, kv head, split) are consecutive.
     c.mb = t % p.n_mb;
@@ -137,6 +179,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
     const int bk = rest / p.n_splits;
     c.b = bk / p.Hkv;
     c.h = bk % p.Hkv;
+    c.bo = c.b;
     c.j0 = (int)((long long)c.s * p.n_kvt / p.n_splits);
     c.j1 = (int)((long long)(c.s + 1) * p.n_kvt / p.n_splits);
     return c;
@@ -155,6 +198,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
   }
   c.b = bh / p.H;
   c.h = bh % p.H;
+  c.bo = c.b;
   return c;
 }
 
@@ -169,6 +213,7 @@ __device__ __forceinline__ int q_tile_pos0(const TileCoord& tc, int qt, const At
 template <class C>
 __device__ __forceinline__ int kv_tiles_for(const TileCoord& tc, int qt, const AttnParams& p) {
   const int pos0 = q_tile_pos0<C>(tc, qt, p);
+  if constexpr (C::VARLEN) return varlen_kv_tiles(pos0, tc.nq, tc.nk, C::CAUSAL);
   if (pos0 >= p.N) return 0;
   if (C::SPLIT) return tc.j1 - tc.j0;
   return C::CAUSAL ? (pos0 / C::BN + 1) : p.n_kvt;
@@ -319,6 +364,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   ATTN_TRACE_DECL;
+  // Work tiles: a count fixed at launch, or (varlen) the plan's, once the plan is seen to have been
+  // built for this launch's sequences, heads, tile height and mask.
+  int n_tiles = p.n_tiles;
+  if constexpr (C::VARLEN) {
+    const bool good = __ldg(p.plan + 1) == p.B && __ldg(p.plan + 2) == p.H && __ldg(p.plan + 3) == C::NQ * C::BM &&
+                      __ldg(p.plan + 4) == (C::CAUSAL ? 1 : 0) && __ldg(p.plan + 6) == p.N && __ldg(p.plan + 7) == p.Nk;
+    n_tiles = good ? min(__ldg(p.plan), p.n_tiles) : 0;   // p.n_tiles: entries the plan buffer holds
+    if (!good && tid == 0 && blockIdx.x == 0) atomicCAS(p.status, 0u, kStatusBadPlan);
+  }
 
   if (warp == C::WARP_LOAD) {
     // ------------------------------------------------------------------ TMA producer
@@ -331,7 +385,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t nq_loads = 0;  // Q loads issued so far
       bool ok = true;
       int iter = 0;
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x, ++iter) {
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++iter) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
@@ -340,6 +394,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           nmax = n > nmax ? n : nmax;
           nq_valid += (n > 0);
         }
+        if (C::VARLEN && nmax == 0) continue;   // every row sees no key: the softmax warps write it
         // Q: wait until the previous work tile's last S = Q K^T has completed.
         if (nq_loads > 0 && !mbar_wait(smem_addr(&bar_q_empty), (nq_loads - 1) & 1, ctl, SITE_Q_EMPTY)) {
           ok = false;
@@ -348,13 +403,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive_expect_tx(smem_addr(&bar_q_full), nq_valid * C::TILE_BYTES);
         for (int qt = 0; qt < C::NQ; ++qt) {
           const int pos0 = q_tile_pos0<C>(tc, qt, p);
-          if (pos0 >= p.N) continue;
+          if (kv_tiles_for<C>(tc, qt, p) == 0) continue;
           for (int ch = 0; ch < C::NCH; ++ch) {
             const uint32_t dst = sQ + (qt * C::NCH + ch) * C::CHUNK_BYTES;
             if (C::SPLIT)   // (d, head in group, position, kv head, batch): G x 128/G packed rows
               tma_load_5d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, 0, pos0, tc.h, tc.b);
             else
-              tma_load_4d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, pos0, tc.h, tc.b);
+              tma_load_4d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, tc.q_base + pos0, tc.h, tc.bo);
           }
         }
         ++nq_loads;
@@ -372,7 +427,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               mbar_arrive_expect_tx(smem_addr(&bar_kv_full[slot]), C::TILE_BYTES);
               for (int ch = 0; ch < C::NCH; ++ch)
                 tma_load_4d(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES, tm, smem_addr(&bar_kv_full[slot]),
-                            ch * C::CE, (tc.j0 + j) * C::BN, kvh, tc.b);
+                            ch * C::CE, tc.k_base + (tc.j0 + j) * C::BN, kvh, tc.bo);
             }
             ++ring;
           }
@@ -423,7 +478,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
         return true;
       };
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int n = kv_tiles_for<C>(tc, myq, p);
         int nmax = 0;
@@ -431,6 +486,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const int nq = kv_tiles_for<C>(tc, qt, p);
           nmax = nq > nmax ? nq : nmax;
         }
+        if (C::VARLEN && nmax == 0) continue;
         if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
         ++nq_loads;
         const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
@@ -508,7 +564,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++p_cnt[buf];
         return true;
       };
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int nmax = kv_tiles_for<C>(tc, 0, p);
         if (nmax == 0) continue;
@@ -562,13 +618,26 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
-    const int Nk = C::SPLIT ? p.Nk : p.N;   // keys per (batch, head)
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile<C>(t, p);
       const int n = kv_tiles_for<C>(tc, qt, p);
-      if (n == 0) continue;
       const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
+      const int Nk = tc.nk;                         // keys of this sequence
+      if (n == 0) {
+        // Varlen: rows that see no key at all get O = 0 and LSE = -inf.
+        if constexpr (C::VARLEN) {
+          const int row = row0 + r;
+          if (row < tc.nq) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                                  ((size_t)(tc.q_base + row) * p.H + tc.h) * C::D);
+#pragma unroll 1
+            for (int v4 = 0; v4 < C::D / 8; ++v4) dst[v4] = make_uint4(0u, 0u, 0u, 0u);
+            p.lse[(size_t)tc.h * p.N + tc.q_base + row] = -INFINITY;
+          }
+        }
+        continue;
+      }
       // Score scale (log2 units) and output scale of this row (FP8: descales per tensor, per head
       // or per block; split-KV rows of one tile belong to different query heads of the group).
       const int h_row = C::SPLIT ? tc.h * p.G + r % p.G : tc.h;
@@ -619,12 +688,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
         // Masking: keys past N (ragged tail) and, on the diagonal tile, keys after the query row.
-        const bool diag = C::CAUSAL && (j == n - 1);
         const int jk = tc.j0 + j;   // KV tile index within the sequence
-        const bool tail = (jk == p.n_kvt - 1) && (Nk % C::BN != 0);
+        // Varlen causal masking is bottom-right aligned (query i sees keys <= i + Nk - Nq), so up
+        // to two tiles can cross the diagonal; with equal lengths only the last one does.
+        const int diag_off = C::VARLEN ? Nk - tc.nq : 0;
+        const bool diag = C::CAUSAL && (C::VARLEN ? (jk * C::BN + C::BN - 1 > row0 + diag_off) : (j == n - 1));
+        const bool tail = (jk == tc.n_kvt - 1) && (Nk % C::BN != 0);
         if (diag || tail) {
           int lim = Nk - jk * C::BN;
-          if (diag) lim = min(lim, (row0 + r) - j * C::BN + 1);
+          if (diag) lim = min(lim, (row0 + r + diag_off) - jk * C::BN + 1);
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c >= lim) x[c] = -INFINITY;
@@ -775,10 +847,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (valid) p.part_lse[prow] = lse_row;
       } else {
         const int row = row0 + r;
-        const bool valid = row < p.N;
+        const bool valid = row < tc.nq;
+        // Varlen: a row whose keys were all masked (its max never left -inf) gets O = 0 and
+        // LSE = -inf; its accumulator holds no meaningful value.
+        const bool empty_row = C::VARLEN && m == -INFINITY;
         const float inv_l = out_scale / l;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                              ((size_t)(tc.b * p.N + (valid ? row : 0)) * p.H + tc.h) * C::D;
+                              ((size_t)(tc.bo * p.N + tc.q_base + (valid ? row : 0)) * p.H + tc.h) * C::D;
 #pragma unroll 1
         for (int c0 = 0; c0 < C::D; c0 += 32) {
           uint32_t ov[32];
@@ -788,7 +863,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2)
-            pk[c >> 1] = pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
+            pk[c >> 1] = empty_row ? 0u
+                                   : pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
@@ -796,7 +872,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           }
         }
-        if (valid) p.lse[((size_t)tc.b * p.H + tc.h) * p.N + row] = lse_row;
+        if (valid) p.lse[((size_t)tc.bo * p.H + tc.h) * p.N + tc.q_base + row] = empty_row ? -INFINITY : lse_row;
       }
     }
   }

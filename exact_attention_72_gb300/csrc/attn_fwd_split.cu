@@ -2,8 +2,8 @@
 #include "launch_impl.cuh"
 
 namespace gb300 {
-template cudaError_t launch_attn_fwd<64, false, false, true>(LaunchArgs&, cudaStream_t);
-template cudaError_t launch_attn_fwd<128, false, false, true>(LaunchArgs&, cudaStream_t);
-template cudaError_t launch_attn_fwd<256, false, false, true>(LaunchArgs&, cudaStream_t);
-template cudaError_t launch_attn_fwd<128, false, true, true>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<64, false, false, true, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<128, false, false, true, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<256, false, false, true, false>(LaunchArgs&, cudaStream_t);
+template cudaError_t launch_attn_fwd<128, false, true, true, false>(LaunchArgs&, cudaStream_t);
 }  // namespace gb300

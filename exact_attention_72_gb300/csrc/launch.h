@@ -13,9 +13,13 @@ struct LaunchArgs {
 };
 
 // Per-instance launcher: grid = min(work tiles, SMs), one persistent CTA per SM. SPLIT selects
-// the split-KV (decode) mode of the kernel.
-template <int D, bool CAUSAL, bool FP8, bool SPLIT = false>
+// the split-KV (decode) mode of the kernel, VARLEN the ragged-batch mode driven by a tile plan.
+template <int D, bool CAUSAL, bool FP8, bool SPLIT = false, bool VARLEN = false>
 cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream);
+
+// Builds the ragged-batch tile plan (varlen_plan.cu): one CTA on the stream.
+cudaError_t launch_varlen_plan(const int* cu_q, const int* cu_k, int B, int H, int rows_per_tile, bool causal,
+                               int total_q, int total_k, int capacity, int* plan, cudaStream_t stream);
 
 // Split-KV combine: merges the n_splits normalized partial results (part_o fp32
 // [S, B, H, Nq, D], part_lse [S, B, H, Nq]) into o (bf16 [B, Nq, H, D]) and lse ([B, H, Nq]).
@@ -44,9 +48,11 @@ cudaError_t launch_quantize_e4m3(const QuantLaunch& q, cudaStream_t stream);
 inline int rows_per_work_tile(int d) { return d <= 128 ? 256 : 128; }
 
 #define GB300_DECLARE_LAUNCH(D, CAUSAL, FP8) \
-  extern template cudaError_t launch_attn_fwd<D, CAUSAL, FP8, false>(LaunchArgs&, cudaStream_t);
+  extern template cudaError_t launch_attn_fwd<D, CAUSAL, FP8, false, false>(LaunchArgs&, cudaStream_t);
 #define GB300_DECLARE_SPLIT(D, FP8) \
-  extern template cudaError_t launch_attn_fwd<D, false, FP8, true>(LaunchArgs&, cudaStream_t);
+  extern template cudaError_t launch_attn_fwd<D, false, FP8, true, false>(LaunchArgs&, cudaStream_t);
+#define GB300_DECLARE_VARLEN(D, CAUSAL, FP8) \
+  extern template cudaError_t launch_attn_fwd<D, CAUSAL, FP8, false, true>(LaunchArgs&, cudaStream_t);
 
 GB300_DECLARE_LAUNCH(64, false, false)
 GB300_DECLARE_LAUNCH(64, true, false)
@@ -60,5 +66,13 @@ GB300_DECLARE_SPLIT(64, false)
 GB300_DECLARE_SPLIT(128, false)
 GB300_DECLARE_SPLIT(256, false)
 GB300_DECLARE_SPLIT(128, true)
+GB300_DECLARE_VARLEN(64, false, false)
+GB300_DECLARE_VARLEN(64, true, false)
+GB300_DECLARE_VARLEN(128, false, false)
+GB300_DECLARE_VARLEN(128, true, false)
+GB300_DECLARE_VARLEN(256, false, false)
+GB300_DECLARE_VARLEN(256, true, false)
+GB300_DECLARE_VARLEN(128, false, true)
+GB300_DECLARE_VARLEN(128, true, true)
 
 }  // namespace gb300

@@ -4,9 +4,9 @@
 
 namespace gb300 {
 
-template <int D, bool CAUSAL, bool FP8, bool SPLIT>
+template <int D, bool CAUSAL, bool FP8, bool SPLIT, bool VARLEN>
 cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
-  using C = AttnCfg<D, CAUSAL, FP8, SPLIT>;
+  using C = AttnCfg<D, CAUSAL, FP8, SPLIT, VARLEN>;
   auto kernel = attn_fwd_kernel<C>;
   // The attribute is per device; setting it on every call is cheap and keeps this stateless.
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -19,6 +19,7 @@ cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (fa.numRegs * C::THREADS < C::REGS_NEEDED) return cudaErrorInvalidConfiguration;
   }
+  // Varlen: n_tiles is the host's upper bound; the kernel reads the plan's own count.
   const int grid = a.params.n_tiles < a.num_sms ? a.params.n_tiles : a.num_sms;
   kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.params);
   return cudaGetLastError();

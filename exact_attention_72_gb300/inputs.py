@@ -121,6 +121,84 @@ FP8_BLOCK_WORKLOADS = {
 }
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """A ragged batch: sequence b has lengths_q[b] queries and lengths_k[b] keys, packed by rows."""
+
+    name: str
+    H: int
+    Hkv: int
+    d: int
+    causal: bool
+    lengths_q: tuple
+    lengths_k: Optional[tuple] = None   # None: same as lengths_q
+    dtype: str = "bf16"
+    seed: int = 1300
+
+    @property
+    def lk(self) -> tuple:
+        return self.lengths_q if self.lengths_k is None else self.lengths_k
+
+    @property
+    def B(self) -> int:
+        return len(self.lengths_q)
+
+    @property
+    def total_q(self) -> int:
+        return int(sum(self.lengths_q))
+
+    @property
+    def total_k(self) -> int:
+        return int(sum(self.lk))
+
+    @property
+    def cu_q(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lengths_q)]).astype(np.int32)
+
+    @property
+    def cu_k(self) -> np.ndarray:
+        return np.concatenate([[0], np.cumsum(self.lk)]).astype(np.int32)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    @property
+    def flops(self) -> float:
+        """Sum over sequences of 4*H*Nq*Nk*d, halved for causal (the benchmark's convention)."""
+        f = sum(4.0 * self.H * nq * nk * self.d for nq, nk in zip(self.lengths_q, self.lk))
+        return f / 2.0 if self.causal else f
+
+
+def varlen_lengths(n: int, lo: int, hi: int, seed: int) -> tuple:
+    """n sequence lengths drawn uniformly from [lo, hi] (numpy PCG64 seeded with ``seed``)."""
+    rng = np.random.default_rng(seed)
+    return tuple(int(x) for x in rng.integers(lo, hi + 1, size=n))
+
+
+# Ragged batch of the GQA configuration's heads: 16 sequences of 256 .. 8192 tokens, causal.
+VARLEN_WORKLOADS = {
+    "varlen_causal_gqa_bf16_16seq_d128": VarlenWorkload("varlen_causal_gqa_bf16_16seq_d128", H=32, Hkv=8, d=128,
+                                                        causal=True, lengths_q=varlen_lengths(16, 256, 8192, 1301),
+                                                        seed=1301),
+}
+
+
+def make_varlen_inputs(w: VarlenWorkload):
+    """Seeded packed q [total_q, H, d], k, v [total_k, Hkv, d] as AttnInputs (bf16 or e4m3)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    q = torch.randn((w.total_q, w.H, w.d), generator=g, dtype=torch.float32)
+    k = torch.randn((w.total_k, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    v = torch.randn((w.total_k, w.Hkv, w.d), generator=g, dtype=torch.float32)
+    if w.dtype == "bf16":
+        return AttnInputs(q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16))
+    q8, sq = quantize_e4m3(q)
+    k8, sk = quantize_e4m3(k)
+    v8, sv = quantize_e4m3(v)
+    return AttnInputs(q8, k8, v8, sq, sk, sv)
+
+
 @dataclasses.dataclass
 class AttnInputs:
     """Stored inputs (what the kernel reads) plus their exact fp64 values."""

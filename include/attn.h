@@ -91,6 +91,53 @@ attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, v
                                   int q_stride_h, const float* descale_k, const float* descale_v,
                                   int kv_stride_b, int kv_stride_h, cudaStream_t stream);
 
+/*
+ * Ragged batches ("varlen"): B sequences packed along the row dimension, described by
+ * cumulative offsets. Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 of
+ * q [total_q, H, d] and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1 of k, v [total_k, Hkv, d];
+ * query and key lengths may differ and may be 0. "flash-attention-3" (ai.thesatyajit.com),
+ * "What is actually in the box" and "Five schedulers"; "FlashAttention-3 Deep Dive"
+ * (mojostudio.in), FAQ on variable-length sequences (cu_seqlens, no padding).
+ *
+ * Causal masking is bottom-right aligned: query i of a sequence with Nq queries and Nk keys sees
+ * keys j <= i + (Nk - Nq), so the last query sees every key; with Nq == Nk this is the usual mask.
+ * A query row that sees no key (Nk == 0, or i + Nk - Nq < 0) gets O = 0 and LSE = -inf.
+ *
+ * attn_varlen_plan — builds the work-tile plan of a ragged batch on the GPU (one small kernel on
+ * `stream`): every (sequence, query head, block of query rows) tile, longest first. A plan
+ * depends on the offsets, B, H, d (through the tile height), causal and the totals, and can be
+ * reused by every forward call with the same batch (e.g. all layers of one step).
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1], starting at 0, non-decreasing, last entry
+ *       <= total_q / total_k. Offsets that break this give a plan marked invalid (a forward
+ *       handed it writes nothing and attn_get_status reports ATTN_ERR_INVALID_ARG).
+ *   plan: DEVICE, 16-byte aligned, plan_bytes >= attn_varlen_plan_bytes(B, H, total_q, d).
+ * INVALID_ARG for null or misaligned pointers, negative sizes or a short buffer; UNSUPPORTED for
+ * d not in {64, 128, 256}.
+ */
+size_t attn_varlen_plan_bytes(int B, int H, int total_q, int d);
+attn_status_t attn_varlen_plan(const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                               int total_q, int total_k, int d, int causal, void* plan,
+                               size_t plan_bytes, cudaStream_t stream);
+
+/*
+ * attn_fwd_varlen — attn_fwd over a ragged batch, asynchronous on `stream`, allocates nothing.
+ *   q [total_q, H, d], k, v [total_k, Hkv, d]: DEVICE, element type `dtype`, 16-byte aligned.
+ *   o [total_q, H, d] bf16 (DEVICE, 16-byte aligned), lse [H, total_q] fp32 (natural log).
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1] as for attn_varlen_plan.
+ *   plan, plan_bytes: built by attn_varlen_plan from the same offsets, B, H, d, causal, total_q
+ *         and total_k, and the size of its buffer. A plan built for other arguments is detected
+ *         on the GPU (nothing is written, and attn_get_status reports ATTN_ERR_INVALID_ARG); so
+ *         is a tile whose sequence's rows fall outside the packed tensors (that tile is skipped).
+ *   descale_q/k/v: e4m3 only, one fp32 each (per tensor), as in attn_fwd.
+ * Same argument checks as attn_fwd; total_q == 0 returns ATTN_OK at once.
+ */
+attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                              const int* cu_seqlens_q, const int* cu_seqlens_k, const void* plan,
+                              size_t plan_bytes, int B, int H, int Hkv, int total_q, int total_k,
+                              int d, float scale, int causal, attn_dtype_t dtype,
+                              const float* descale_q, const float* descale_k,
+                              const float* descale_v, cudaStream_t stream);
+
 /* Rows per descale block of the block-scaled e4m3 forward: q in blocks of 128 query positions,
  * k in blocks of 64 key positions, both within one (batch, head). */
 #define ATTN_FP8_Q_BLOCK 128
@@ -227,8 +274,10 @@ attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* 
 /*
  * attn_get_status — synchronizes `stream`, then returns ATTN_ERR_TIMEOUT if any kernel of this
  * library on the current device gave up a bounded wait since the last attn_clear_status,
- * ATTN_ERR_CUDA if the synchronization failed, else ATTN_OK. `detail` (may be NULL) receives
- * the raw status word (0, or 0x40000000 | wait-site code).
+ * ATTN_ERR_INVALID_ARG if a varlen forward was handed a plan that does not match it (or that the
+ * plan builder marked invalid), ATTN_ERR_CUDA if the synchronization failed, else ATTN_OK.
+ * `detail` (may be NULL) receives the raw status word (0, 0x40000000 | wait-site code, or
+ * 0x2000000C for a rejected plan).
  */
 attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail);
 

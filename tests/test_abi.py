@@ -141,3 +141,31 @@ def test_quantize_and_blockscaled_validation(lib):
 
     assert f(N=0) == INV and f(H=0) == INV
     assert f(d=64) == UNS
+
+
+def test_varlen_validation(lib):
+    INV, UNS = binding.ATTN_ERR_INVALID_ARG, binding.ATTN_ERR_UNSUPPORTED
+    need = binding.attn_varlen_plan_bytes(3, 4, 1000, 128)
+    # header (8 words), 4 prefix words, padding to 8 bytes, then 4 heads x (ceil(1000/256) + 3) tiles
+    assert need == ((8 + 3 + 2) & ~1) * 4 + 4 * (4 + 3) * 8
+    assert binding.attn_varlen_plan_bytes(0, 4, 1000, 128) == 0
+    assert binding.attn_varlen_plan_bytes(3, 4, 1000, 96) == 0
+
+    def plan(cu_q=1 << 12, cu_k=1 << 13, B=3, H=4, tq=1000, tk=1000, d=128, p=1 << 20, nbytes=1 << 16):
+        return lib.attn_varlen_plan(cu_q, cu_k, B, H, tq, tk, d, 1, p, nbytes, None)
+
+    assert plan(cu_q=0) == INV and plan(p=0) == INV
+    assert plan(B=0) == INV and plan(tq=-1) == INV
+    assert plan(d=96) == UNS
+    assert plan(p=(1 << 20) + 8) == INV          # plan not 16-byte aligned
+    assert plan(nbytes=need - 1) == INV           # plan buffer too small
+
+    def fwd(q=1 << 16, plan=1 << 28, plan_bytes=1 << 16, B=3, H=4, Hkv=2, tq=1000, tk=900, d=128, scale=0.1):
+        return lib.attn_fwd_varlen(q, 1 << 20, 1 << 24, 1 << 26, 1 << 27, 1 << 12, 1 << 13, plan, plan_bytes, B, H,
+                                   Hkv, tq, tk, d, scale, 1, 0, None, None, None, None)
+
+    assert fwd(q=0) == INV and fwd(plan=0) == INV
+    assert fwd(plan_bytes=16) == INV              # shorter than the plan header
+    assert fwd(B=0) == INV and fwd(tq=-1) == INV and fwd(H=3, Hkv=2) == INV
+    assert fwd(d=96) == UNS and fwd(scale=0.0) == UNS
+    assert fwd(tq=0) == binding.ATTN_OK           # no query rows: nothing to do
