@@ -520,6 +520,170 @@ def measure_e2e(args, w, x, dev, dist, world):
             "entry_point": "attn_fwd_host"}
 
 
+# ------------------------------------------------------------------------------------ backward
+BWD_FLOP_FACTOR = 2.5   # five tile GEMMs against the forward's two (the usual backward convention)
+
+
+def bwd_config(w):
+    c = config_of(w)
+    c["pass"] = "backward (dQ, dK, dV; O and LSE from one untimed forward)"
+    return c
+
+
+def bwd_cpu_sample(w, x, do, seconds: float, rows=1024, max_steps=None):
+    """The backward oracle on causal prefixes of `rows` rows of successive heads (a valid
+    sub-problem: a prefix of a causal sequence does not see later keys)."""
+    import numpy as np
+    import oracle
+    g = w.H // w.Hkv
+    heads = [(b, h) for b in range(w.B) for h in range(w.H)]
+    n = min(rows, w.N)
+    flops = elapsed = 0.0
+    steps = 0
+    while elapsed < seconds and (max_steps is None or steps < max_steps):
+        b, h = heads[steps % len(heads)]
+        f = lambda t, hh: t[b, :n, hh, :].float().double().numpy()
+        q, k, v, dd = f(x.q, h), f(x.k, h // g), f(x.v, h // g), f(do, h)
+        t0 = time.perf_counter()
+        oracle.attention_backward_head(q, k, v, dd, w.scale, w.causal)
+        elapsed += time.perf_counter() - t0
+        flops += BWD_FLOP_FACTOR * 4.0 * w.d * n * n / (2.0 if w.causal else 1.0)
+        steps += 1
+    desc = (f"{steps} backward sub-problems of the first {n} rows and keys of a head (fp64, P materialised) "
+            f"of the {w.name} workload; FLOPs credited by the metric's convention")
+    return (flops / elapsed / 1e12 if elapsed > 0 else 0.0), desc, elapsed, steps
+
+
+def run_bwd_reference(args, w, x):
+    from exact_attention_72_gb300 import inputs
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    do = inputs.make_grad_output(w)
+    if args.warmup > 0:
+        bwd_cpu_sample(w, x, do, seconds=1e9, rows=512, max_steps=args.warmup)
+    tflops, desc, secs, steps = bwd_cpu_sample(w, x, do, seconds=1e9, rows=512, max_steps=args.steps)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(1, steps) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": bwd_config(w),
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_bwd_ours(args, w, x):
+    import torch
+    from exact_attention_72_gb300 import binding, build, inputs
+    rank, world, local = rank_info()
+    dist = init_dist(world)
+    build.build()
+    binding.lib()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    do_h = inputs.make_grad_output(w)
+    q, k, v, do = x.q.to(dev), x.k.to(dev), x.v.to(dev), do_h.to(dev)
+    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(binding.attn_bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flops = BWD_FLOP_FACTOR * w.flops
+
+    def step():
+        binding.attn_bwd(q, k, v, o, lse, do, w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    for i in range(max(args.warmup, 0)):
+        flush.fill_(i & 0xFF)
+        step()
+    torch.cuda.synchronize()
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
+    sampler = ClockSampler(local)
+    sampler.wait_first()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    t_host1 = time.time()
+    time.sleep(0.12)
+    sampler.stop()
+    durs = [a_.elapsed_time(b_) for a_, b_ in zip(starts, ends)]
+    st, detail = binding.attn_get_status()
+    if st != binding.ATTN_OK:
+        raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
+    total_ms = max_over_ranks(dist, sum(durs))
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    mean_ms = statistics.fmean(durs)
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    peak, peak_src = peaks()
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "peak_source": peak_src,
+                "kernel": "the backward pass as one unit: preprocess + attn_bwd_dkdv_kernel + attn_bwd_dq_kernel "
+                          "(algorithmic FLOPs: five tile GEMMs; the kernels execute seven)",
+                "kernel_ms": {"mean": mean_ms, "min": min(durs), "max": max(durs)}}
+    e2e = None
+    if not args.no_e2e:
+        hs = [t.pin_memory() for t in (x.q, x.k, x.v)] + [do_h.pin_memory(), o.cpu().pin_memory(),
+                                                           lse.cpu().pin_memory()]
+        outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+        devs = (q, k, v, do, o, lse)
+
+        def e2e_step():
+            for d_, h_ in zip(devs, hs):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for h_, d_ in zip(outs_h, (dq, dk, dv)):
+                h_.copy_(d_, non_blocking=True)
+
+        for _ in range(max(args.warmup, 0)):
+            e2e_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        ms = max_over_ranks(dist, e0.elapsed_time(e1))
+        e2e = {"value": flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hs),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h),
+               "ms_per_step": ms / args.steps, "entry_point": "attn_bwd on pinned host copies"}
+    clocks = sampler.summary(t_host0, t_host1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tflops, desc, secs, _ = bwd_cpu_sample(w, x, do_h, args.cpu_seconds)
+        cpu = {"value": tflops, "unit": "TFLOP/s", "cores": cores_used(), "kind": "oracle",
+               "sample": desc + f"; {secs:.1f} s of CPU work"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": bwd_config(w), "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": args.steps * 3, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 # ------------------------------------------------------------------------------------ ragged batch
 def varlen_config(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "d": w.d, "causal": w.causal,
@@ -717,6 +881,16 @@ def main(argv=None):
             return 0
         x = inputs.make_varlen_inputs(w)
         (run_varlen_reference if args.impl == "reference" else run_varlen_ours)(args, w, x)
+        return 0
+    if name in inputs.BWD_WORKLOADS:
+        w = inputs.BWD_WORKLOADS[name]
+        if args.batch is not None:
+            w = w.replace(B=args.batch, name=f"{w.name}_b{args.batch}")
+        rank, world, _ = rank_info()
+        if args.impl == "reference" and rank != 0:
+            return 0
+        x = inputs.make_inputs(w)
+        (run_bwd_reference if args.impl == "reference" else run_bwd_ours)(args, w, x)
         return 0
     table = {**inputs.WORKLOADS, **inputs.DECODE_WORKLOADS, **inputs.FP8_BLOCK_WORKLOADS}
     w = table[name]

@@ -57,6 +57,10 @@ def lib() -> ctypes.CDLL:
     L.attn_varlen_plan.argtypes = [vp, vp, i, i, i, i, i, i, vp, sz, vp]
     L.attn_fwd_varlen.restype = i
     L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp, vp, vp, vp]
+    L.attn_bwd_workspace_bytes.restype = sz
+    L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
+    L.attn_bwd.restype = i
+    L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -241,6 +245,39 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, plan, causal: bool, sca
                                ptrs[1] or None, ptrs[2] or None, _stream_handle(stream))
     _check(st, "attn_fwd_varlen")
     return out, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, N: int) -> int:
+    return int(lib().attn_bwd_workspace_bytes(B, H, N))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool, scale: Optional[float] = None, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of attn_fwd for bf16 q/o/dout [B,N,H,d], k/v [B,N,Hkv,d], lse [B,H,N]."""
+    import torch
+    B, N, H, d = q.shape
+    Hkv = k.shape[2]
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    if k.shape != (B, N, Hkv, d) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shapes: q, o, dout [B, N, H, d]; k, v [B, N, Hkv, d]")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_cuda or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 CUDA tensor [B, H, N]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = attn_bwd_workspace_bytes(B, H, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Hkv, N, d, float(scale),
+                        int(bool(causal)), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 ATTN_FP8_Q_BLOCK = 128   # query rows per q descale block (attn_fwd_fp8_blockscaled)

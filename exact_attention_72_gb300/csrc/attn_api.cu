@@ -628,6 +628,70 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+size_t attn_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  const size_t np = ((size_t)N + 127) / 128 * 128;
+  return 2 * round_up((size_t)B * H * np * 4, 256);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N, int d,
+                       float scale, int causal, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  attn_status_t st = check_shape(B, H, Hkv, N, d, scale, ATTN_DTYPE_BF16);
+  if (st != ATTN_OK) return st;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;   // dK, dV, S, dP must fit TMEM's 512 columns
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace) return ATTN_ERR_INVALID_ARG;
+  const void* a16[8] = {q, k, v, o, dout, dq, dk, dv};
+  for (const void* ptr : a16)
+    if (!aligned(ptr, 16)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, N)) return ATTN_ERR_INVALID_ARG;
+  const size_t nq = (size_t)B * N * H * d * 2, nkv = (size_t)B * N * Hkv * d * 2, nl = (size_t)B * H * N * 4;
+  // outputs (and the workspace) must not overlap any input or each other
+  const void* outs[4] = {dq, dk, dv, workspace};
+  const size_t out_bytes[4] = {nq, nkv, nkv, workspace_bytes};
+  const void* ins[6] = {q, k, v, o, dout, lse};
+  const size_t in_bytes[6] = {nq, nkv, nkv, nq, nq, nl};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (ranges_overlap(outs[i], out_bytes[i], ins[j], in_bytes[j])) return ATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (ranges_overlap(outs[i], out_bytes[i], outs[j], out_bytes[j])) return ATTN_ERR_INVALID_ARG;
+  }
+  DeviceInfo* di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  gb300::BwdLaunchArgs a;
+  memset(&a, 0, sizeof(a));
+  if (!make_map(&a.tm_q, q, false, d, N, H, B) || !make_map(&a.tm_do, dout, false, d, N, H, B) ||
+      !make_map(&a.tm_k, k, false, d, N, Hkv, B) || !make_map(&a.tm_v, v, false, d, N, Hkv, B))
+    return ATTN_ERR_CUDA;
+  const int np = (N + 127) / 128 * 128;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.lse2 = static_cast<float*>(workspace);
+  a.dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)B * H * np * 4, 256));
+  a.num_sms = di->num_sms;
+  gb300::BwdParams& p = a.params;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.lse2 = a.lse2;
+  p.dd = a.dd;
+  p.B = B;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
+  p.N = N;
+  p.Np = np;
+  p.n_t = np / 128;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = di->status;
+  p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
+  return gb300::launch_attn_bwd(a, d, causal != 0, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 size_t attn_quantize_e4m3_descale_count(int B, int N, int Hx, int block_rows) {
   if (B < 1 || N < 1 || Hx < 1 || block_rows < 1) return 0;
   return (size_t)B * Hx * (size_t)((N + (long long)block_rows - 1) / block_rows);

@@ -1,0 +1,552 @@
+// Backward pass of the fused attention forward on sm_103a: dQ, dK, dV from Q, K, V, dO, the
+// forward's LSE and D = rowsum(dO * O).
+//
+// With S = scale Q K^T (+ causal mask), P = exp(S - LSE) row by row, dP = dO V^T and
+// dS = P * (dP - D): dV = P^T dO, dK = scale dS^T Q, dQ = scale dS K. P is recomputed from the
+// LSE the forward wrote; nothing else of the forward is kept. The pages name the pieces of the
+// FA3 backward: recomputation, a preprocess that forms D and the base-2 LSE, dQ accumulation,
+// the GQA path for dK and dV, and a longest-first scheduler for causal masking
+// ("FlashAttention-3 Deep Dive" (mojostudio.in), its backward-pass sections; "flash-attention-3"
+// (ai.thesatyajit.com), "Five schedulers").
+//
+// Two kernels, no atomics. Each recomputes S and dP on the tensor cores (tcgen05, fp32 in TMEM)
+// and keeps one fp32 accumulator tile in TMEM for its whole loop:
+//   * attn_bwd_dkdv_kernel: one CTA per (batch, kv head, 128-key tile j). It loops over every
+//     query head of the kv head's group and every 128-row query tile i that sees tile j,
+//     computing S^T = K_j Q_i^T and dP^T = V_j dO_i^T with keys as TMEM lanes, so P^T and dS^T
+//     (bf16, written over S^T and dP^T in TMEM) are the A operands of dV += P^T dO_i and
+//     dK += dS^T Q_i. The GQA sum over query heads happens inside the CTA.
+//   * attn_bwd_dq_kernel: one CTA per (batch, query head, 128-row query tile i); it loops over
+//     the key tiles j that tile i sees, computing S and dP with queries as lanes and
+//     dQ += dS K_j with dS (bf16, written over S in TMEM) as the A operand.
+// S and dP are computed twice in all (once per kernel): 7 tile GEMMs against 5 for a single
+// kernel that accumulates dQ across CTAs, traded for deterministic results and no fp32 atomic
+// traffic.
+//
+// Roles (192 threads): warps 0-3 elementwise (thread = TMEM lane = one row of the 128-row tile),
+// warp 4 issues the MMAs, warp 5 the TMA loads. Every wait is bounded (status word + abort flag).
+#pragma once
+#include "attn_fwd_kernel.cuh"
+
+namespace gb300 {
+
+struct BwdParams {
+  __nv_bfloat16* dq;     // [B, N, H, D]
+  __nv_bfloat16* dk;     // [B, N, Hkv, D]
+  __nv_bfloat16* dv;     // [B, N, Hkv, D]
+  const float* lse2;     // [B, H, Np]: LSE * log2(e); rows from N to Np: +inf
+  const float* dd;       // [B, H, Np]: rowsum(dO * O); rows from N to Np: 0
+  int B, H, Hkv, G, N, Np;   // Np: N rounded up to a multiple of 128
+  int n_t;                   // 128-row tiles per sequence (queries and keys alike)
+  float scale, scale_log2;
+  int n_tiles;
+  uint32_t* status;
+  unsigned long long timeout_ns;
+};
+
+template <int D_, bool CAUSAL_>
+struct BwdCfg {
+  static constexpr int D = D_;
+  static constexpr bool CAUSAL = CAUSAL_;
+  static constexpr bool FP8 = false;
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int CE = 64;                           // bf16 elements in one 128-byte row
+  static constexpr int NCH = D / CE;
+  static constexpr int CHUNK_BYTES = 128 * 128;
+  static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // 128 rows x D bf16
+  static constexpr int KSTEPS_QK = D / 16;
+  static constexpr int KSTEPS_PV = 8;                     // 128 rows of the MN-major B operand
+  static constexpr int PV_ROWS = 16;
+  static constexpr uint32_t IDESC_QK = make_idesc(kFmtBF16, 128, 128, false, false);
+  static constexpr uint32_t IDESC_PV = make_idesc(kFmtBF16, 128, D, false, true);
+  static constexpr int STAGES = 2;
+  static constexpr int VEC_BYTES = 2 * 128 * 4;           // per stage: LSE2 and D of 128 query rows
+  // shared memory: two resident tiles, then STAGES x (two streamed tiles), then the vectors
+  static constexpr int SMEM_USED = 2 * TILE_BYTES + STAGES * 2 * TILE_BYTES + STAGES * VEC_BYTES + 1024;
+  // At least 116 KB so that one CTA holds an SM: each takes all 512 TMEM columns.
+  static constexpr int SMEM_BYTES = SMEM_USED > 118784 ? SMEM_USED : 118784;
+  // TMEM columns: S (or S^T, later P / dS in bf16) at 0, dP at 128, accumulators from 256
+  static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int THREADS = 192;
+  static constexpr int WARP_MMA = 4, WARP_LOAD = 5;
+  static_assert(ACC1 + D <= TMEM_COLS, "TMEM budget: head dim up to 128");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+enum : uint32_t { SITE_B_KV = 21, SITE_B_ST = 22, SITE_B_S = 23, SITE_B_P = 24, SITE_B_ACC = 25, SITE_B_EMPTY = 26 };
+
+// dst (+)= A[tmem, bf16, 128 x 128] * B[smem, 128 x D, MN-major]: 8 k-steps of 16.
+template <class C>
+__device__ __forceinline__ void issue_ts_128(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr, bool accumulate) {
+  const uint64_t b0 = make_sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+#pragma unroll
+  for (int kk = 0; kk < C::KSTEPS_PV; ++kk)
+    mma_f16_ts(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4), C::IDESC_PV,
+               (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// Writes the lane's row of an fp32 accumulator (D columns at tcol) times `mul` as bf16 to dst.
+template <int D>
+__device__ __forceinline__ void store_acc_row(uint32_t tcol, float mul, __nv_bfloat16* dst, bool valid) {
+#pragma unroll 1
+  for (int c0 = 0; c0 < D; c0 += 32) {
+    uint32_t v[32];
+    tmem_ld_32cols(tcol + c0, v);
+    tmem_ld_wait();
+    reg_fence32(v);
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 32; c += 2) pk[c >> 1] = pack_bf16x2(__uint_as_float(v[c]) * mul, __uint_as_float(v[c + 1]) * mul);
+    if (valid) {
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// dK, dV: one CTA per (b, kv head, key tile j); steps over (query head g of the group, tile i).
+// Causal: tile j is seen by query tiles i >= j; tiles go in ascending j (the longest first).
+// ---------------------------------------------------------------------------------------------
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty, bar_st_full[C::STAGES], bar_st_empty[C::STAGES];
+  __shared__ __align__(8) uint64_t bar_s_full, bar_p_ready, bar_acc_full, bar_acc_empty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile uint32_t abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sK = smem_addr(smem), sV = sK + C::TILE_BYTES;
+  const uint32_t sStage = sV + C::TILE_BYTES;                          // stage s: Q at +0, dO at +TILE
+  float* vec = reinterpret_cast<float*>(smem + 2 * C::TILE_BYTES + C::STAGES * 2 * C::TILE_BYTES);
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+  if (tid == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_addr(&bar_kv_full), 1);
+    mbar_init(smem_addr(&bar_kv_empty), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_addr(&bar_st_full[s]), 1);
+      mbar_init(smem_addr(&bar_st_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar_s_full), 1);
+    mbar_init(smem_addr(&bar_p_ready), 128);
+    mbar_init(smem_addr(&bar_acc_full), 1);
+    mbar_init(smem_addr(&bar_acc_empty), 128);
+    mbar_init(smem_addr(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(smem_addr(&tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int BHkv = p.B * p.Hkv;
+  // work tile t -> (b, kv head, key tile j); steps of the tile
+  auto decode = [&](int t, int& b, int& kvh, int& j, int& i0) {
+    j = t / BHkv;
+    const int bh = t % BHkv;
+    b = bh / p.Hkv;
+    kvh = bh % p.Hkv;
+    i0 = C::CAUSAL ? j : 0;
+  };
+
+  if (warp == C::WARP_LOAD) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      uint32_t tiles = 0, steps = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        int b, kvh, j, i0;
+        decode(t, b, kvh, j, i0);
+        if (tiles > 0 && !mbar_wait(smem_addr(&bar_kv_empty), (tiles - 1) & 1, ctl, SITE_B_EMPTY)) { ok = false; break; }
+        mbar_arrive_expect_tx(smem_addr(&bar_kv_full), 2 * C::TILE_BYTES);
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          tma_load_4d(sK + ch * C::CHUNK_BYTES, &tm_k, smem_addr(&bar_kv_full), ch * C::CE, j * 128, kvh, b);
+          tma_load_4d(sV + ch * C::CHUNK_BYTES, &tm_v, smem_addr(&bar_kv_full), ch * C::CE, j * 128, kvh, b);
+        }
+        ++tiles;
+        const int ni = p.n_t - i0;
+        for (int k = 0; ok && k < p.G * ni; ++k) {
+          const int h = kvh * p.G + k / ni, i = i0 + k % ni;
+          const int s = steps % C::STAGES;
+          if (steps >= (uint32_t)C::STAGES &&
+              !mbar_wait(smem_addr(&bar_st_empty[s]), ((steps / C::STAGES) - 1) & 1, ctl, SITE_B_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(&bar_st_full[s]);
+          const uint32_t dst = sStage + s * 2 * C::TILE_BYTES;
+          mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES + C::VEC_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            tma_load_4d(dst + ch * C::CHUNK_BYTES, &tm_q, bar, ch * C::CE, i * 128, h, b);
+            tma_load_4d(dst + C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_do, bar, ch * C::CE, i * 128, h, b);
+          }
+          const size_t row = ((size_t)b * p.H + h) * p.Np + (size_t)i * 128;
+          bulk_load(smem_addr(vec + s * 256), p.lse2 + row, 512, bar);
+          bulk_load(smem_addr(vec + s * 256 + 128), p.dd + row, 512, bar);
+          ++steps;
+        }
+      }
+      if (!ok) {
+        // let copies still in flight land before the CTA exits
+        for (uint32_t q = steps > (uint32_t)C::STAGES ? steps - C::STAGES : 0u; q < steps; ++q) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_st_full[q % C::STAGES]), (q / C::STAGES) & 1) &&
+                 global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+        if (tiles > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_kv_full), (tiles - 1) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+      }
+    }
+  } else if (warp == C::WARP_MMA) {
+    if (lane == 0) {
+      uint32_t tiles = 0, steps = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        int b, kvh, j, i0;
+        decode(t, b, kvh, j, i0);
+        if (!mbar_wait(smem_addr(&bar_kv_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
+        const int n = p.G * (p.n_t - i0);
+        for (int k = 0; k < n; ++k) {
+          const int s = steps % C::STAGES;
+          const uint32_t sQ = sStage + s * 2 * C::TILE_BYTES, sdO = sQ + C::TILE_BYTES;
+          if (!mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk<C>(tmem + C::S_COL, sK, sQ);     // S^T = K_j Q_i^T
+          issue_qk<C>(tmem + C::DP_COL, sV, sdO);   // dP^T = V_j dO_i^T
+          tc_commit(smem_addr(&bar_s_full));
+          if (!mbar_wait(smem_addr(&bar_p_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+          if (k == 0 && tiles > 0 &&
+              !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
+          tc_fence_after();
+          issue_ts_128<C>(tmem + C::ACC0, tmem + C::S_COL, sdO, k > 0);    // dV += P^T dO_i
+          issue_ts_128<C>(tmem + C::ACC1, tmem + C::DP_COL, sQ, k > 0);    // dK += dS^T Q_i
+          tc_commit(smem_addr(&bar_st_empty[s]));
+          ++steps;
+        }
+        if (!ok) break;
+        tc_commit(smem_addr(&bar_acc_full));
+        tc_commit(smem_addr(&bar_kv_empty));
+        ++tiles;
+      }
+      tc_commit(smem_addr(&bar_drain));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else {
+    // elementwise: thread = key row r of the tile (TMEM lane)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::S_COL, tP = tmem + lane_base + C::DP_COL;
+    uint32_t tiles = 0, steps = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      int b, kvh, j, i0;
+      decode(t, b, kvh, j, i0);
+      const int key = j * 128 + r;
+      const int ni = p.n_t - i0;
+      for (int k = 0; k < p.G * ni; ++k) {
+        const int i = i0 + k % ni;
+        const int s = steps % C::STAGES;
+        // S^T, dP^T in TMEM, and this stage's LSE2 / D vectors in shared memory (the stage is not
+        // refilled before this step's p_ready arrival)
+        bool w = mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
+        w = w && mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        const float* lse2 = vec + s * 256;
+        const float* dd = lse2 + 128;
+        const bool diag = C::CAUSAL && i == j;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t sv[32], dv[32];
+          tmem_ld_32cols(tS + c0, sv);
+          tmem_ld_32cols(tP + c0, dv);
+          tmem_ld_wait();
+          reg_fence32(sv);
+          reg_fence32(dv);
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float pr[2], dsr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = c0 + c + e;   // query row i*128 + col
+              float pv = ex2(__uint_as_float(sv[c + e]) * p.scale_log2 - lse2[col]);
+              if (diag && col < r) pv = 0.0f;   // key after the query
+              pr[e] = pv;
+              dsr[e] = pv * (__uint_as_float(dv[c + e]) - dd[col]);
+            }
+            pk[c >> 1] = pack_bf16x2(pr[0], pr[1]);
+            dk[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
+          }
+          tmem_st_16cols(tS + (c0 >> 1), pk);   // P^T over the S^T columns already read
+          tmem_st_16cols(tP + (c0 >> 1), dk);   // dS^T over the dP^T columns already read
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_p_ready));
+        ++steps;
+      }
+      if (!ok) break;
+      const bool w = mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = key < p.N;
+      const size_t orow = ((size_t)(b * p.N + (valid ? key : 0)) * p.Hkv + kvh) * C::D;
+      store_acc_row<C::D>(tmem + lane_base + C::ACC0, 1.0f, p.dv + orow, valid);
+      store_acc_row<C::D>(tmem + lane_base + C::ACC1, p.scale, p.dk + orow, valid);
+      tc_fence_before();
+      mbar_arrive(smem_addr(&bar_acc_empty));
+      ++tiles;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------------------------
+// dQ: one CTA per (b, query head, query tile i); steps over the key tiles i sees.
+// Causal: tile i sees key tiles j <= i; tiles go in descending i (the longest first).
+// ---------------------------------------------------------------------------------------------
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1)
+attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const BwdParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_st_full[C::STAGES], bar_st_empty[C::STAGES];
+  __shared__ __align__(8) uint64_t bar_s_full, bar_p_ready, bar_acc_full, bar_acc_empty, bar_drain;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile uint32_t abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_addr(smem), sdO = sQ + C::TILE_BYTES;
+  const uint32_t sStage = sdO + C::TILE_BYTES;                         // stage s: K at +0, V at +TILE
+  const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
+  if (tid == 0) {
+    abort_flag = 0u;
+    mbar_init(smem_addr(&bar_q_full), 1);
+    mbar_init(smem_addr(&bar_q_empty), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_addr(&bar_st_full[s]), 1);
+      mbar_init(smem_addr(&bar_st_empty[s]), 1);
+    }
+    mbar_init(smem_addr(&bar_s_full), 1);
+    mbar_init(smem_addr(&bar_p_ready), 128);
+    mbar_init(smem_addr(&bar_acc_full), 1);
+    mbar_init(smem_addr(&bar_acc_empty), 128);
+    mbar_init(smem_addr(&bar_drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == C::WARP_MMA) {
+    tmem_alloc(smem_addr(&tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int BH = p.B * p.H;
+  auto decode = [&](int t, int& b, int& h, int& i, int& nj) {
+    i = C::CAUSAL ? p.n_t - 1 - t / BH : t / BH;
+    const int bh = t % BH;
+    b = bh / p.H;
+    h = bh % p.H;
+    nj = C::CAUSAL ? i + 1 : p.n_t;
+  };
+
+  if (warp == C::WARP_LOAD) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+      uint32_t tiles = 0, steps = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        int b, h, i, nj;
+        decode(t, b, h, i, nj);
+        const int kvh = h / p.G;
+        if (tiles > 0 && !mbar_wait(smem_addr(&bar_q_empty), (tiles - 1) & 1, ctl, SITE_B_EMPTY)) { ok = false; break; }
+        mbar_arrive_expect_tx(smem_addr(&bar_q_full), 2 * C::TILE_BYTES);
+        for (int ch = 0; ch < C::NCH; ++ch) {
+          tma_load_4d(sQ + ch * C::CHUNK_BYTES, &tm_q, smem_addr(&bar_q_full), ch * C::CE, i * 128, h, b);
+          tma_load_4d(sdO + ch * C::CHUNK_BYTES, &tm_do, smem_addr(&bar_q_full), ch * C::CE, i * 128, h, b);
+        }
+        ++tiles;
+        for (int jj = 0; ok && jj < nj; ++jj) {
+          const int s = steps % C::STAGES;
+          if (steps >= (uint32_t)C::STAGES &&
+              !mbar_wait(smem_addr(&bar_st_empty[s]), ((steps / C::STAGES) - 1) & 1, ctl, SITE_B_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t bar = smem_addr(&bar_st_full[s]);
+          const uint32_t dst = sStage + s * 2 * C::TILE_BYTES;
+          mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch) {
+            tma_load_4d(dst + ch * C::CHUNK_BYTES, &tm_k, bar, ch * C::CE, jj * 128, kvh, b);
+            tma_load_4d(dst + C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v, bar, ch * C::CE, jj * 128, kvh, b);
+          }
+          ++steps;
+        }
+      }
+      if (!ok) {
+        for (uint32_t q = steps > (uint32_t)C::STAGES ? steps - C::STAGES : 0u; q < steps; ++q) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_st_full[q % C::STAGES]), (q / C::STAGES) & 1) &&
+                 global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+        if (tiles > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_q_full), (tiles - 1) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+      }
+    }
+  } else if (warp == C::WARP_MMA) {
+    if (lane == 0) {
+      uint32_t tiles = 0, steps = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+        int b, h, i, nj;
+        decode(t, b, h, i, nj);
+        if (!mbar_wait(smem_addr(&bar_q_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
+        for (int jj = 0; jj < nj; ++jj) {
+          const int s = steps % C::STAGES;
+          const uint32_t sK = sStage + s * 2 * C::TILE_BYTES, sV = sK + C::TILE_BYTES;
+          if (!mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST)) { ok = false; break; }
+          tc_fence_after();
+          issue_qk<C>(tmem + C::S_COL, sQ, sK);     // S = Q_i K_j^T
+          issue_qk<C>(tmem + C::DP_COL, sdO, sV);   // dP = dO_i V_j^T
+          tc_commit(smem_addr(&bar_s_full));
+          if (!mbar_wait(smem_addr(&bar_p_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+          if (jj == 0 && tiles > 0 &&
+              !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
+          tc_fence_after();
+          issue_ts_128<C>(tmem + C::ACC0, tmem + C::S_COL, sK, jj > 0);    // dQ += dS K_j
+          tc_commit(smem_addr(&bar_st_empty[s]));
+          ++steps;
+        }
+        if (!ok) break;
+        tc_commit(smem_addr(&bar_acc_full));
+        tc_commit(smem_addr(&bar_q_empty));
+        ++tiles;
+      }
+      tc_commit(smem_addr(&bar_drain));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else {
+    // elementwise: thread = query row r of the tile (TMEM lane)
+    const int r = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t tS = tmem + lane_base + C::S_COL, tP = tmem + lane_base + C::DP_COL;
+    uint32_t tiles = 0, steps = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      int b, h, i, nj;
+      decode(t, b, h, i, nj);
+      const int qrow = i * 128 + r;
+      const size_t vrow = ((size_t)b * p.H + h) * p.Np + qrow;   // padded rows: +inf / 0
+      const float lse2 = __ldg(p.lse2 + vrow), dd = __ldg(p.dd + vrow);
+      for (int jj = 0; jj < nj; ++jj) {
+        const bool w = mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        const bool diag = C::CAUSAL && jj == i;
+        const bool tail = jj == p.n_t - 1 && (p.N & 127) != 0;
+        const int lim = diag ? r + 1 : (tail ? (p.N & 127) : 128);   // keys of this tile the row sees
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t sv[32], dv[32];
+          tmem_ld_32cols(tS + c0, sv);
+          tmem_ld_32cols(tP + c0, dv);
+          tmem_ld_wait();
+          reg_fence32(sv);
+          reg_fence32(dv);
+          uint32_t dk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float dsr[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              float pv = ex2(__uint_as_float(sv[c + e]) * p.scale_log2 - lse2);
+              if (c0 + c + e >= lim) pv = 0.0f;
+              dsr[e] = pv * (__uint_as_float(dv[c + e]) - dd);
+            }
+            dk[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
+          }
+          tmem_st_16cols(tS + (c0 >> 1), dk);   // dS over the S columns already read
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_p_ready));
+        ++steps;
+      }
+      if (!ok) break;
+      const bool w = mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      const bool valid = qrow < p.N;
+      const size_t orow = ((size_t)(b * p.N + (valid ? qrow : 0)) * p.H + h) * C::D;
+      store_acc_row<C::D>(tmem + lane_base + C::ACC0, p.scale, p.dq + orow, valid);
+      tc_fence_before();
+      mbar_arrive(smem_addr(&bar_acc_empty));
+      ++tiles;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// D = rowsum(dO * O) and LSE * log2(e), per (b, h, row), rows padded to Np (D = 0, LSE2 = +inf).
+template <int D>
+__global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
+                                                                 const float* lse, float* lse2, float* dd, int B,
+                                                                 int H, int N, int Np) {
+  const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // one warp per row
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)B * H * Np) return;
+  const int row = (int)(w % Np);
+  const long long bh = w / Np;
+  const int h = (int)(bh % H), b = (int)(bh / H);
+  float acc = 0.0f;
+  if (row < N) {
+    const size_t base = ((size_t)(b * N + row) * H + h) * D;
+#pragma unroll
+    for (int c = lane * 2; c < D; c += 64) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(o + base + c));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + base + c));
+      acc = fmaf(x.x, y.x, fmaf(x.y, y.y, acc));
+    }
+  }
+#pragma unroll
+  for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (lane == 0) {
+    dd[w] = acc;
+    lse2[w] = row < N ? lse[bh * N + row] * 1.4426950408889634f : INFINITY;
+  }
+}
+
+}  // namespace gb300

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 
 namespace gb300 {
@@ -16,6 +17,19 @@ struct LaunchArgs {
 // the split-KV (decode) mode of the kernel, VARLEN the ragged-batch mode driven by a tile plan.
 template <int D, bool CAUSAL, bool FP8, bool SPLIT = false, bool VARLEN = false>
 cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream);
+
+// Backward pass (attn_bwd.cu): preprocess, then the dK/dV and dQ kernels, on one stream.
+struct BwdLaunchArgs {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  BwdParams params;          // n_tiles is set per kernel
+  const void* o;             // bf16 [B, N, H, D]
+  const void* dout;          // bf16 [B, N, H, D]
+  const float* lse;          // [B, H, N]
+  float* lse2;               // workspace [B, H, Np]
+  float* dd;                 // workspace [B, H, Np]
+  int num_sms;
+};
+cudaError_t launch_attn_bwd(BwdLaunchArgs& a, int d, bool causal, cudaStream_t stream);
 
 // Builds the ragged-batch tile plan (varlen_plan.cu): one CTA on the stream.
 cudaError_t launch_varlen_plan(const int* cu_q, const int* cu_k, int B, int H, int rows_per_tile, bool causal,

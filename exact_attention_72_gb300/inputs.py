@@ -121,6 +121,21 @@ FP8_BLOCK_WORKLOADS = {
 }
 
 
+# Backward pass on the GQA configuration's shape: q, k, v and the output gradient dO drawn in that
+# order (fp32 randn, rounded to bf16); O and LSE come from the forward.
+BWD_WORKLOADS = {
+    "bwd_causal_gqa_bf16_n8192_d128": Workload("bwd_causal_gqa_bf16_n8192_d128", B=2, H=32, Hkv=8, N=8192, d=128,
+                                               causal=True, seed=1401),
+}
+
+
+def make_grad_output(w: Workload, seed: Optional[int] = None) -> torch.Tensor:
+    """Seeded output gradient dO [B, N, H, d] in bf16 (drawn after q, k, v from its own seed)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed((w.seed if seed is None else seed) + 100000)
+    return torch.randn((w.B, w.N, w.H, w.d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
 @dataclasses.dataclass(frozen=True)
 class VarlenWorkload:
     """A ragged batch: sequence b has lengths_q[b] queries and lengths_k[b] keys, packed by rows."""

@@ -138,6 +138,28 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
                               const float* descale_q, const float* descale_k,
                               const float* descale_v, cudaStream_t stream);
 
+/*
+ * attn_bwd — gradients of attn_fwd (bf16, d in {64, 128}): dQ, dK, dV from q, k, v, the
+ * forward's output o and LSE, and the output gradient dout. With S = scale q k^T (+ causal
+ * mask), P = exp(S - LSE), dP = dout v^T and D = rowsum(dout * o): dS = P * (dP - D),
+ * dv = P^T dout, dk = scale dS^T q, dq = scale dS k; with GQA, dk and dv sum over each kv
+ * head's query heads. P is recomputed from the LSE. "FlashAttention-3 Deep Dive" (mojostudio.in),
+ * the backward-pass sections (recomputation, the D / LSE preprocess, the GQA path);
+ * "flash-attention-3" (ai.thesatyajit.com), "Five schedulers" (longest-first causal backward).
+ *   q, dout, o, dq: DEVICE bf16 [B, N, H, d]; k, v, dk, dv: DEVICE bf16 [B, N, Hkv, d];
+ *   lse: DEVICE fp32 [B, H, N] as attn_fwd wrote it; all 16-byte aligned (lse 4).
+ *   workspace: DEVICE, 256-byte aligned, >= attn_bwd_workspace_bytes(B, H, N): D and the base-2
+ *   LSE, rows padded to a multiple of 128. Outputs and workspace must not overlap the inputs or
+ *   each other. Three kernels on `stream` (preprocess, dK/dV, dQ); no atomics, so the results
+ *   are deterministic. INVALID_ARG / UNSUPPORTED as attn_fwd (d == 256 is UNSUPPORTED here);
+ *   a bounded wait that gives up is reported by attn_get_status.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N);
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int H, int Hkv, int N,
+                       int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                       cudaStream_t stream);
+
 /* Rows per descale block of the block-scaled e4m3 forward: q in blocks of 128 query positions,
  * k in blocks of 64 key positions, both within one (batch, head). */
 #define ATTN_FP8_Q_BLOCK 128
