@@ -18,13 +18,21 @@
 //     dK += dS^T Q_i. The GQA sum over query heads happens inside the CTA.
 //   * attn_bwd_dq_kernel: one CTA per (batch, query head, 128-row query tile i); it loops over
 //     the key tiles j that tile i sees, computing S and dP with queries as lanes and
-//     dQ += dS K_j with dS (bf16, written over S in TMEM) as the A operand.
+//     dQ += dS K_j with dS (bf16, written over S in TMEM) as the A operand. S is double-buffered
+//     (TMEM has room here), so S_{j+1} runs while the elementwise warps work on step j.
 // S and dP are computed twice in all (once per kernel): 7 tile GEMMs against 5 for a single
 // kernel that accumulates dQ across CTAs, traded for deterministic results and no fp32 atomic
 // traffic.
 //
-// Roles (192 threads): warps 0-3 elementwise (thread = TMEM lane = one row of the 128-row tile),
-// warp 4 issues the MMAs, warp 5 the TMA loads. Every wait is bounded (status word + abort flag).
+// Roles (320 threads): warps 0-7 elementwise, two warpgroups that split the 128 columns of a
+// tile (thread = TMEM lane = one row, warpgroup g = columns 64g .. 64g+63); warp 8 issues the
+// MMAs, warp 9 the TMA loads. The elementwise work of a step runs in two passes with their own
+// barriers: P from S (the dV GEMM can start, while the dP GEMM may still run), then dS from dP.
+// bf16 results are written in place over the fp32 columns they came from, so both warpgroups
+// read their whole half first and meet at a named barrier before any write: packed column c/2
+// of one half lies in the fp32 columns of the other. Every wait is bounded (status word + abort
+// flag); on a failed wait the elementwise warps keep stepping through the named barriers without
+// work, so no warp is left at a barrier.
 #pragma once
 #include "attn_fwd_kernel.cuh"
 
@@ -68,9 +76,13 @@ struct BwdCfg {
   // TMEM columns: S (or S^T, later P / dS in bf16) at 0, dP at 128, accumulators from 256
   static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 192;
-  static constexpr int WARP_MMA = 4, WARP_LOAD = 5;
+  static constexpr int THREADS = 320;
+  static constexpr int EW_THREADS = 256;                  // elementwise warps 0-7
+  static constexpr int WARP_MMA = 8, WARP_LOAD = 9;
+  // dQ kernel: S double buffer at 0 and 128, dP at 256, dQ at 384
+  static constexpr int Q_S0 = 0, Q_S1 = 128, Q_DP = 256, Q_ACC = 384;
   static_assert(ACC1 + D <= TMEM_COLS, "TMEM budget: head dim up to 128");
+  static_assert(Q_ACC + D <= TMEM_COLS, "TMEM budget (dQ kernel)");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -86,11 +98,12 @@ __device__ __forceinline__ void issue_ts_128(uint32_t d_tmem, uint32_t a_tmem, u
                (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// Writes the lane's row of an fp32 accumulator (D columns at tcol) times `mul` as bf16 to dst.
-template <int D>
-__device__ __forceinline__ void store_acc_row(uint32_t tcol, float mul, __nv_bfloat16* dst, bool valid) {
+// Writes columns [c_begin, c_end) of the lane's row of an fp32 accumulator (at tcol) times `mul`
+// as bf16 to dst (the row's first column).
+__device__ __forceinline__ void store_acc_row(uint32_t tcol, int c_begin, int c_end, float mul, __nv_bfloat16* dst,
+                                              bool valid) {
 #pragma unroll 1
-  for (int c0 = 0; c0 < D; c0 += 32) {
+  for (int c0 = c_begin; c0 < c_end; c0 += 32) {
     uint32_t v[32];
     tmem_ld_32cols(tcol + c0, v);
     tmem_ld_wait();
@@ -106,6 +119,32 @@ __device__ __forceinline__ void store_acc_row(uint32_t tcol, float mul, __nv_bfl
   }
 }
 
+// Loads 64 fp32 columns (two 32-column reads) of the lane's row into x.
+__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, float* x) {
+  uint32_t a[32], b[32];
+  tmem_ld_32cols(taddr, a);
+  tmem_ld_32cols(taddr + 32, b);
+  tmem_ld_wait();
+  reg_fence32(a);
+  reg_fence32(b);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    x[c] = __uint_as_float(a[c]);
+    x[32 + c] = __uint_as_float(b[c]);
+  }
+}
+
+// Packs 64 values as bf16 pairs and writes them as 32 columns at taddr.
+__device__ __forceinline__ void tmem_st_64_as_bf16(uint32_t taddr, const float* x) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
+    tmem_st_16cols(taddr + 16 * h, pk);
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // dK, dV: one CTA per (b, kv head, key tile j); steps over (query head g of the group, tile i).
 // Causal: tile j is seen by query tiles i >= j; tiles go in ascending j (the longest first).
@@ -117,7 +156,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_kv_full, bar_kv_empty, bar_st_full[C::STAGES], bar_st_empty[C::STAGES];
-  __shared__ __align__(8) uint64_t bar_s_full, bar_p_ready, bar_acc_full, bar_acc_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_s_full, bar_dp_full, bar_p_ready, bar_ds_ready, bar_acc_full, bar_acc_empty;
+  __shared__ __align__(8) uint64_t bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -135,9 +175,11 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       mbar_init(smem_addr(&bar_st_empty[s]), 1);
     }
     mbar_init(smem_addr(&bar_s_full), 1);
-    mbar_init(smem_addr(&bar_p_ready), 128);
+    mbar_init(smem_addr(&bar_dp_full), 1);
+    mbar_init(smem_addr(&bar_p_ready), C::EW_THREADS);
+    mbar_init(smem_addr(&bar_ds_ready), C::EW_THREADS);
     mbar_init(smem_addr(&bar_acc_full), 1);
-    mbar_init(smem_addr(&bar_acc_empty), 128);
+    mbar_init(smem_addr(&bar_acc_empty), C::EW_THREADS);
     mbar_init(smem_addr(&bar_drain), 1);
     fence_mbar_init();
   }
@@ -227,13 +269,16 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           if (!mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST)) { ok = false; break; }
           tc_fence_after();
           issue_qk<C>(tmem + C::S_COL, sK, sQ);     // S^T = K_j Q_i^T
-          issue_qk<C>(tmem + C::DP_COL, sV, sdO);   // dP^T = V_j dO_i^T
           tc_commit(smem_addr(&bar_s_full));
+          issue_qk<C>(tmem + C::DP_COL, sV, sdO);   // dP^T = V_j dO_i^T
+          tc_commit(smem_addr(&bar_dp_full));
           if (!mbar_wait(smem_addr(&bar_p_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
           if (k == 0 && tiles > 0 &&
               !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
           tc_fence_after();
           issue_ts_128<C>(tmem + C::ACC0, tmem + C::S_COL, sdO, k > 0);    // dV += P^T dO_i
+          if (!mbar_wait(smem_addr(&bar_ds_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+          tc_fence_after();
           issue_ts_128<C>(tmem + C::ACC1, tmem + C::DP_COL, sQ, k > 0);    // dK += dS^T Q_i
           tc_commit(smem_addr(&bar_st_empty[s]));
           ++steps;
@@ -247,14 +292,16 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else {
-    // elementwise: thread = key row r of the tile (TMEM lane)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  } else if (warp < 8) {
+    // elementwise: thread = key row r of the tile (TMEM lane), warpgroup wg = query columns
+    // 64 wg .. 64 wg + 63
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::S_COL, tP = tmem + lane_base + C::DP_COL;
     uint32_t tiles = 0, steps = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
       int b, kvh, j, i0;
       decode(t, b, kvh, j, i0);
       const int key = j * 128 + r;
@@ -262,56 +309,62 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       for (int k = 0; k < p.G * ni; ++k) {
         const int i = i0 + k % ni;
         const int s = steps % C::STAGES;
-        // S^T, dP^T in TMEM, and this stage's LSE2 / D vectors in shared memory (the stage is not
-        // refilled before this step's p_ready arrival)
-        bool w = mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
+        // pass 1: P^T from S^T (this stage's LSE2 / D vectors are in shared memory; the stage is
+        // not refilled before this step's ds_ready arrival)
+        bool w = ok && mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
         w = w && mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        tc_fence_after();
-        const float* lse2 = vec + s * 256;
-        const float* dd = lse2 + 128;
+        ok = __all_sync(0xffffffffu, w);
+        const float* lse2 = vec + s * 256 + wg * 64;
+        const float* dd = vec + s * 256 + 128 + wg * 64;
         const bool diag = C::CAUSAL && i == j;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t sv[32], dv[32];
-          tmem_ld_32cols(tS + c0, sv);
-          tmem_ld_32cols(tP + c0, dv);
-          tmem_ld_wait();
-          reg_fence32(sv);
-          reg_fence32(dv);
-          uint32_t pk[16], dk[16];
+        float pf[64];
+        if (ok) {
+          tc_fence_after();
+          tmem_ld_64cols(tS + wg * 64, pf);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float pr[2], dsr[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = c0 + c + e;   // query row i*128 + col
-              float pv = ex2(__uint_as_float(sv[c + e]) * p.scale_log2 - lse2[col]);
-              if (diag && col < r) pv = 0.0f;   // key after the query
-              pr[e] = pv;
-              dsr[e] = pv * (__uint_as_float(dv[c + e]) - dd[col]);
-            }
-            pk[c >> 1] = pack_bf16x2(pr[0], pr[1]);
-            dk[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
+          for (int c = 0; c < 64; ++c) {
+            const float pv = ex2(pf[c] * p.scale_log2 - lse2[c]);
+            pf[c] = (diag && wg * 64 + c < r) ? 0.0f : pv;   // key after the query
           }
-          tmem_st_16cols(tS + (c0 >> 1), pk);   // P^T over the S^T columns already read
-          tmem_st_16cols(tP + (c0 >> 1), dk);   // dS^T over the dP^T columns already read
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_addr(&bar_p_ready));
+        named_bar_sync(1, C::EW_THREADS);   // every S^T column read before any P^T write
+        if (ok) {
+          tmem_st_64_as_bf16(tS + wg * 32, pf);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bar_p_ready));
+        }
+        // pass 2: dS^T = P^T * (dP^T - D)
+        w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
+        ok = __all_sync(0xffffffffu, w);
+        if (ok) {
+          float dp[64];
+          tc_fence_after();
+          tmem_ld_64cols(tP + wg * 64, dp);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pf[c] = pf[c] * (dp[c] - dd[c]);
+        }
+        named_bar_sync(2, C::EW_THREADS);   // every dP^T column read before any dS^T write
+        if (ok) {
+          tmem_st_64_as_bf16(tP + wg * 32, pf);
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bar_ds_ready));
+        }
         ++steps;
       }
-      if (!ok) break;
-      const bool w = mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
-      const bool valid = key < p.N;
-      const size_t orow = ((size_t)(b * p.N + (valid ? key : 0)) * p.Hkv + kvh) * C::D;
-      store_acc_row<C::D>(tmem + lane_base + C::ACC0, 1.0f, p.dv + orow, valid);
-      store_acc_row<C::D>(tmem + lane_base + C::ACC1, p.scale, p.dk + orow, valid);
-      tc_fence_before();
-      mbar_arrive(smem_addr(&bar_acc_empty));
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 dK
+      bool w = ok && mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
+      ok = __all_sync(0xffffffffu, w);
+      if (ok) {
+        tc_fence_after();
+        const bool valid = key < p.N;
+        const size_t orow = ((size_t)(b * p.N + (valid ? key : 0)) * p.Hkv + kvh) * C::D;
+        if (wg == 0) store_acc_row(tmem + lane_base + C::ACC0, 0, C::D, 1.0f, p.dv + orow, valid);
+        else store_acc_row(tmem + lane_base + C::ACC1, 0, C::D, p.scale, p.dk + orow, valid);
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_acc_empty));
+      }
       ++tiles;
     }
   }
@@ -333,7 +386,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_st_full[C::STAGES], bar_st_empty[C::STAGES];
-  __shared__ __align__(8) uint64_t bar_s_full, bar_p_ready, bar_acc_full, bar_acc_empty, bar_drain;
+  __shared__ __align__(8) uint64_t bar_s_full2[2], bar_dp_full, bar_ds_ready, bar_acc_full, bar_acc_empty, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -349,10 +402,12 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(smem_addr(&bar_st_full[s]), 1);
       mbar_init(smem_addr(&bar_st_empty[s]), 1);
     }
-    mbar_init(smem_addr(&bar_s_full), 1);
-    mbar_init(smem_addr(&bar_p_ready), 128);
+    mbar_init(smem_addr(&bar_s_full2[0]), 1);
+    mbar_init(smem_addr(&bar_s_full2[1]), 1);
+    mbar_init(smem_addr(&bar_dp_full), 1);
+    mbar_init(smem_addr(&bar_ds_ready), C::EW_THREADS);
     mbar_init(smem_addr(&bar_acc_full), 1);
-    mbar_init(smem_addr(&bar_acc_empty), 128);
+    mbar_init(smem_addr(&bar_acc_empty), C::EW_THREADS);
     mbar_init(smem_addr(&bar_drain), 1);
     fence_mbar_init();
   }
@@ -423,29 +478,40 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
   } else if (warp == C::WARP_MMA) {
     if (lane == 0) {
+      // S_j goes to buffer j % 2 (global step parity); S_{j+1} is issued before step j's dQ GEMM
       uint32_t tiles = 0, steps = 0;
       bool ok = true;
+      auto stage_k = [&](uint32_t st) { return sStage + (st % C::STAGES) * 2 * C::TILE_BYTES; };
+      auto issue_s = [&](uint32_t st) -> bool {
+        if (!mbar_wait(smem_addr(&bar_st_full[st % C::STAGES]), (st / C::STAGES) & 1, ctl, SITE_B_ST)) return false;
+        tc_fence_after();
+        issue_qk<C>(tmem + ((st & 1) ? C::Q_S1 : C::Q_S0), sQ, stage_k(st));   // S = Q_i K_j^T
+        tc_commit(smem_addr(&bar_s_full2[st & 1]));
+        return true;
+      };
+      auto issue_dp = [&](uint32_t st) {
+        issue_qk<C>(tmem + C::Q_DP, sdO, stage_k(st) + C::TILE_BYTES);           // dP = dO_i V_j^T
+        tc_commit(smem_addr(&bar_dp_full));
+      };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
         int b, h, i, nj;
         decode(t, b, h, i, nj);
         if (!mbar_wait(smem_addr(&bar_q_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
+        if (!issue_s(steps)) { ok = false; break; }
+        issue_dp(steps);
         for (int jj = 0; jj < nj; ++jj) {
-          const int s = steps % C::STAGES;
-          const uint32_t sK = sStage + s * 2 * C::TILE_BYTES, sV = sK + C::TILE_BYTES;
-          if (!mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST)) { ok = false; break; }
-          tc_fence_after();
-          issue_qk<C>(tmem + C::S_COL, sQ, sK);     // S = Q_i K_j^T
-          issue_qk<C>(tmem + C::DP_COL, sdO, sV);   // dP = dO_i V_j^T
-          tc_commit(smem_addr(&bar_s_full));
-          if (!mbar_wait(smem_addr(&bar_p_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+          const uint32_t cur = steps + jj;
+          if (jj + 1 < nj && !issue_s(cur + 1)) { ok = false; break; }
+          if (!mbar_wait(smem_addr(&bar_ds_ready), cur & 1, ctl, SITE_B_P)) { ok = false; break; }
           if (jj == 0 && tiles > 0 &&
               !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
           tc_fence_after();
-          issue_ts_128<C>(tmem + C::ACC0, tmem + C::S_COL, sK, jj > 0);    // dQ += dS K_j
-          tc_commit(smem_addr(&bar_st_empty[s]));
-          ++steps;
+          issue_ts_128<C>(tmem + C::Q_ACC, tmem + ((cur & 1) ? C::Q_S1 : C::Q_S0), stage_k(cur), jj > 0);   // dQ += dS K_j
+          tc_commit(smem_addr(&bar_st_empty[cur % C::STAGES]));
+          if (jj + 1 < nj) issue_dp(cur + 1);
         }
         if (!ok) break;
+        steps += nj;
         tc_commit(smem_addr(&bar_acc_full));
         tc_commit(smem_addr(&bar_q_empty));
         ++tiles;
@@ -454,62 +520,66 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else {
-    // elementwise: thread = query row r of the tile (TMEM lane)
-    const int r = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_base + C::S_COL, tP = tmem + lane_base + C::DP_COL;
+  } else if (warp < 8) {
+    // elementwise: thread = query row r of the tile (TMEM lane), warpgroup wg = key columns
+    // 64 wg .. 64 wg + 63
+    const int wg = warp >> 2;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t tiles = 0, steps = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
       int b, h, i, nj;
       decode(t, b, h, i, nj);
       const int qrow = i * 128 + r;
       const size_t vrow = ((size_t)b * p.H + h) * p.Np + qrow;   // padded rows: +inf / 0
       const float lse2 = __ldg(p.lse2 + vrow), dd = __ldg(p.dd + vrow);
       for (int jj = 0; jj < nj; ++jj) {
-        const bool w = mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
-        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-        tc_fence_after();
+        const uint32_t tS = tmem + lane_base + ((steps & 1) ? C::Q_S1 : C::Q_S0);
         const bool diag = C::CAUSAL && jj == i;
         const bool tail = jj == p.n_t - 1 && (p.N & 127) != 0;
         const int lim = diag ? r + 1 : (tail ? (p.N & 127) : 128);   // keys of this tile the row sees
-#pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t sv[32], dv[32];
-          tmem_ld_32cols(tS + c0, sv);
-          tmem_ld_32cols(tP + c0, dv);
-          tmem_ld_wait();
-          reg_fence32(sv);
-          reg_fence32(dv);
-          uint32_t dk[16];
+        bool w = ok && mbar_wait(smem_addr(&bar_s_full2[steps & 1]), (steps >> 1) & 1, ctl, SITE_B_S);
+        ok = __all_sync(0xffffffffu, w);
+        float pf[64];
+        if (ok) {
+          tc_fence_after();
+          tmem_ld_64cols(tS + wg * 64, pf);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float dsr[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              float pv = ex2(__uint_as_float(sv[c + e]) * p.scale_log2 - lse2);
-              if (c0 + c + e >= lim) pv = 0.0f;
-              dsr[e] = pv * (__uint_as_float(dv[c + e]) - dd);
-            }
-            dk[c >> 1] = pack_bf16x2(dsr[0], dsr[1]);
+          for (int c = 0; c < 64; ++c) {
+            const float pv = ex2(pf[c] * p.scale_log2 - lse2);
+            pf[c] = wg * 64 + c < lim ? pv : 0.0f;
           }
-          tmem_st_16cols(tS + (c0 >> 1), dk);   // dS over the S columns already read
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(smem_addr(&bar_p_ready));
+        w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
+        ok = __all_sync(0xffffffffu, w);
+        if (ok) {
+          float dp[64];
+          tc_fence_after();
+          tmem_ld_64cols(tmem + lane_base + C::Q_DP + wg * 64, dp);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pf[c] = pf[c] * (dp[c] - dd);
+        }
+        named_bar_sync(1, C::EW_THREADS);   // every S and dP column read before any dS write
+        if (ok) {
+          tmem_st_64_as_bf16(tS + wg * 32, pf);   // dS over this step's S buffer
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_addr(&bar_ds_ready));
+        }
         ++steps;
       }
-      if (!ok) break;
-      const bool w = mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
-      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-      tc_fence_after();
-      const bool valid = qrow < p.N;
-      const size_t orow = ((size_t)(b * p.N + (valid ? qrow : 0)) * p.H + h) * C::D;
-      store_acc_row<C::D>(tmem + lane_base + C::ACC0, p.scale, p.dq + orow, valid);
-      tc_fence_before();
-      mbar_arrive(smem_addr(&bar_acc_empty));
+      bool w = ok && mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
+      ok = __all_sync(0xffffffffu, w);
+      if (ok) {
+        tc_fence_after();
+        const bool valid = qrow < p.N;
+        const size_t orow = ((size_t)(b * p.N + (valid ? qrow : 0)) * p.H + h) * C::D;
+        store_acc_row(tmem + lane_base + C::Q_ACC, wg * (C::D / 2), (wg + 1) * (C::D / 2), p.scale, p.dq + orow,
+                      valid);
+        tc_fence_before();
+        mbar_arrive(smem_addr(&bar_acc_empty));
+      }
       ++tiles;
     }
   }
