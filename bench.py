@@ -166,11 +166,17 @@ def hbm_peak():
         return 6800.0, "fallback (6.8 TB/s, earlier GB300 measurement)"
 
 
+# Sources the forward kernel's device code is built from: a change to any of them voids the
+# committed DRAM-traffic figures (host-side files and other kernels do not).
+FWD_KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "ptx.cuh", "varlen.cuh", "launch_impl.cuh", "attn_fwd_bf16_d128.cu",
+                      "attn_fwd_bf16_d64.cu", "attn_fwd_bf16_d256.cu", "attn_fwd_fp8_d128.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode() + f.read())
+    for name in FWD_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
