@@ -90,9 +90,13 @@ bool pipeline_ready(DeviceInfo* di) {
   return di->pipe_ok;
 }
 
-// attn_fwd_host work split: chunks of whole batches (B >= 4) or, for B < 4, one batch and a
-// contiguous range of KV heads (with their query heads), so each chunk is a self-contained
-// attention problem whose copies can overlap another chunk's kernel. At most four chunks.
+// attn_fwd_host work split: chunks of whole batches (B >= kHostChunks) or, for fewer batches, one
+// batch and a contiguous range of KV heads (with their query heads), so each chunk is a
+// self-contained attention problem whose copies can overlap another chunk's kernel. The
+// host-device link (about 210 GB/s each way) bounds the call; smaller chunks shorten the
+// first upload and the last download that nothing overlaps.
+constexpr int kHostChunks = 8;
+static_assert(kHostChunks <= kMaxChunks, "chunk events");
 struct HostChunk {
   int b0, nb;      // batches [b0, b0 + nb)
   int g0, ng;      // kv heads [g0, g0 + ng); query heads [g0 G, (g0 + ng) G)
@@ -115,13 +119,13 @@ int plan_host_chunks(int B, int H, int Hkv, int N, int d, size_t elt, HostChunk*
     *total = off;
   };
   *total = 0;
-  if (B >= 4) {
-    for (int i = 0; i < 4; ++i) {
-      const int b0 = (int)((long long)B * i / 4), b1 = (int)((long long)B * (i + 1) / 4);
+  if (B >= kHostChunks) {
+    for (int i = 0; i < kHostChunks; ++i) {
+      const int b0 = (int)((long long)B * i / kHostChunks), b1 = (int)((long long)B * (i + 1) / kHostChunks);
       if (b1 > b0) add(b0, b1 - b0, 0, Hkv);
     }
   } else {
-    const int S = std::min(Hkv, (4 + B - 1) / B);
+    const int S = std::min(Hkv, std::max(1, kHostChunks / B));   // B * S <= kHostChunks
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < S; ++i) {
         const int g0 = (int)((long long)Hkv * i / S), g1 = (int)((long long)Hkv * (i + 1) / S);
