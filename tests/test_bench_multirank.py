@@ -52,3 +52,15 @@ def test_reference_arm_only_rank0_prints():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_other_families():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    for workload in ("varlen_causal_gqa_bf16_16seq_d128", "bwd_causal_gqa_bf16_n8192_d128",
+                     "fp8_block_hadamard_noncausal_n8192_d128", "decode_gqa_bf16_nq1_nk16384_d128"):
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                            "--warmup", "0", "--workload", workload], env=env, capture_output=True, text=True,
+                           timeout=600)
+        assert r.returncode == 0, r.stderr[-1000:]
+        line = json.loads(r.stdout.strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["value"] > 0 and line["config"]["workload"] == workload
