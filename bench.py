@@ -322,6 +322,8 @@ def run_ours(args, w, x):
     stream = torch.cuda.current_stream()
     decode = w.name in DECODE_NAMES
     if decode:
+        if w.splits == 0:   # the library's split heuristic (about one wave of SMs)
+            w = w.replace(splits=binding.attn_splitkv_num_splits(w.B, w.H, w.Hkv, w.N, w.n_keys, w.d))
         ws = torch.empty(binding.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.N, w.d, w.splits), dtype=torch.uint8,
                          device=dev)
 

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_workspace_bytes.argtypes = [i, i, i]
     L.attn_bwd.restype = i
     L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
+    L.attn_splitkv_num_splits.restype = i
+    L.attn_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -340,6 +342,11 @@ def quantize_e4m3(x, block_rows: int, signs=None, out=None, descale=None, stream
 
 def attn_quantize_e4m3_descale_count(B: int, N: int, Hx: int, block_rows: int) -> int:
     return int(lib().attn_quantize_e4m3_descale_count(B, N, Hx, block_rows))
+
+
+def attn_splitkv_num_splits(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:
+    """The library's split count for a decode shape on the current device (about one wave)."""
+    return int(lib().attn_splitkv_num_splits(B, H, Hkv, Nq, Nk, d))
 
 
 def attn_fwd_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, descale_q=None, descale_k=None,

@@ -454,6 +454,30 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   return (ok && joined && synced) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Nq < 1 || Nk < 1) return 1;
+  int sms = 152;
+  DeviceInfo* di = device_info();
+  if (di) sms = di->num_sms;
+  // Persistent CTAs run the (batch, kv head, query block, split) units in waves of `sms`. A
+  // split of T key tiles costs about T + 2 tiles of time (the extra: its Q load, partial-result
+  // write and share of the merge), so the time is about waves(S) * (ceil(n_kvt / S) + 2);
+  // take the S that minimises it (the smaller one on ties).
+  const long long units = (long long)B * Hkv * (((long long)Nq * (H / Hkv) + 127) / 128);
+  const long long n_kvt = (Nk + 127) / 128;
+  const long long s_max = std::min<long long>(n_kvt, kMaxSplits);
+  long long best_s = 1, best_cost = -1;
+  for (long long s = 1; s <= s_max; ++s) {
+    const long long waves = (units * s + sms - 1) / sms;
+    const long long cost = waves * ((n_kvt + s - 1) / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_s = s;
+    }
+  }
+  return (int)best_s;
+}
+
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
   return splitkv_part_o_bytes(B, H, Nq, d, num_splits) + round_up((size_t)num_splits * B * H * Nq * 4, 256);
@@ -498,7 +522,7 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
     return ATTN_ERR_CUDA;
   const int n_kvt = (Nk + 127) / 128;
   const int S = num_splits < n_kvt ? num_splits : n_kvt;   // every split gets at least one KV tile
-  const int rows = gb300::rows_per_work_tile(d);
+  const int rows = gb300::rows_per_split_work_tile(d);
   float* part_o = static_cast<float*>(workspace);
   float* part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + splitkv_part_o_bytes(B, H, Nq, d, num_splits));
   gb300::AttnParams& p = a.params;

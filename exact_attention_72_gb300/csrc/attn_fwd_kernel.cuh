@@ -81,7 +81,9 @@ struct AttnCfg {
   static_assert(!(SPLIT && CAUSAL), "split-KV mode has no causal mask");
   static_assert(!(SPLIT && VARLEN), "split-KV and varlen modes are separate");
   static constexpr int ELT = FP8 ? 1 : 2;                 // bytes per q/k/v element
-  static constexpr int NQ = (D <= 128) ? 2 : 1;           // 128-row Q tiles per CTA
+  // 128-row Q tiles per CTA. Split-KV (decode) units have few query rows, usually one tile, so
+  // they take the one-tile pipeline, whose S double buffer lets S_{j+1} run during softmax j.
+  static constexpr int NQ = (D <= 128 && !SPLIT_) ? 2 : 1;
   static constexpr int BM = 128, BN = 128;                // query rows per Q tile, keys per KV tile
   static constexpr int CE = 128 / ELT;                    // elements in one 128-byte swizzle row
   static constexpr int NCH = D / CE;                      // 128-byte column chunks per row

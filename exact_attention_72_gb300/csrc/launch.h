@@ -60,6 +60,8 @@ cudaError_t launch_quantize_e4m3(const QuantLaunch& q, cudaStream_t stream);
 
 // Rows of queries one CTA work tile covers for head dim d (two 128-row tiles for d <= 128).
 inline int rows_per_work_tile(int d) { return d <= 128 ? 256 : 128; }
+// Split-KV mode always runs one 128-row Q tile per CTA.
+inline int rows_per_split_work_tile(int) { return 128; }
 
 #define GB300_DECLARE_LAUNCH(D, CAUSAL, FP8) \
   extern template cudaError_t launch_attn_fwd<D, CAUSAL, FP8, false, false>(LaunchArgs&, cudaStream_t);

@@ -51,7 +51,7 @@ class Workload:
     k_outlier_frac: float = 0.0    # fraction of K entries replaced by +-k_outlier_mag
     k_outlier_mag: float = 8.0
     Nk: Optional[int] = None       # keys per sequence when it differs from N (decode shapes)
-    splits: int = 1                # split-KV ranges (decode shapes)
+    splits: int = 1                # split-KV ranges (decode shapes); 0: the library's choice
 
     @property
     def n_keys(self) -> int:
@@ -105,9 +105,9 @@ HEADLINE = "causal_gqa_bf16_n8192_d128"
 # Decode-shaped workloads for the split-KV path (few queries, long KV sequence, no mask).
 DECODE_WORKLOADS = {
     "decode_gqa_bf16_nq1_nk16384_d128": Workload("decode_gqa_bf16_nq1_nk16384_d128", B=8, H=32, Hkv=8, N=1,
-                                                 d=128, causal=False, seed=1101, Nk=16384, splits=16),
+                                                 d=128, causal=False, seed=1101, Nk=16384, splits=0),
     "decode_gqa_bf16_nq16_nk8192_d128": Workload("decode_gqa_bf16_nq16_nk8192_d128", B=4, H=32, Hkv=8, N=16,
-                                                 d=128, causal=False, seed=1102, Nk=8192, splits=8),
+                                                 d=128, causal=False, seed=1102, Nk=8192, splits=0),
 }
 
 

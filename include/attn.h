@@ -266,6 +266,15 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
 /* Device bytes attn_fwd_splitkv needs for its partial results (0 for invalid arguments). */
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 
+/*
+ * attn_splitkv_num_splits — a split count for attn_fwd_splitkv on the current device. Units
+ * (batch, kv head, query block, split) run in waves of SMs; a split of T key tiles costs about
+ * T + 2 tiles of time (Q load, partial-result write, merge), so the count minimises
+ * waves * (ceil(Nk / 128 / S) + 2) over 1 <= S <= min(ceil(Nk / 128), 128). Host-only; uses 152
+ * SMs when no device can be queried; returns 1 for invalid sizes.
+ */
+int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d);
+
 /* Size of the fixed device scratch used by attn_fwd_splitkv_static (16 MiB). */
 #define ATTN_SPLITKV_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
 

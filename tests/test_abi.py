@@ -169,3 +169,11 @@ def test_varlen_validation(lib):
     assert fwd(B=0) == INV and fwd(tq=-1) == INV and fwd(H=3, Hkv=2) == INV
     assert fwd(d=96) == UNS and fwd(scale=0.0) == UNS
     assert fwd(tq=0) == binding.ATTN_OK           # no query rows: nothing to do
+
+
+def test_split_heuristic_bounds(lib):
+    # clamped to [1, ceil(Nk / 128)] (152 SMs when no device can be queried)
+    for args in [(8, 32, 8, 1, 16384, 128), (4, 32, 8, 16, 8192, 128), (1, 1, 1, 1, 100, 64), (64, 64, 8, 1, 512, 128)]:
+        s = binding.attn_splitkv_num_splits(*args)
+        assert 1 <= s <= -(-args[4] // 128)
+    assert binding.attn_splitkv_num_splits(0, 1, 1, 1, 1, 128) == 1

@@ -22,7 +22,9 @@ def run_split(w, x, splits=None):
     kw = {}
     if desc is not None:
         kw = dict(descale_q=desc[0], descale_k=desc[1], descale_v=desc[2])
-    o, lse = binding.attn_fwd_splitkv(q, k, v, splits or w.splits, scale=w.scale, **kw)
+    # 0 splits: the library's heuristic (what the benchmark's decode workloads use)
+    s = splits or w.splits or binding.attn_splitkv_num_splits(w.B, w.H, w.Hkv, w.N, w.n_keys, w.d)
+    o, lse = binding.attn_fwd_splitkv(q, k, v, s, scale=w.scale, **kw)
     st, detail = binding.attn_get_status()
     assert st == binding.ATTN_OK, f"device status {st} detail {detail:#x}"
     return o, lse
