@@ -24,13 +24,13 @@
 // kernel that accumulates dQ across CTAs, traded for deterministic results and no fp32 atomic
 // traffic.
 //
-// Roles (320 threads): warps 0-7 elementwise, two warpgroups that split the 128 columns of a
-// tile (thread = TMEM lane = one row, warpgroup g = columns 64g .. 64g+63); warp 8 issues the
-// MMAs, warp 9 the TMA loads. The elementwise work of a step runs in two passes with their own
+// Roles (576 threads): warps 0-15 elementwise, four warpgroups that split the 128 columns of a
+// tile (thread = TMEM lane = one row, warpgroup g = columns 32g .. 32g+31); warp 16 issues the
+// MMAs, warp 17 the TMA loads. The elementwise work of a step runs in two passes with their own
 // barriers: P from S (the dV GEMM can start, while the dP GEMM may still run), then dS from dP.
-// bf16 results are written in place over the fp32 columns they came from, so both warpgroups
-// read their whole half first and meet at a named barrier before any write: packed column c/2
-// of one half lies in the fp32 columns of the other. Every wait is bounded (status word + abort
+// bf16 results are written in place over the fp32 columns they came from, so all warpgroups
+// read their columns first and meet at a named barrier before any write: packed column c/2 of
+// one group's columns lies in the fp32 columns of another. Every wait is bounded (status word + abort
 // flag); on a failed wait the elementwise warps keep stepping through the named barriers without
 // work, so no warp is left at a barrier.
 #pragma once
@@ -76,9 +76,12 @@ struct BwdCfg {
   // TMEM columns: S (or S^T, later P / dS in bf16) at 0, dP at 128, accumulators from 256
   static constexpr int S_COL = 0, DP_COL = 128, ACC0 = 256, ACC1 = 256 + D;
   static constexpr int TMEM_COLS = 512;
-  static constexpr int THREADS = 320;
-  static constexpr int EW_THREADS = 256;                  // elementwise warps 0-7
-  static constexpr int WARP_MMA = 8, WARP_LOAD = 9;
+  // Elementwise warpgroups: each takes CPG of the tile's 128 columns for all 128 rows (lanes).
+  static constexpr int EWG = 4;
+  static constexpr int CPG = 128 / EWG;
+  static constexpr int EW_THREADS = 128 * EWG;
+  static constexpr int WARP_MMA = 4 * EWG, WARP_LOAD = 4 * EWG + 1;
+  static constexpr int THREADS = (4 * EWG + 2) * 32;
   // dQ kernel: S double buffer at 0 and 128, dP at 256, dQ at 384
   static constexpr int Q_S0 = 0, Q_S1 = 128, Q_DP = 256, Q_ACC = 384;
   static_assert(ACC1 + D <= TMEM_COLS, "TMEM budget: head dim up to 128");
@@ -119,26 +122,25 @@ __device__ __forceinline__ void store_acc_row(uint32_t tcol, int c_begin, int c_
   }
 }
 
-// Loads 64 fp32 columns (two 32-column reads) of the lane's row into x.
-__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, float* x) {
-  uint32_t a[32], b[32];
-  tmem_ld_32cols(taddr, a);
-  tmem_ld_32cols(taddr + 32, b);
-  tmem_ld_wait();
-  reg_fence32(a);
-  reg_fence32(b);
+// Loads N (32 or 64) fp32 columns of the lane's row into x.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* x) {
+  uint32_t a[N];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    x[c] = __uint_as_float(a[c]);
-    x[32 + c] = __uint_as_float(b[c]);
-  }
+  for (int h = 0; h < N / 32; ++h) tmem_ld_32cols(taddr + 32 * h, a + 32 * h);
+  tmem_ld_wait();
+#pragma unroll
+  for (int h = 0; h < N / 32; ++h) reg_fence32(a + 32 * h);
+#pragma unroll
+  for (int c = 0; c < N; ++c) x[c] = __uint_as_float(a[c]);
 }
 
-// Packs 64 values as bf16 pairs and writes them as 32 columns at taddr.
-__device__ __forceinline__ void tmem_st_64_as_bf16(uint32_t taddr, const float* x) {
+// Packs N values as bf16 pairs and writes them as N / 2 columns at taddr.
+template <int N>
+__device__ __forceinline__ void tmem_st_as_bf16(uint32_t taddr, const float* x) {
   uint32_t pk[16];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
+  for (int h = 0; h < N / 32; ++h) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(x[32 * h + 2 * c], x[32 * h + 2 * c + 1]);
     tmem_st_16cols(taddr + 16 * h, pk);
@@ -292,9 +294,9 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else if (warp < 8) {
+  } else if (warp < C::WARP_MMA) {
     // elementwise: thread = key row r of the tile (TMEM lane), warpgroup wg = query columns
-    // 64 wg .. 64 wg + 63
+    // CPG wg .. CPG wg + CPG - 1
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -314,22 +316,22 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         bool w = ok && mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
         w = w && mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST);
         ok = __all_sync(0xffffffffu, w);
-        const float* lse2 = vec + s * 256 + wg * 64;
-        const float* dd = vec + s * 256 + 128 + wg * 64;
+        const float* lse2 = vec + s * 256 + wg * C::CPG;
+        const float* dd = vec + s * 256 + 128 + wg * C::CPG;
         const bool diag = C::CAUSAL && i == j;
-        float pf[64];
+        float pf[C::CPG];
         if (ok) {
           tc_fence_after();
-          tmem_ld_64cols(tS + wg * 64, pf);
+          tmem_ld_cols<C::CPG>(tS + wg * C::CPG, pf);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < C::CPG; ++c) {
             const float pv = ex2(pf[c] * p.scale_log2 - lse2[c]);
-            pf[c] = (diag && wg * 64 + c < r) ? 0.0f : pv;   // key after the query
+            pf[c] = (diag && wg * C::CPG + c < r) ? 0.0f : pv;   // key after the query
           }
         }
         named_bar_sync(1, C::EW_THREADS);   // every S^T column read before any P^T write
         if (ok) {
-          tmem_st_64_as_bf16(tS + wg * 32, pf);
+          tmem_st_as_bf16<C::CPG>(tS + wg * (C::CPG / 2), pf);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(smem_addr(&bar_p_ready));
@@ -338,30 +340,33 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
         ok = __all_sync(0xffffffffu, w);
         if (ok) {
-          float dp[64];
+          float dp[C::CPG];
           tc_fence_after();
-          tmem_ld_64cols(tP + wg * 64, dp);
+          tmem_ld_cols<C::CPG>(tP + wg * C::CPG, dp);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pf[c] = pf[c] * (dp[c] - dd[c]);
+          for (int c = 0; c < C::CPG; ++c) pf[c] = pf[c] * (dp[c] - dd[c]);
         }
         named_bar_sync(2, C::EW_THREADS);   // every dP^T column read before any dS^T write
         if (ok) {
-          tmem_st_64_as_bf16(tP + wg * 32, pf);
+          tmem_st_as_bf16<C::CPG>(tP + wg * (C::CPG / 2), pf);
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(smem_addr(&bar_ds_ready));
         }
         ++steps;
       }
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 dK
+      // epilogue: the first half of the warpgroups write dV, the second half dK, each a range of
+      // the D columns
       bool w = ok && mbar_wait(smem_addr(&bar_acc_full), tiles & 1, ctl, SITE_B_ACC);
       ok = __all_sync(0xffffffffu, w);
       if (ok) {
         tc_fence_after();
         const bool valid = key < p.N;
         const size_t orow = ((size_t)(b * p.N + (valid ? key : 0)) * p.Hkv + kvh) * C::D;
-        if (wg == 0) store_acc_row(tmem + lane_base + C::ACC0, 0, C::D, 1.0f, p.dv + orow, valid);
-        else store_acc_row(tmem + lane_base + C::ACC1, 0, C::D, p.scale, p.dk + orow, valid);
+        constexpr int HALF = C::EWG / 2, W = C::D / HALF;
+        const int part = wg % HALF;
+        if (wg < HALF) store_acc_row(tmem + lane_base + C::ACC0, part * W, (part + 1) * W, 1.0f, p.dv + orow, valid);
+        else store_acc_row(tmem + lane_base + C::ACC1, part * W, (part + 1) * W, p.scale, p.dk + orow, valid);
         tc_fence_before();
         mbar_arrive(smem_addr(&bar_acc_empty));
       }
@@ -520,9 +525,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else if (warp < 8) {
+  } else if (warp < C::WARP_MMA) {
     // elementwise: thread = query row r of the tile (TMEM lane), warpgroup wg = key columns
-    // 64 wg .. 64 wg + 63
+    // CPG wg .. CPG wg + CPG - 1
     const int wg = warp >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -541,28 +546,28 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int lim = diag ? r + 1 : (tail ? (p.N & 127) : 128);   // keys of this tile the row sees
         bool w = ok && mbar_wait(smem_addr(&bar_s_full2[steps & 1]), (steps >> 1) & 1, ctl, SITE_B_S);
         ok = __all_sync(0xffffffffu, w);
-        float pf[64];
+        float pf[C::CPG];
         if (ok) {
           tc_fence_after();
-          tmem_ld_64cols(tS + wg * 64, pf);
+          tmem_ld_cols<C::CPG>(tS + wg * C::CPG, pf);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < C::CPG; ++c) {
             const float pv = ex2(pf[c] * p.scale_log2 - lse2);
-            pf[c] = wg * 64 + c < lim ? pv : 0.0f;
+            pf[c] = wg * C::CPG + c < lim ? pv : 0.0f;
           }
         }
         w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
         ok = __all_sync(0xffffffffu, w);
         if (ok) {
-          float dp[64];
+          float dp[C::CPG];
           tc_fence_after();
-          tmem_ld_64cols(tmem + lane_base + C::Q_DP + wg * 64, dp);
+          tmem_ld_cols<C::CPG>(tmem + lane_base + C::Q_DP + wg * C::CPG, dp);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) pf[c] = pf[c] * (dp[c] - dd);
+          for (int c = 0; c < C::CPG; ++c) pf[c] = pf[c] * (dp[c] - dd);
         }
         named_bar_sync(1, C::EW_THREADS);   // every S and dP column read before any dS write
         if (ok) {
-          tmem_st_64_as_bf16(tS + wg * 32, pf);   // dS over this step's S buffer
+          tmem_st_as_bf16<C::CPG>(tS + wg * (C::CPG / 2), pf);   // dS over this step's S buffer
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(smem_addr(&bar_ds_ready));
@@ -575,8 +580,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc_fence_after();
         const bool valid = qrow < p.N;
         const size_t orow = ((size_t)(b * p.N + (valid ? qrow : 0)) * p.H + h) * C::D;
-        store_acc_row(tmem + lane_base + C::Q_ACC, wg * (C::D / 2), (wg + 1) * (C::D / 2), p.scale, p.dq + orow,
-                      valid);
+        constexpr int NG = (C::D / 32 < C::EWG) ? C::D / 32 : C::EWG;   // 32-column pieces per group
+        if (wg < NG)
+          store_acc_row(tmem + lane_base + C::Q_ACC, wg * (C::D / NG), (wg + 1) * (C::D / NG), p.scale, p.dq + orow,
+                        valid);
         tc_fence_before();
         mbar_arrive(smem_addr(&bar_acc_empty));
       }

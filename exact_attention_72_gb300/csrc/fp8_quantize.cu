@@ -44,8 +44,8 @@ struct QCfg {
   static constexpr int WARPS = THREADS / 32;
   static constexpr int EPL = D / 4;                  // values per lane: a quarter of a row
   static constexpr int NP = EPL / 2;                 // packed fp32 pairs per lane
-  static constexpr int HALF_BYTES = kChunkRows * 128;   // one 64-column slab of a stage
-  static constexpr int STAGE_BYTES = (D / 64) * HALF_BYTES;
+  static constexpr int SLAB_BYTES = kChunkRows * 128;   // one 64-column slab of a stage (128 rows)
+  static constexpr int STAGE_BYTES = (D / 64) * SLAB_BYTES;
   static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 2);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 };
@@ -61,7 +61,7 @@ __device__ __forceinline__ void load_quarter_row(const uint8_t* stage, int r, in
   for (int p = 0; p < EPL / 8; ++p) {
     const int off = q * (EPL * 2) + p * 16;      // byte offset of the piece within the row
     const int slab = off >> 7, c = (off & 127) >> 4;
-    const uint4 t = *reinterpret_cast<const uint4*>(stage + slab * QCfg<D>::HALF_BYTES + r * 128 + ((c ^ (r & 7)) << 4));
+    const uint4 t = *reinterpret_cast<const uint4*>(stage + slab * QCfg<D>::SLAB_BYTES + r * 128 + ((c ^ (r & 7)) << 4));
     w[4 * p] = t.x;
     w[4 * p + 1] = t.y;
     w[4 * p + 2] = t.z;
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS) quantize_kernel(const __grid
     mbar_arrive_expect_tx(bar, chunk_bytes);
 #pragma unroll
     for (int s = 0; s < D / 64; ++s)
-      tma_load_4d(smem_addr(smem + stage * C::STAGE_BYTES + s * C::HALF_BYTES), &tm, bar, 64 * s, cp.row_begin, cp.h,
+      tma_load_4d(smem_addr(smem + stage * C::STAGE_BYTES + s * C::SLAB_BYTES), &tm, bar, 64 * s, cp.row_begin, cp.h,
                   cp.b);
   };
   if (tid == 0)
