@@ -44,7 +44,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-constexpr int kMaxChunks = 8;
+constexpr int kMaxChunks = 10;   // eight even chunks, the first and last of them halved
 
 struct DeviceInfo {
   std::once_flag once;
@@ -96,7 +96,7 @@ bool pipeline_ready(DeviceInfo* di) {
 // host-device link (about 210 GB/s each way) bounds the call; smaller chunks shorten the
 // first upload and the last download that nothing overlaps.
 constexpr int kHostChunks = 8;
-static_assert(kHostChunks <= kMaxChunks, "chunk events");
+static_assert(kHostChunks + 2 <= kMaxChunks, "chunk events");
 struct HostChunk {
   int b0, nb;      // batches [b0, b0 + nb)
   int g0, ng;      // kv heads [g0, g0 + ng); query heads [g0 G, (g0 + ng) G)
@@ -119,18 +119,47 @@ int plan_host_chunks(int B, int H, int Hkv, int N, int d, size_t elt, HostChunk*
     *total = off;
   };
   *total = 0;
+  struct Spec {
+    int b0, nb, g0, ng;
+  };
+  Spec spec[kMaxChunks];
+  int ns = 0;
   if (B >= kHostChunks) {
     for (int i = 0; i < kHostChunks; ++i) {
       const int b0 = (int)((long long)B * i / kHostChunks), b1 = (int)((long long)B * (i + 1) / kHostChunks);
-      if (b1 > b0) add(b0, b1 - b0, 0, Hkv);
+      if (b1 > b0) spec[ns++] = {b0, b1 - b0, 0, Hkv};
     }
   } else {
     const int S = std::min(Hkv, std::max(1, kHostChunks / B));   // B * S <= kHostChunks
     for (int b = 0; b < B; ++b)
       for (int i = 0; i < S; ++i) {
         const int g0 = (int)((long long)Hkv * i / S), g1 = (int)((long long)Hkv * (i + 1) / S);
-        if (g1 > g0) add(b, 1, g0, g1 - g0);
+        if (g1 > g0) spec[ns++] = {b, 1, g0, g1 - g0};
       }
+  }
+  // The first chunk's upload and the last chunk's kernel and download overlap nothing: halve
+  // those two chunks (by batches, else by kv heads) when they can be halved.
+  auto halves = [&](const Spec& x, Spec& lo, Spec& hi) -> bool {
+    if (x.nb >= 2) {
+      lo = {x.b0, x.nb / 2, x.g0, x.ng};
+      hi = {x.b0 + x.nb / 2, x.nb - x.nb / 2, x.g0, x.ng};
+      return true;
+    }
+    if (x.ng >= 2) {
+      lo = {x.b0, x.nb, x.g0, x.ng / 2};
+      hi = {x.b0, x.nb, x.g0 + x.ng / 2, x.ng - x.ng / 2};
+      return true;
+    }
+    return false;
+  };
+  for (int i = 0; i < ns; ++i) {
+    Spec lo, hi;
+    if ((i == 0 || i == ns - 1) && ns > 1 && halves(spec[i], lo, hi)) {
+      add(lo.b0, lo.nb, lo.g0, lo.ng);
+      add(hi.b0, hi.nb, hi.g0, hi.ng);
+    } else {
+      add(spec[i].b0, spec[i].nb, spec[i].g0, spec[i].ng);
+    }
   }
   *total += 256;   // fp8 descales
   return nc;
