@@ -80,6 +80,7 @@ struct BwdCfg {
   static constexpr int EWG = 4;
   static constexpr int CPG = 128 / EWG;
   static constexpr int EW_THREADS = 128 * EWG;
+  static constexpr int EW_WARPS = 4 * EWG;                 // arrivals on the elementwise barriers
   static constexpr int WARP_MMA = 4 * EWG, WARP_LOAD = 4 * EWG + 1;
   static constexpr int THREADS = (4 * EWG + 2) * 32;
   // dQ kernel: S double buffer at 0 and 128, dP at 256, dQ at 384
@@ -88,6 +89,13 @@ struct BwdCfg {
   static_assert(Q_ACC + D <= TMEM_COLS, "TMEM budget (dQ kernel)");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+
+// One arrival per warp: every lane has finished what precedes the call (its own tcgen05 waits and
+// fences included) before lane 0 arrives. The barrier counts warps, not threads.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 
 enum : uint32_t { SITE_B_KV = 21, SITE_B_ST = 22, SITE_B_S = 23, SITE_B_P = 24, SITE_B_ACC = 25, SITE_B_EMPTY = 26 };
 
@@ -178,10 +186,10 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     mbar_init(smem_addr(&bar_s_full), 1);
     mbar_init(smem_addr(&bar_dp_full), 1);
-    mbar_init(smem_addr(&bar_p_ready), C::EW_THREADS);
-    mbar_init(smem_addr(&bar_ds_ready), C::EW_THREADS);
+    mbar_init(smem_addr(&bar_p_ready), C::EW_WARPS);
+    mbar_init(smem_addr(&bar_ds_ready), C::EW_WARPS);
     mbar_init(smem_addr(&bar_acc_full), 1);
-    mbar_init(smem_addr(&bar_acc_empty), C::EW_THREADS);
+    mbar_init(smem_addr(&bar_acc_empty), C::EW_WARPS);
     mbar_init(smem_addr(&bar_drain), 1);
     fence_mbar_init();
   }
@@ -264,28 +272,41 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         int b, kvh, j, i0;
         decode(t, b, kvh, j, i0);
         if (!mbar_wait(smem_addr(&bar_kv_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
+        // Issue order per step k: dV_k, S^T_{k+1}, dK_k, dP^T_{k+1}. S^T_{k+1} overwrites P^T_k and
+        // dP^T_{k+1} overwrites dS^T_k, each after the GEMM that reads them (the MMAs of one thread
+        // run in issue order), so the next step's S^T runs while the elementwise warps form dS^T_k.
         const int n = p.G * (p.n_t - i0);
-        for (int k = 0; k < n; ++k) {
-          const int s = steps % C::STAGES;
-          const uint32_t sQ = sStage + s * 2 * C::TILE_BYTES, sdO = sQ + C::TILE_BYTES;
-          if (!mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST)) { ok = false; break; }
+        auto stage_q = [&](uint32_t st) { return sStage + (st % C::STAGES) * 2 * C::TILE_BYTES; };
+        auto issue_st = [&](uint32_t st) -> bool {
+          if (!mbar_wait(smem_addr(&bar_st_full[st % C::STAGES]), (st / C::STAGES) & 1, ctl, SITE_B_ST)) return false;
           tc_fence_after();
-          issue_qk<C>(tmem + C::S_COL, sK, sQ);     // S^T = K_j Q_i^T
+          issue_qk<C>(tmem + C::S_COL, sK, stage_q(st));     // S^T = K_j Q_i^T
           tc_commit(smem_addr(&bar_s_full));
-          issue_qk<C>(tmem + C::DP_COL, sV, sdO);   // dP^T = V_j dO_i^T
+          return true;
+        };
+        auto issue_dpt = [&](uint32_t st) {
+          issue_qk<C>(tmem + C::DP_COL, sV, stage_q(st) + C::TILE_BYTES);   // dP^T = V_j dO_i^T
           tc_commit(smem_addr(&bar_dp_full));
-          if (!mbar_wait(smem_addr(&bar_p_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+        };
+        if (!issue_st(steps)) { ok = false; break; }
+        issue_dpt(steps);
+        for (int k = 0; k < n; ++k) {
+          const uint32_t cur = steps + k;
+          const uint32_t sQ = stage_q(cur), sdO = sQ + C::TILE_BYTES;
+          if (!mbar_wait(smem_addr(&bar_p_ready), cur & 1, ctl, SITE_B_P)) { ok = false; break; }
           if (k == 0 && tiles > 0 &&
               !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
           tc_fence_after();
           issue_ts_128<C>(tmem + C::ACC0, tmem + C::S_COL, sdO, k > 0);    // dV += P^T dO_i
-          if (!mbar_wait(smem_addr(&bar_ds_ready), steps & 1, ctl, SITE_B_P)) { ok = false; break; }
+          if (k + 1 < n && !issue_st(cur + 1)) { ok = false; break; }
+          if (!mbar_wait(smem_addr(&bar_ds_ready), cur & 1, ctl, SITE_B_P)) { ok = false; break; }
           tc_fence_after();
           issue_ts_128<C>(tmem + C::ACC1, tmem + C::DP_COL, sQ, k > 0);    // dK += dS^T Q_i
-          tc_commit(smem_addr(&bar_st_empty[s]));
-          ++steps;
+          tc_commit(smem_addr(&bar_st_empty[cur % C::STAGES]));
+          if (k + 1 < n) issue_dpt(cur + 1);
         }
         if (!ok) break;
+        steps += n;
         tc_commit(smem_addr(&bar_acc_full));
         tc_commit(smem_addr(&bar_kv_empty));
         ++tiles;
@@ -334,7 +355,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tmem_st_as_bf16<C::CPG>(tS + wg * (C::CPG / 2), pf);
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(smem_addr(&bar_p_ready));
+          warp_arrive(smem_addr(&bar_p_ready));
         }
         // pass 2: dS^T = P^T * (dP^T - D)
         w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
@@ -351,7 +372,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tmem_st_as_bf16<C::CPG>(tP + wg * (C::CPG / 2), pf);
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(smem_addr(&bar_ds_ready));
+          warp_arrive(smem_addr(&bar_ds_ready));
         }
         ++steps;
       }
@@ -368,7 +389,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (wg < HALF) store_acc_row(tmem + lane_base + C::ACC0, part * W, (part + 1) * W, 1.0f, p.dv + orow, valid);
         else store_acc_row(tmem + lane_base + C::ACC1, part * W, (part + 1) * W, p.scale, p.dk + orow, valid);
         tc_fence_before();
-        mbar_arrive(smem_addr(&bar_acc_empty));
+        warp_arrive(smem_addr(&bar_acc_empty));
       }
       ++tiles;
     }
@@ -410,9 +431,9 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     mbar_init(smem_addr(&bar_s_full2[0]), 1);
     mbar_init(smem_addr(&bar_s_full2[1]), 1);
     mbar_init(smem_addr(&bar_dp_full), 1);
-    mbar_init(smem_addr(&bar_ds_ready), C::EW_THREADS);
+    mbar_init(smem_addr(&bar_ds_ready), C::EW_WARPS);
     mbar_init(smem_addr(&bar_acc_full), 1);
-    mbar_init(smem_addr(&bar_acc_empty), C::EW_THREADS);
+    mbar_init(smem_addr(&bar_acc_empty), C::EW_WARPS);
     mbar_init(smem_addr(&bar_drain), 1);
     fence_mbar_init();
   }
@@ -570,7 +591,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tmem_st_as_bf16<C::CPG>(tS + wg * (C::CPG / 2), pf);   // dS over this step's S buffer
           tmem_st_wait();
           tc_fence_before();
-          mbar_arrive(smem_addr(&bar_ds_ready));
+          warp_arrive(smem_addr(&bar_ds_ready));
         }
         ++steps;
       }
@@ -585,7 +606,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           store_acc_row(tmem + lane_base + C::Q_ACC, wg * (C::D / NG), (wg + 1) * (C::D / NG), p.scale, p.dq + orow,
                         valid);
         tc_fence_before();
-        mbar_arrive(smem_addr(&bar_acc_empty));
+        warp_arrive(smem_addr(&bar_acc_empty));
       }
       ++tiles;
     }
