@@ -726,14 +726,14 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   a.o = o;
   a.dout = dout;
   a.lse = lse;
-  a.lse2 = static_cast<float*>(workspace);
+  a.nlse2 = static_cast<float*>(workspace);
   a.dd = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up((size_t)B * H * np * 4, 256));
   a.num_sms = di->num_sms;
   gb300::BwdParams& p = a.params;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.lse2 = a.lse2;
+  p.nlse2 = a.nlse2;
   p.dd = a.dd;
   p.B = B;
   p.H = H;

@@ -1,4 +1,4 @@
-// Launchers of the backward pass: preprocess (D, LSE2), then dK/dV, then dQ, all on one stream.
+// Launchers of the backward pass: preprocess (D, -LSE log2 e), then dK/dV, then dQ, all on one stream.
 #include <algorithm>
 
 #include "launch.h"
@@ -22,7 +22,7 @@ cudaError_t launch_bwd(BwdLaunchArgs& a, cudaStream_t s) {
   const BwdParams& p = a.params;
   const long long rows = (long long)p.B * p.H * p.Np;
   attn_bwd_preprocess_kernel<D><<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.lse2, a.dd, p.B,
+      static_cast<const __nv_bfloat16*>(a.o), static_cast<const __nv_bfloat16*>(a.dout), a.lse, a.nlse2, a.dd, p.B,
       p.H, p.N, p.Np);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -42,7 +42,7 @@ struct BwdParams {
   __nv_bfloat16* dq;     // [B, N, H, D]
   __nv_bfloat16* dk;     // [B, N, Hkv, D]
   __nv_bfloat16* dv;     // [B, N, Hkv, D]
-  const float* lse2;     // [B, H, Np]: LSE * log2(e); rows from N to Np: +inf
+  const float* nlse2;    // [B, H, Np]: -LSE * log2(e); rows from N to Np: -inf
   const float* dd;       // [B, H, Np]: rowsum(dO * O); rows from N to Np: 0
   int B, H, Hkv, G, N, Np;   // Np: N rounded up to a multiple of 128
   int n_t;                   // 128-row tiles per sequence (queries and keys alike)
@@ -68,7 +68,7 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_QK = make_idesc(kFmtBF16, 128, 128, false, false);
   static constexpr uint32_t IDESC_PV = make_idesc(kFmtBF16, 128, D, false, true);
   static constexpr int STAGES = 2;
-  static constexpr int VEC_BYTES = 2 * 128 * 4;           // per stage: LSE2 and D of 128 query rows
+  static constexpr int VEC_BYTES = 2 * 128 * 4;           // per stage: -LSE2 and D of 128 query rows
   // shared memory: two resident tiles, then STAGES x (two streamed tiles), then the vectors
   static constexpr int SMEM_USED = 2 * TILE_BYTES + STAGES * 2 * TILE_BYTES + STAGES * VEC_BYTES + 1024;
   // At least 116 KB so that one CTA holds an SM: each takes all 512 TMEM columns.
@@ -246,7 +246,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_load_4d(dst + C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_do, bar, ch * C::CE, i * 128, h, b);
           }
           const size_t row = ((size_t)b * p.H + h) * p.Np + (size_t)i * 128;
-          bulk_load(smem_addr(vec + s * 256), p.lse2 + row, 512, bar);
+          bulk_load(smem_addr(vec + s * 256), p.nlse2 + row, 512, bar);
           bulk_load(smem_addr(vec + s * 256 + 128), p.dd + row, 512, bar);
           ++steps;
         }
@@ -337,17 +337,30 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         bool w = ok && mbar_wait(smem_addr(&bar_s_full), steps & 1, ctl, SITE_B_S);
         w = w && mbar_wait(smem_addr(&bar_st_full[s]), (steps / C::STAGES) & 1, ctl, SITE_B_ST);
         ok = __all_sync(0xffffffffu, w);
-        const float* lse2 = vec + s * 256 + wg * C::CPG;
-        const float* dd = vec + s * 256 + 128 + wg * C::CPG;
+        // this group's query columns of -LSE2 and D, as float4 (broadcast reads)
+        const float4* nl4 = reinterpret_cast<const float4*>(vec + s * 256 + wg * C::CPG);
+        const float4* dd4 = reinterpret_cast<const float4*>(vec + s * 256 + 128 + wg * C::CPG);
         const bool diag = C::CAUSAL && i == j;
         float pf[C::CPG];
         if (ok) {
           tc_fence_after();
           tmem_ld_cols<C::CPG>(tS + wg * C::CPG, pf);
+          const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int c = 0; c < C::CPG; ++c) {
-            const float pv = ex2(pf[c] * p.scale_log2 - lse2[c]);
-            pf[c] = (diag && wg * C::CPG + c < r) ? 0.0f : pv;   // key after the query
+          for (int c = 0; c < C::CPG; c += 4) {
+            const float4 nl = nl4[c >> 2];
+            float t0, t1, t2, t3;
+            f2_unpack(f2_fma(f2_pack(pf[c], pf[c + 1]), sl2, f2_pack(nl.x, nl.y)), t0, t1);
+            f2_unpack(f2_fma(f2_pack(pf[c + 2], pf[c + 3]), sl2, f2_pack(nl.z, nl.w)), t2, t3);
+            pf[c] = ex2(t0);
+            pf[c + 1] = ex2(t1);
+            pf[c + 2] = ex2(t2);
+            pf[c + 3] = ex2(t3);
+          }
+          if (diag) {
+#pragma unroll
+            for (int c = 0; c < C::CPG; ++c)
+              if (wg * C::CPG + c < r) pf[c] = 0.0f;   // key after the query
           }
         }
         named_bar_sync(1, C::EW_THREADS);   // every S^T column read before any P^T write
@@ -365,7 +378,13 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tc_fence_after();
           tmem_ld_cols<C::CPG>(tP + wg * C::CPG, dp);
 #pragma unroll
-          for (int c = 0; c < C::CPG; ++c) pf[c] = pf[c] * (dp[c] - dd[c]);
+          for (int c = 0; c < C::CPG; c += 4) {
+            const float4 d4 = dd4[c >> 2];
+            f2_unpack(f2_mul(f2_pack(pf[c], pf[c + 1]), f2_sub(f2_pack(dp[c], dp[c + 1]), f2_pack(d4.x, d4.y))), pf[c],
+                      pf[c + 1]);
+            f2_unpack(f2_mul(f2_pack(pf[c + 2], pf[c + 3]), f2_sub(f2_pack(dp[c + 2], dp[c + 3]), f2_pack(d4.z, d4.w))),
+                      pf[c + 2], pf[c + 3]);
+          }
         }
         named_bar_sync(2, C::EW_THREADS);   // every dP^T column read before any dS^T write
         if (ok) {
@@ -559,7 +578,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       decode(t, b, h, i, nj);
       const int qrow = i * 128 + r;
       const size_t vrow = ((size_t)b * p.H + h) * p.Np + qrow;   // padded rows: +inf / 0
-      const float lse2 = __ldg(p.lse2 + vrow), dd = __ldg(p.dd + vrow);
+      const float nlse2 = __ldg(p.nlse2 + vrow), dd = __ldg(p.dd + vrow);
+      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2), nl2 = f2_pack(nlse2, nlse2), dd2 = f2_pack(dd, dd);
       for (int jj = 0; jj < nj; ++jj) {
         const uint32_t tS = tmem + lane_base + ((steps & 1) ? C::Q_S1 : C::Q_S0);
         const bool diag = C::CAUSAL && jj == i;
@@ -572,9 +592,11 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_after();
           tmem_ld_cols<C::CPG>(tS + wg * C::CPG, pf);
 #pragma unroll
-          for (int c = 0; c < C::CPG; ++c) {
-            const float pv = ex2(pf[c] * p.scale_log2 - lse2);
-            pf[c] = wg * C::CPG + c < lim ? pv : 0.0f;
+          for (int c = 0; c < C::CPG; c += 2) {
+            float t0, t1;
+            f2_unpack(f2_fma(f2_pack(pf[c], pf[c + 1]), sl2, nl2), t0, t1);
+            pf[c] = wg * C::CPG + c < lim ? ex2(t0) : 0.0f;
+            pf[c + 1] = wg * C::CPG + c + 1 < lim ? ex2(t1) : 0.0f;
           }
         }
         w = ok && mbar_wait(smem_addr(&bar_dp_full), steps & 1, ctl, SITE_B_S);
@@ -584,7 +606,8 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_after();
           tmem_ld_cols<C::CPG>(tmem + lane_base + C::Q_DP + wg * C::CPG, dp);
 #pragma unroll
-          for (int c = 0; c < C::CPG; ++c) pf[c] = pf[c] * (dp[c] - dd);
+          for (int c = 0; c < C::CPG; c += 2)
+            f2_unpack(f2_mul(f2_pack(pf[c], pf[c + 1]), f2_sub(f2_pack(dp[c], dp[c + 1]), dd2)), pf[c], pf[c + 1]);
         }
         named_bar_sync(1, C::EW_THREADS);   // every S and dP column read before any dS write
         if (ok) {
@@ -618,10 +641,10 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// D = rowsum(dO * O) and LSE * log2(e), per (b, h, row), rows padded to Np (D = 0, LSE2 = +inf).
+// D = rowsum(dO * O) and -LSE * log2(e), per (b, h, row), rows padded to Np (D = 0, -LSE2 = -inf).
 template <int D>
 __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const __nv_bfloat16* o, const __nv_bfloat16* dout,
-                                                                 const float* lse, float* lse2, float* dd, int B,
+                                                                 const float* lse, float* nlse2, float* dd, int B,
                                                                  int H, int N, int Np) {
   const long long w = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // one warp per row
   const int lane = threadIdx.x & 31;
@@ -643,7 +666,7 @@ __global__ void __launch_bounds__(256) attn_bwd_preprocess_kernel(const __nv_bfl
   for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
   if (lane == 0) {
     dd[w] = acc;
-    lse2[w] = row < N ? lse[bh * N + row] * 1.4426950408889634f : INFINITY;
+    nlse2[w] = row < N ? lse[bh * N + row] * -1.4426950408889634f : -INFINITY;
   }
 }
 

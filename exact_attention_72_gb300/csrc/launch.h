@@ -25,7 +25,7 @@ struct BwdLaunchArgs {
   const void* o;             // bf16 [B, N, H, D]
   const void* dout;          // bf16 [B, N, H, D]
   const float* lse;          // [B, H, N]
-  float* lse2;               // workspace [B, H, Np]
+  float* nlse2;              // workspace [B, H, Np]
   float* dd;                 // workspace [B, H, Np]
   int num_sms;
 };
