@@ -38,7 +38,7 @@ constexpr float kE4M3Max = 448.0f;
 constexpr int kChunkRows = 128;          // most rows of one chunk (one smem stage)
 constexpr uint32_t kSiteQuantFull = 11;  // wait site recorded in the status word on a timeout
 
-template <int D>
+template <int D, bool ROT>
 struct QCfg {
   static constexpr int THREADS = 512;                // 16 warps x 8 rows = 128 rows
   static constexpr int WARPS = THREADS / 32;
@@ -46,7 +46,9 @@ struct QCfg {
   static constexpr int NP = EPL / 2;                 // packed fp32 pairs per lane
   static constexpr int SLAB_BYTES = kChunkRows * 128;   // one 64-column slab of a stage (128 rows)
   static constexpr int STAGE_BYTES = (D / 64) * SLAB_BYTES;
-  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? 3 : 2);
+  // Loads in flight per CTA. The rotated d = 128 kernel holds one CTA per SM (registers), so it
+  // takes a deep ring; the others fit two CTAs per SM with the shallower one.
+  static constexpr int STAGES = D == 64 ? 4 : (D == 128 ? (ROT ? 6 : 3) : 3);
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 };
 
@@ -61,7 +63,7 @@ __device__ __forceinline__ void load_quarter_row(const uint8_t* stage, int r, in
   for (int p = 0; p < EPL / 8; ++p) {
     const int off = q * (EPL * 2) + p * 16;      // byte offset of the piece within the row
     const int slab = off >> 7, c = (off & 127) >> 4;
-    const uint4 t = *reinterpret_cast<const uint4*>(stage + slab * QCfg<D>::SLAB_BYTES + r * 128 + ((c ^ (r & 7)) << 4));
+    const uint4 t = *reinterpret_cast<const uint4*>(stage + slab * (kChunkRows * 128) + r * 128 + ((c ^ (r & 7)) << 4));
     w[4 * p] = t.x;
     w[4 * p + 1] = t.y;
     w[4 * p + 2] = t.z;
@@ -201,14 +203,14 @@ __device__ __forceinline__ ChunkPos chunk_pos(int c, const gb300::QuantLaunch& a
 // descale slot with an atomic max. MODE 2: codes of the chunk from the block maximum in the slot.
 // ROT: rows are rotated by diag(signs) H_D first.
 template <int D, int MODE, bool ROT>
-__global__ void __launch_bounds__(QCfg<D>::THREADS) quantize_kernel(const __grid_constant__ CUtensorMap tm,
+__global__ void __launch_bounds__(QCfg<D, ROT>::THREADS) quantize_kernel(const __grid_constant__ CUtensorMap tm,
                                                                    const gb300::QuantLaunch a, int n_chunks) {
-  using C = QCfg<D>;
+  using C = QCfg<D, ROT>;
   using namespace gb300;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[C::STAGES];
-  __shared__ float red[C::WARPS];
+  __shared__ float red[2][C::WARPS];   // per-warp maxima, alternating between chunks
   __shared__ uint32_t abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int r = 8 * warp + (lane & 7);   // row of the chunk this lane works on
@@ -282,10 +284,18 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS) quantize_kernel(const __grid
       float amax = valid ? pairs_amax<C::NP>(v) : 0.0f;
 #pragma unroll
       for (int m = 16; m > 0; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-      if (lane == 0) red[warp] = amax;
+      float* rk = red[k & 1];
+      if (lane == 0) rk[warp] = amax;
       __syncthreads();
-      amax = red[gw0];
-      for (int i = gw0 + 1; i < gw1; ++i) amax = fmaxf(amax, red[i]);
+      // Every warp has read the stage: refill it while the codes are formed. (The next chunk
+      // writes the other half of red; the one after waits at that chunk's barrier for every
+      // warp, so no warp still reads this half then.)
+      if (tid == 0) {
+        const int next = c + C::STAGES * gridDim.x;
+        if (next < n_chunks) issue(next, stage);
+      }
+      amax = rk[gw0];
+      for (int i = gw0 + 1; i < gw1; ++i) amax = fmaxf(amax, rk[i]);
       const bool writer = lane == 0 && warp == gw0 && grp_valid;
       if constexpr (MODE == 1) {
         // non-negative floats order like their bit patterns
@@ -296,10 +306,12 @@ __global__ void __launch_bounds__(QCfg<D>::THREADS) quantize_kernel(const __grid
         if (writer) *ds_slot = stored_descale<D>(ds, ROT);
       }
     }
-    __syncthreads();   // the stage (and red) are read: refill the stage
-    if (tid == 0) {
-      const int next = c + C::STAGES * gridDim.x;
-      if (next < n_chunks) issue(next, stage);
+    if constexpr (MODE == 2) {
+      __syncthreads();   // the stage is read: refill it
+      if (tid == 0) {
+        const int next = c + C::STAGES * gridDim.x;
+        if (next < n_chunks) issue(next, stage);
+      }
     }
   }
   if (!ok && tid == 0) {
@@ -324,7 +336,7 @@ __global__ void finalize_descale_kernel(float* descale, int n, bool rotated) {
 
 template <int D, int MODE, bool ROT>
 cudaError_t launch_mode(const gb300::QuantLaunch& q, int n_chunks, cudaStream_t s) {
-  using C = QCfg<D>;
+  using C = QCfg<D, ROT>;
   auto kern = quantize_kernel<D, MODE, ROT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;

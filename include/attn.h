@@ -219,10 +219,11 @@ size_t attn_quantize_e4m3_descale_count(int B, int N, int Hx, int block_rows);
  * descales, given here as HOST pointers to one float each) to device buffers owned by the
  * caller (`workspace`, at least attn_fwd_host_workspace_bytes(...) bytes of device memory,
  * 256-byte aligned), runs the forward, and copies o and lse back to host memory.
- * The work is split into up to four chunks (whole batches when B >= 4, otherwise one batch and a
- * range of KV heads with their query heads); the upload of one chunk, the kernel of another and
- * the download of a third run concurrently on internal streams (created once per device, never
- * on later calls; the call allocates no memory). The call starts after the work already queued
+ * The work is split into up to eight chunks (whole batches when B >= 8, otherwise one batch and a
+ * range of KV heads with their query heads), and the first and last chunks are halved when they
+ * can be (up to ten in all): their copies overlap no kernel. The upload of one chunk, the kernel
+ * of another and the download of a third run concurrently on internal streams (created once per
+ * device, never on later calls; the call allocates no memory). The call starts after the work already queued
  * on `stream` and returns after synchronizing `stream`, with o and lse in host memory. Host
  * buffers may be pageable or pinned; only pinned buffers let the copies overlap. Calls on the
  * same device are serialized. Returns as attn_fwd, plus ATTN_ERR_INVALID_ARG for a too-small or
