@@ -5,7 +5,8 @@ One step = one attn_fwd call over the whole workload (B=2, H=32, Hkv=8, N=8192, 
 bf16 by default). Prints ONE JSON line on rank 0:
   value      device-timed TFLOP/s (4*B*H*N^2*d, halved for causal), summed over ranks, with
              inputs resident in HBM; CUDA events around each launch on the launching stream,
-             L2 flushed (256 MiB write) before every step outside the events;
+             L2 flushed (256 MiB write, then a 256 MiB read that drains the dirty lines) before
+             every step, outside the events;
   e2e        the same metric through attn_fwd_host (pinned host buffers, H2D of q/k/v and D2H
              of o/lse inside the timed region);
   roofline   tensor-core bound: achieved TFLOP/s of the attention kernel against the measured
@@ -36,6 +37,21 @@ METRIC = "attn fwd TFLOP/s (bf16, causal, N=8192, d=128) and % of GB300 dense pe
 FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 DECODE_NAMES = {"decode_gqa_bf16_nq1_nk16384_d128", "decode_gqa_bf16_nq16_nk8192_d128"}
+
+
+class L2Flush:
+    """Evicts the step's inputs from L2 before a timed step: writes a buffer larger than L2, then
+    reads a second one. The read makes the write's dirty lines drain to DRAM here, outside the
+    timed events, instead of during the next step's kernel."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xFF)
+        self.r.max()
 
 
 def parse_args(argv=None):
@@ -296,7 +312,7 @@ def config_of(w):
                                  "random Hadamard rotation, v one descale per head"}
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "N": w.N, "d": w.d, "causal": w.causal, **extra,
             "qkv_dtype": w.dtype, "k_outliers": w.k_outlier_frac,
-            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "l2": "flushed before every step (256 MiB write, then a 256 MiB read that drains its dirty lines; outside the timed events)",
             "parallelism": "replicas (one full workload per GPU)"}
 
 
@@ -318,7 +334,7 @@ def run_ours(args, w, x):
               for n, s in (("descale_q", x.descale_q), ("descale_k", x.descale_k), ("descale_v", x.descale_v))}
     o = torch.empty((w.B, w.N, w.H, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     decode = w.name in DECODE_NAMES
     if decode:
@@ -350,7 +366,7 @@ def run_ours(args, w, x):
             binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, **kw)
 
     for i in range(max(args.warmup, 0)):
-        flush.fill_(i & 0xFF)
+        flush(i)
         step()
     torch.cuda.synchronize()
     st, detail = binding.attn_get_status()
@@ -365,7 +381,7 @@ def run_ours(args, w, x):
     torch.cuda.synchronize()
     t_host0 = time.time()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         starts[i].record(stream)
         step(i)
         ends[i].record(stream)
@@ -598,7 +614,7 @@ def run_bwd_ours(args, w, x):
     o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(binding.attn_bwd_workspace_bytes(w.B, w.H, w.N), dtype=torch.uint8, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     flops = BWD_FLOP_FACTOR * w.flops
 
@@ -606,7 +622,7 @@ def run_bwd_ours(args, w, x):
         binding.attn_bwd(q, k, v, o, lse, do, w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
 
     for i in range(max(args.warmup, 0)):
-        flush.fill_(i & 0xFF)
+        flush(i)
         step()
     torch.cuda.synchronize()
     st, detail = binding.attn_get_status()
@@ -620,7 +636,7 @@ def run_bwd_ours(args, w, x):
     torch.cuda.synchronize()
     t_host0 = time.time()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -697,7 +713,7 @@ def varlen_config(w):
     return {"workload": w.name, "B": w.B, "H": w.H, "Hkv": w.Hkv, "d": w.d, "causal": w.causal,
             "lengths_q": list(w.lengths_q), "lengths_k": list(w.lk), "total_q": w.total_q, "qkv_dtype": w.dtype,
             "plan": "attn_varlen_plan built once before timing and reused by every step",
-            "l2": "flushed before every step (256 MiB write, outside the timed events)",
+            "l2": "flushed before every step (256 MiB write, then a 256 MiB read that drains its dirty lines; outside the timed events)",
             "parallelism": "replicas (one full workload per GPU)"}
 
 
@@ -779,7 +795,7 @@ def run_varlen_ours(args, w, x):
     cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device=dev)
     o = torch.empty((w.total_q, w.H, w.d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.H, w.total_q), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
     # the plan: built once, like a serving loop reusing it across layers; its build time is reported
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -791,7 +807,7 @@ def run_varlen_ours(args, w, x):
         binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, plan, w.causal, scale=w.scale, out=o, lse=lse, **kw)
 
     for i in range(max(args.warmup, 0)):
-        flush.fill_(i & 0xFF)
+        flush(i)
         step()
     torch.cuda.synchronize()
     plan_ms = p0.elapsed_time(p1)
@@ -806,7 +822,7 @@ def run_varlen_ours(args, w, x):
     torch.cuda.synchronize()
     t_host0 = time.time()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush(i)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
