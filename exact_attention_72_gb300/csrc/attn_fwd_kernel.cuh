@@ -329,6 +329,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // Split mode: the combine kernel is launched as a programmatic dependent; let its CTAs be
+  // scheduled now (they wait for this grid to finish before reading anything).
+  if constexpr (C::SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
   const uint32_t sKV = smem_base + C::Q_BYTES;

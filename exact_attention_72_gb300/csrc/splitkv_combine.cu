@@ -4,7 +4,10 @@
 // a direct consequence of the softmax definition (the "combine math" of split-KV decoding named in
 // the "Hopper" tag page (l1-ca0.github.io), section 10.2.1 title).
 // One warp per output row; each lane owns D/32 consecutive columns. Memory-bound: every partial
-// row is read once and O is written once in bf16.
+// row is read once and O is written once in bf16. The kernel is launched as a programmatic
+// dependent of the split kernel: its CTAs may be scheduled while the split kernel runs and wait
+// (griddepcontrol.wait) until that grid has finished and its writes are visible, so the launch
+// latency of this short kernel overlaps the split kernel's tail.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -18,6 +21,7 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
                                                               __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                                                               int S, int B, int H, int Nq) {
   constexpr int PER = D / 32;   // columns per lane
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long rows = (long long)B * H * Nq;   // row = (b H + h) Nq + n, the layout of lse
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
@@ -60,13 +64,22 @@ cudaError_t launch_splitkv_combine(const float* part_o, const float* part_lse, v
   const long long cap = 8LL * num_sms;
   if (blocks > cap) blocks = cap;
   auto* ob = static_cast<__nv_bfloat16*>(o);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   switch (D) {
-    case 64: splitkv_combine_kernel<64><<<(int)blocks, 256, 0, stream>>>(part_o, part_lse, ob, lse, S, B, H, Nq); break;
-    case 128: splitkv_combine_kernel<128><<<(int)blocks, 256, 0, stream>>>(part_o, part_lse, ob, lse, S, B, H, Nq); break;
-    case 256: splitkv_combine_kernel<256><<<(int)blocks, 256, 0, stream>>>(part_o, part_lse, ob, lse, S, B, H, Nq); break;
+    case 64: return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<64>, part_o, part_lse, ob, lse, S, B, H, Nq);
+    case 128: return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<128>, part_o, part_lse, ob, lse, S, B, H, Nq);
+    case 256: return cudaLaunchKernelEx(&cfg, splitkv_combine_kernel<256>, part_o, part_lse, ob, lse, S, B, H, Nq);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace gb300
