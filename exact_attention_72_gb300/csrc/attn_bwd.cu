@@ -31,7 +31,7 @@ cudaError_t launch_bwd(BwdLaunchArgs& a, cudaStream_t s) {
   if ((e = launch_persistent(attn_bwd_dkdv_kernel<C>, C::SMEM_BYTES, C::THREADS, a, p1, s)) != cudaSuccess) return e;
   BwdParams p2 = p;
   p2.n_tiles = p.n_t * p.B * p.H;
-  return launch_persistent(attn_bwd_dq_kernel<C>, C::SMEM_BYTES, C::THREADS, a, p2, s);
+  return launch_persistent(attn_bwd_dq_kernel<C>, C::DQ_SMEM_BYTES, C::THREADS, a, p2, s);
 }
 
 }  // namespace

@@ -83,11 +83,16 @@ struct BwdCfg {
   static constexpr int EW_WARPS = 4 * EWG;                 // arrivals on the elementwise barriers
   static constexpr int WARP_MMA = 4 * EWG, WARP_LOAD = 4 * EWG + 1;
   static constexpr int THREADS = (4 * EWG + 2) * 32;
+  // dQ kernel shared memory: Q and dO, then a K ring and a V ring of their own
+  static constexpr int DQ_KS = 3, DQ_VS = 2;
+  static constexpr int DQ_SMEM_USED = 2 * TILE_BYTES + (DQ_KS + DQ_VS) * TILE_BYTES + 1024;
+  static constexpr int DQ_SMEM_BYTES = DQ_SMEM_USED > 118784 ? DQ_SMEM_USED : 118784;
   // dQ kernel: S double buffer at 0 and 128, dP at 256, dQ at 384
   static constexpr int Q_S0 = 0, Q_S1 = 128, Q_DP = 256, Q_ACC = 384;
   static_assert(ACC1 + D <= TMEM_COLS, "TMEM budget: head dim up to 128");
   static_assert(Q_ACC + D <= TMEM_COLS, "TMEM budget (dQ kernel)");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(DQ_SMEM_BYTES <= 232448 - 1024, "shared memory budget (dQ kernel; 1 KB static)");
 };
 
 // One arrival per warp: every lane has finished what precedes the call (its own tcgen05 waits and
@@ -430,22 +435,29 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                    const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_st_full[C::STAGES], bar_st_empty[C::STAGES];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_k_full[C::DQ_KS], bar_k_empty[C::DQ_KS];
+  __shared__ __align__(8) uint64_t bar_v_full[C::DQ_VS], bar_v_empty[C::DQ_VS];
   __shared__ __align__(8) uint64_t bar_s_full2[2], bar_dp_full, bar_ds_ready, bar_acc_full, bar_acc_empty, bar_drain;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_addr(smem), sdO = sQ + C::TILE_BYTES;
-  const uint32_t sStage = sdO + C::TILE_BYTES;                         // stage s: K at +0, V at +TILE
+  // K and V have rings of their own: K_j is read by S_j and, a step later, by dQ_j; V_j only by
+  // dP_j. A third K stage lets K_{j+2} load while dQ_j still reads K_j.
+  const uint32_t sK = sdO + C::TILE_BYTES, sV = sK + C::DQ_KS * C::TILE_BYTES;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
   if (tid == 0) {
     abort_flag = 0u;
     mbar_init(smem_addr(&bar_q_full), 1);
     mbar_init(smem_addr(&bar_q_empty), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_addr(&bar_st_full[s]), 1);
-      mbar_init(smem_addr(&bar_st_empty[s]), 1);
+    for (int s = 0; s < C::DQ_KS; ++s) {
+      mbar_init(smem_addr(&bar_k_full[s]), 1);
+      mbar_init(smem_addr(&bar_k_empty[s]), 1);
+    }
+    for (int s = 0; s < C::DQ_VS; ++s) {
+      mbar_init(smem_addr(&bar_v_full[s]), 1);
+      mbar_init(smem_addr(&bar_v_empty[s]), 1);
     }
     mbar_init(smem_addr(&bar_s_full2[0]), 1);
     mbar_init(smem_addr(&bar_s_full2[1]), 1);
@@ -479,7 +491,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      uint32_t tiles = 0, steps = 0;
+      uint32_t tiles = 0, kq = 0, vq = 0;   // work tiles, K loads and V loads issued
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
         int b, h, i, nj;
@@ -493,26 +505,39 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
         ++tiles;
         for (int jj = 0; ok && jj < nj; ++jj) {
-          const int s = steps % C::STAGES;
-          if (steps >= (uint32_t)C::STAGES &&
-              !mbar_wait(smem_addr(&bar_st_empty[s]), ((steps / C::STAGES) - 1) & 1, ctl, SITE_B_EMPTY)) {
+          const int ks = kq % C::DQ_KS, vs = vq % C::DQ_VS;
+          if (kq >= (uint32_t)C::DQ_KS &&
+              !mbar_wait(smem_addr(&bar_k_empty[ks]), ((kq / C::DQ_KS) - 1) & 1, ctl, SITE_B_EMPTY)) {
             ok = false;
             break;
           }
-          const uint32_t bar = smem_addr(&bar_st_full[s]);
-          const uint32_t dst = sStage + s * 2 * C::TILE_BYTES;
-          mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES);
-          for (int ch = 0; ch < C::NCH; ++ch) {
-            tma_load_4d(dst + ch * C::CHUNK_BYTES, &tm_k, bar, ch * C::CE, jj * 128, kvh, b);
-            tma_load_4d(dst + C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v, bar, ch * C::CE, jj * 128, kvh, b);
+          mbar_arrive_expect_tx(smem_addr(&bar_k_full[ks]), C::TILE_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_4d(sK + ks * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_k, smem_addr(&bar_k_full[ks]), ch * C::CE,
+                        jj * 128, kvh, b);
+          ++kq;
+          if (vq >= (uint32_t)C::DQ_VS &&
+              !mbar_wait(smem_addr(&bar_v_empty[vs]), ((vq / C::DQ_VS) - 1) & 1, ctl, SITE_B_EMPTY)) {
+            ok = false;
+            break;
           }
-          ++steps;
+          mbar_arrive_expect_tx(smem_addr(&bar_v_full[vs]), C::TILE_BYTES);
+          for (int ch = 0; ch < C::NCH; ++ch)
+            tma_load_4d(sV + vs * C::TILE_BYTES + ch * C::CHUNK_BYTES, &tm_v, smem_addr(&bar_v_full[vs]), ch * C::CE,
+                        jj * 128, kvh, b);
+          ++vq;
         }
       }
       if (!ok) {
-        for (uint32_t q = steps > (uint32_t)C::STAGES ? steps - C::STAGES : 0u; q < steps; ++q) {
+        // let copies still in flight land before the CTA exits
+        for (uint32_t q = kq > (uint32_t)C::DQ_KS ? kq - C::DQ_KS : 0u; q < kq; ++q) {
           const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(smem_addr(&bar_st_full[q % C::STAGES]), (q / C::STAGES) & 1) &&
+          while (!mbar_try_wait(smem_addr(&bar_k_full[q % C::DQ_KS]), (q / C::DQ_KS) & 1) &&
+                 global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+        for (uint32_t q = vq > (uint32_t)C::DQ_VS ? vq - C::DQ_VS : 0u; q < vq; ++q) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_v_full[q % C::DQ_VS]), (q / C::DQ_VS) & 1) &&
                  global_timer_ns() - t0 < p.timeout_ns) {}
         }
         if (tiles > 0) {
@@ -523,42 +548,51 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
   } else if (warp == C::WARP_MMA) {
     if (lane == 0) {
-      // S_j goes to buffer j % 2 (global step parity); S_{j+1} is issued before step j's dQ GEMM
+      // Per step j: S_{j+1} into the other S buffer, then (once dS_j is in TMEM) dP_{j+1}, then
+      // dQ_j. dP_{j+1} overwrites dP_j, which the elementwise warps read before writing dS_j; it
+      // runs ahead of dQ_j so the next elementwise pass finds it done.
       uint32_t tiles = 0, steps = 0;
       bool ok = true;
-      auto stage_k = [&](uint32_t st) { return sStage + (st % C::STAGES) * 2 * C::TILE_BYTES; };
       auto issue_s = [&](uint32_t st) -> bool {
-        if (!mbar_wait(smem_addr(&bar_st_full[st % C::STAGES]), (st / C::STAGES) & 1, ctl, SITE_B_ST)) return false;
+        if (!mbar_wait(smem_addr(&bar_k_full[st % C::DQ_KS]), (st / C::DQ_KS) & 1, ctl, SITE_B_ST)) return false;
         tc_fence_after();
-        issue_qk<C>(tmem + ((st & 1) ? C::Q_S1 : C::Q_S0), sQ, stage_k(st));   // S = Q_i K_j^T
+        issue_qk<C>(tmem + ((st & 1) ? C::Q_S1 : C::Q_S0), sQ, sK + (st % C::DQ_KS) * C::TILE_BYTES);   // S = Q_i K_j^T
         tc_commit(smem_addr(&bar_s_full2[st & 1]));
         return true;
       };
-      auto issue_dp = [&](uint32_t st) {
-        issue_qk<C>(tmem + C::Q_DP, sdO, stage_k(st) + C::TILE_BYTES);           // dP = dO_i V_j^T
+      auto issue_dp = [&](uint32_t st) -> bool {
+        if (!mbar_wait(smem_addr(&bar_v_full[st % C::DQ_VS]), (st / C::DQ_VS) & 1, ctl, SITE_B_ST)) return false;
+        tc_fence_after();
+        issue_qk<C>(tmem + C::Q_DP, sdO, sV + (st % C::DQ_VS) * C::TILE_BYTES);           // dP = dO_i V_j^T
         tc_commit(smem_addr(&bar_dp_full));
+        tc_commit(smem_addr(&bar_v_empty[st % C::DQ_VS]));
+        return true;
       };
       for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
         int b, h, i, nj;
         decode(t, b, h, i, nj);
         if (!mbar_wait(smem_addr(&bar_q_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
-        if (!issue_s(steps)) { ok = false; break; }
-        issue_dp(steps);
+        if (!issue_s(steps) || !issue_dp(steps)) { ok = false; break; }
+        // Q and dO are read by the S and dP GEMMs only: free them after the tile's last dP.
+        if (nj == 1) tc_commit(smem_addr(&bar_q_empty));
         for (int jj = 0; jj < nj; ++jj) {
           const uint32_t cur = steps + jj;
           if (jj + 1 < nj && !issue_s(cur + 1)) { ok = false; break; }
           if (!mbar_wait(smem_addr(&bar_ds_ready), cur & 1, ctl, SITE_B_P)) { ok = false; break; }
+          if (jj + 1 < nj) {
+            if (!issue_dp(cur + 1)) { ok = false; break; }
+            if (jj + 2 == nj) tc_commit(smem_addr(&bar_q_empty));
+          }
           if (jj == 0 && tiles > 0 &&
               !mbar_wait(smem_addr(&bar_acc_empty), (tiles - 1) & 1, ctl, SITE_B_ACC)) { ok = false; break; }
           tc_fence_after();
-          issue_ts_128<C>(tmem + C::Q_ACC, tmem + ((cur & 1) ? C::Q_S1 : C::Q_S0), stage_k(cur), jj > 0);   // dQ += dS K_j
-          tc_commit(smem_addr(&bar_st_empty[cur % C::STAGES]));
-          if (jj + 1 < nj) issue_dp(cur + 1);
+          issue_ts_128<C>(tmem + C::Q_ACC, tmem + ((cur & 1) ? C::Q_S1 : C::Q_S0),
+                          sK + (cur % C::DQ_KS) * C::TILE_BYTES, jj > 0);   // dQ += dS K_j
+          tc_commit(smem_addr(&bar_k_empty[cur % C::DQ_KS]));
         }
         if (!ok) break;
         steps += nj;
         tc_commit(smem_addr(&bar_acc_full));
-        tc_commit(smem_addr(&bar_q_empty));
         ++tiles;
       }
       tc_commit(smem_addr(&bar_drain));
