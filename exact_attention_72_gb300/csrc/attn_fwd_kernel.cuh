@@ -113,7 +113,11 @@ struct AttnCfg {
   // registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The host checks the
   // compiled register count before launching (an over-subscribed increase would never return).
   static constexpr bool REG_SPLIT = (NQ == 2);
-  static constexpr int THREADS = REG_SPLIT ? 384 : (SOFTMAX_WARPS + MMA_WARPS + 1) * 32;
+  // With a two-stage ring (d = 256: 64 KB tiles) K_j always takes stage 0 and V_j stage 1. Then
+  // K and V get a producer warp each (WARP_LOAD: Q and K, WARP_LOAD + 1: V), so the next K can
+  // load as soon as S has read the last one, without queueing behind V's wait for PV.
+  static constexpr bool TWO_LOADERS = (NS == 2);
+  static constexpr int THREADS = REG_SPLIT ? 384 : (SOFTMAX_WARPS + MMA_WARPS + 1 + (TWO_LOADERS ? 1 : 0)) * 32;
   static constexpr uint32_t REGS_SOFTMAX = 200, REGS_OTHER = 96;
   static constexpr int REGS_NEEDED = SOFTMAX_WARPS * 32 * REGS_SOFTMAX + 128 * REGS_OTHER;
   static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
@@ -379,7 +383,76 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if (!good && tid == 0 && blockIdx.x == 0) atomicCAS(p.status, 0u, kStatusBadPlan);
   }
 
-  if (warp == C::WARP_LOAD) {
+  if (C::TWO_LOADERS && (warp == C::WARP_LOAD || warp == C::WARP_LOAD + 1)) {
+    // ------------------------------------------------------------------ TMA producers, K and V
+    if (lane == 0) {
+      const bool is_v = warp == C::WARP_LOAD + 1;   // stage 1: V tiles; stage 0: Q and K tiles
+      const uint32_t slot = is_v ? 1u : 0u;
+      if (!is_v) tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(is_v ? &tm_v : &tm_k);
+      uint32_t cnt = 0;       // K (or V) tiles issued so far
+      uint32_t nq_loads = 0;  // Q loads issued so far (K warp)
+      bool ok = true;
+      int iter = 0;
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++iter) {
+        const TileCoord tc = decode_tile<C>(t, p);
+        const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
+        int nmax = 0, nq_valid = 0;
+        for (int qt = 0; qt < C::NQ; ++qt) {
+          const int n = kv_tiles_for<C>(tc, qt, p);
+          nmax = n > nmax ? n : nmax;
+          nq_valid += (n > 0);
+        }
+        if (C::VARLEN && nmax == 0) continue;   // every row sees no key: the softmax warps write it
+        if (!is_v) {
+          // Q: wait until the previous work tile's last S = Q K^T has completed.
+          if (nq_loads > 0 && !mbar_wait(smem_addr(&bar_q_empty), (nq_loads - 1) & 1, ctl, SITE_Q_EMPTY)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(smem_addr(&bar_q_full), nq_valid * C::TILE_BYTES);
+          for (int qt = 0; qt < C::NQ; ++qt) {
+            const int pos0 = q_tile_pos0<C>(tc, qt, p);
+            if (kv_tiles_for<C>(tc, qt, p) == 0) continue;
+            for (int ch = 0; ch < C::NCH; ++ch) {
+              const uint32_t dst = sQ + (qt * C::NCH + ch) * C::CHUNK_BYTES;
+              if (C::SPLIT)
+                tma_load_5d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, 0, pos0, tc.h, tc.b);
+              else
+                tma_load_4d(dst, &tm_q, smem_addr(&bar_q_full), ch * C::CE, tc.q_base + pos0, tc.h, tc.bo);
+            }
+          }
+          ++nq_loads;
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+          // load number cnt of this stage waits for the release of load cnt - 1
+          if (cnt > 0 && !mbar_wait(smem_addr(&bar_kv_empty[slot]), (cnt - 1) & 1, ctl, SITE_KV_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const bool skip = p.debug_skip_load && blockIdx.x == 0 && iter == 0 && j == 0 && is_v;
+          if (!skip) {
+            mbar_arrive_expect_tx(smem_addr(&bar_kv_full[slot]), C::TILE_BYTES);
+            for (int ch = 0; ch < C::NCH; ++ch)
+              tma_load_4d(sKV + slot * C::TILE_BYTES + ch * C::CHUNK_BYTES, is_v ? &tm_v : &tm_k,
+                          smem_addr(&bar_kv_full[slot]), ch * C::CE, tc.k_base + (tc.j0 + j) * C::BN, kvh, tc.bo);
+          }
+          ++cnt;
+        }
+      }
+      if (!ok) {
+        // Unwinding: let the copy still in flight land before the CTA exits.
+        if (cnt > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_kv_full[slot]), (cnt - 1) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+        if (nq_loads > 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(smem_addr(&bar_q_full), (nq_loads - 1) & 1) && global_timer_ns() - t0 < p.timeout_ns) {}
+        }
+      }
+    }
+  } else if (warp == C::WARP_LOAD) {
     // ------------------------------------------------------------------ TMA producer
     if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
