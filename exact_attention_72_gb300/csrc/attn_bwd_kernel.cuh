@@ -224,7 +224,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
       tma_prefetch_desc(&tm_do);
       uint32_t tiles = 0, steps = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL>(0); ok && t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
         int b, kvh, j, i0;
         decode(t, b, kvh, j, i0);
         if (tiles > 0 && !mbar_wait(smem_addr(&bar_kv_empty), (tiles - 1) & 1, ctl, SITE_B_EMPTY)) { ok = false; break; }
@@ -273,7 +273,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (lane == 0) {
       uint32_t tiles = 0, steps = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL>(0); ok && t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
         int b, kvh, j, i0;
         decode(t, b, kvh, j, i0);
         if (!mbar_wait(smem_addr(&bar_kv_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
@@ -329,7 +329,7 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t tS = tmem + lane_base + C::S_COL, tP = tmem + lane_base + C::DP_COL;
     uint32_t tiles = 0, steps = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    for (int turn = 0, t = deal_tile<C::CAUSAL>(0); t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
       int b, kvh, j, i0;
       decode(t, b, kvh, j, i0);
       const int key = j * 128 + r;
@@ -493,7 +493,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tma_prefetch_desc(&tm_do);
       uint32_t tiles = 0, kq = 0, vq = 0;   // work tiles, K loads and V loads issued
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL>(0); ok && t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
         int b, h, i, nj;
         decode(t, b, h, i, nj);
         const int kvh = h / p.G;
@@ -568,7 +568,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tc_commit(smem_addr(&bar_v_empty[st % C::DQ_VS]));
         return true;
       };
-      for (int t = blockIdx.x; ok && t < p.n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL>(0); ok && t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
         int b, h, i, nj;
         decode(t, b, h, i, nj);
         if (!mbar_wait(smem_addr(&bar_q_full), tiles & 1, ctl, SITE_B_KV)) { ok = false; break; }
@@ -607,7 +607,7 @@ attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     uint32_t tiles = 0, steps = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x) {
+    for (int turn = 0, t = deal_tile<C::CAUSAL>(0); t < p.n_tiles; t = deal_tile<C::CAUSAL>(++turn)) {
       int b, h, i, nj;
       decode(t, b, h, i, nj);
       const int qrow = i * 128 + r;

@@ -248,6 +248,17 @@ __device__ unsigned long long g_attn_trace[2 * 32 * 1024];
   } while (0)
 #endif
 
+// Work tile of a CTA's turn-th turn: turn k deals tiles k G .. k G + G - 1 to the G persistent
+// CTAs. With ZIGZAG (tiles sorted longest first: causal masks, varlen plans) the deal runs forward
+// on even turns and backward on odd ones, so the CTA that took the longest tile of one turn takes
+// the shortest of the next. Plain round-robin gives CTA 0 the longest tile of every turn. Tiles of
+// equal cost keep the plain deal. Once a CTA's tile is past the end, so are all its later ones.
+template <bool ZIGZAG>
+__device__ __forceinline__ int deal_tile(int turn) {
+  const int g = (int)gridDim.x, c = (int)blockIdx.x;
+  return turn * g + ((ZIGZAG && (turn & 1)) ? g - 1 - c : c);
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -394,7 +405,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t nq_loads = 0;  // Q loads issued so far (K warp)
       bool ok = true;
       int iter = 0;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++iter) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn), ++iter) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
@@ -463,7 +474,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t nq_loads = 0;  // Q loads issued so far
       bool ok = true;
       int iter = 0;
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++iter) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn), ++iter) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
@@ -556,7 +567,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
         return true;
       };
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int n = kv_tiles_for<C>(tc, myq, p);
         int nmax = 0;
@@ -642,7 +653,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++p_cnt[buf];
         return true;
       };
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int nmax = kv_tiles_for<C>(tc, 0, p);
         if (nmax == 0) continue;
@@ -697,7 +708,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+    for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
       const TileCoord tc = decode_tile<C>(t, p);
       const int n = kv_tiles_for<C>(tc, qt, p);
       const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
