@@ -488,23 +488,15 @@ int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {
   int sms = 152;
   DeviceInfo* di = device_info();
   if (di) sms = di->num_sms;
-  // Persistent CTAs run the (batch, kv head, query block, split) units in waves of `sms`. A
-  // split of T key tiles costs about T + 2 tiles of time (the extra: its Q load, partial-result
-  // write and share of the merge), so the time is about waves(S) * (ceil(n_kvt / S) + 2);
-  // take the S that minimises it (the smaller one on ties).
+  // The (batch, kv head, query block) units stream K and V at close to the HBM bandwidth once
+  // about two thirds of the SMs or more take part. So split each unit as far as one wave of SMs
+  // allows and no further: a second, partial wave, or more units per CTA, only adds Q loads,
+  // partial-result writes and merge work.
   const long long units = (long long)B * Hkv * (((long long)Nq * (H / Hkv) + 127) / 128);
   const long long n_kvt = (Nk + 127) / 128;
   const long long s_max = std::min<long long>(n_kvt, kMaxSplits);
-  long long best_s = 1, best_cost = -1;
-  for (long long s = 1; s <= s_max; ++s) {
-    const long long waves = (units * s + sms - 1) / sms;
-    const long long cost = waves * ((n_kvt + s - 1) / s + 2);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_s = s;
-    }
-  }
-  return (int)best_s;
+  const long long s = sms / units;
+  return (int)std::max<long long>(1, std::min<long long>(s, s_max));
 }
 
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {

@@ -268,11 +268,11 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 
 /*
- * attn_splitkv_num_splits — a split count for attn_fwd_splitkv on the current device. Units
- * (batch, kv head, query block, split) run in waves of SMs; a split of T key tiles costs about
- * T + 2 tiles of time (Q load, partial-result write, merge), so the count minimises
- * waves * (ceil(Nk / 128 / S) + 2) over 1 <= S <= min(ceil(Nk / 128), 128). Host-only; uses 152
- * SMs when no device can be queried; returns 1 for invalid sizes.
+ * attn_splitkv_num_splits — a split count for attn_fwd_splitkv on the current device: the
+ * largest S with U * S <= #SMs, where U = B * Hkv * ceil(Nq * H / Hkv / 128) units, clamped to
+ * 1 <= S <= min(ceil(Nk / 128), 128). One wave of split units streams K and V near the HBM
+ * bandwidth; more splits only add partial results to merge. Host-only; uses 152 SMs when no
+ * device can be queried; returns 1 for invalid sizes.
  */
 int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d);
 

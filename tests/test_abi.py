@@ -177,3 +177,9 @@ def test_split_heuristic_bounds(lib):
         s = binding.attn_splitkv_num_splits(*args)
         assert 1 <= s <= -(-args[4] // 128)
     assert binding.attn_splitkv_num_splits(0, 1, 1, 1, 1, 128) == 1
+    # one wave on 152 SMs: 64 units (B8 x Hkv8, one query block each) -> 2 splits; 32 units -> 4;
+    # more units than SMs -> no split; a single unit -> one split per key tile, up to 128
+    assert binding.attn_splitkv_num_splits(8, 32, 8, 1, 16384, 128) == 2
+    assert binding.attn_splitkv_num_splits(4, 32, 8, 16, 8192, 128) == 4
+    assert binding.attn_splitkv_num_splits(64, 64, 8, 1, 512, 128) == 1
+    assert binding.attn_splitkv_num_splits(1, 8, 1, 1, 16384, 128) == 128
