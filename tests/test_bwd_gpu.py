@@ -52,6 +52,8 @@ CASES = [
     (1, 100, 2, 2, 64, False),
     (1, 1, 2, 1, 128, True),
     (1, 513, 8, 2, 64, True),
+    # 160 dK/dV and 320 dQ tiles on a 152-SM grid: partial zig-zag turns in both kernels
+    (1, 1024, 40, 20, 128, True),
 ]
 
 

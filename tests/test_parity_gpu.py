@@ -37,6 +37,8 @@ SMALL = [
     small("outliers_causal", B=1, H=4, Hkv=1, N=512, d=128, causal=True, k_outlier_frac=0.005),
     small("fp8_noncausal", B=1, H=2, Hkv=2, N=512, d=128, dtype="fp8_e4m3"),
     small("fp8_causal", B=1, H=2, Hkv=1, N=640, d=128, causal=True, dtype="fp8_e4m3"),
+    # 160 causal work tiles on a 152-SM grid: a second, partial turn dealt in reverse (zig-zag)
+    small("causal_gqa_two_turns", B=1, H=40, Hkv=20, N=1024, d=128, causal=True, seed=78),
 ]
 
 
