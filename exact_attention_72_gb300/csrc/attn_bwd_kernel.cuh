@@ -295,6 +295,8 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         };
         if (!issue_st(steps)) { ok = false; break; }
         issue_dpt(steps);
+        // K and V are read by the S^T and dP^T GEMMs only: free them after the tile's last dP^T.
+        if (n == 1) tc_commit(smem_addr(&bar_kv_empty));
         for (int k = 0; k < n; ++k) {
           const uint32_t cur = steps + k;
           const uint32_t sQ = stage_q(cur), sdO = sQ + C::TILE_BYTES;
@@ -308,12 +310,14 @@ attn_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
           tc_fence_after();
           issue_ts_128<C>(tmem + C::ACC1, tmem + C::DP_COL, sQ, k > 0);    // dK += dS^T Q_i
           tc_commit(smem_addr(&bar_st_empty[cur % C::STAGES]));
-          if (k + 1 < n) issue_dpt(cur + 1);
+          if (k + 1 < n) {
+            issue_dpt(cur + 1);
+            if (k + 2 == n) tc_commit(smem_addr(&bar_kv_empty));
+          }
         }
         if (!ok) break;
         steps += n;
         tc_commit(smem_addr(&bar_acc_full));
-        tc_commit(smem_addr(&bar_kv_empty));
         ++tiles;
       }
       tc_commit(smem_addr(&bar_drain));
