@@ -19,15 +19,19 @@
 //   * attn_bwd_dq_kernel: one CTA per (batch, query head, 128-row query tile i); it loops over
 //     the key tiles j that tile i sees, computing S and dP with queries as lanes and
 //     dQ += dS K_j with dS (bf16, written over S in TMEM) as the A operand. S is double-buffered
-//     (TMEM has room here), so S_{j+1} runs while the elementwise warps work on step j.
+//     (TMEM has room here), so S_{j+1} runs while the elementwise warps work on step j, and K
+//     and V stream through rings of their own (three and two stages).
+// Both kernels are persistent; causal work tiles go longest first and are dealt to the CTAs in
+// zig-zag turns (deal_tile).
 // S and dP are computed twice in all (once per kernel): 7 tile GEMMs against 5 for a single
 // kernel that accumulates dQ across CTAs, traded for deterministic results and no fp32 atomic
 // traffic.
 //
 // Roles (576 threads): warps 0-15 elementwise, four warpgroups that split the 128 columns of a
 // tile (thread = TMEM lane = one row, warpgroup g = columns 32g .. 32g+31); warp 16 issues the
-// MMAs, warp 17 the TMA loads. The elementwise work of a step runs in two passes with their own
-// barriers: P from S (the dV GEMM can start, while the dP GEMM may still run), then dS from dP.
+// MMAs, warp 17 the TMA loads. In the dK/dV kernel the elementwise work of a step runs in two
+// passes with their own barriers: P from S (the dV GEMM can start, while the dP GEMM may still
+// run), then dS from dP. The dQ kernel forms dS in one pass.
 // bf16 results are written in place over the fp32 columns they came from, so all warpgroups
 // read their columns first and meet at a named barrier before any write: packed column c/2 of
 // one group's columns lies in the fp32 columns of another. Every wait is bounded (status word + abort
