@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp, sz, vp]
     L.attn_splitkv_num_splits.restype = i
     L.attn_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
+    L.attn_fwd_halved_tail_tiles.restype = i
+    L.attn_fwd_halved_tail_tiles.argtypes = [i, i, i, i, i]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -342,6 +344,11 @@ def quantize_e4m3(x, block_rows: int, signs=None, out=None, descale=None, stream
 
 def attn_quantize_e4m3_descale_count(B: int, N: int, Hx: int, block_rows: int) -> int:
     return int(lib().attn_quantize_e4m3_descale_count(B, N, Hx, block_rows))
+
+
+def attn_fwd_halved_tail_tiles(B: int, H: int, N: int, d: int, causal: bool) -> int:
+    """Work tiles of an attn_fwd call whose key range the library halves across two launches."""
+    return int(lib().attn_fwd_halved_tail_tiles(B, H, N, d, int(bool(causal))))
 
 
 def attn_splitkv_num_splits(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:

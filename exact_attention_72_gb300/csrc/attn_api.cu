@@ -351,11 +351,26 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
   p.debug_skip_load = g_skip_load;
   a.num_sms = di->num_sms;
-  cudaError_t e;
-  switch (d) {
-    case 64: e = dispatch_d<64>(a, causal != 0, fp8, stream); break;
-    case 128: e = dispatch_d<128>(a, causal != 0, fp8, stream); break;
-    default: e = dispatch_d<256>(a, causal != 0, fp8, stream); break;
+  // A last wave that would leave more than half of the SMs idle is halved along the keys: the
+  // first launch takes the first halves, a dependent launch the second halves and the merge.
+  const int halved = gb300::halved_tail_tiles(p.n_tiles, p.n_kvt, a.num_sms, causal != 0);
+  p.tail_mode = halved ? 1 : 0;
+  p.tail_first = p.n_tiles - halved;
+  p.tail_kvt = p.n_kvt / 2;
+  auto launch = [&](gb300::LaunchArgs& x) -> cudaError_t {
+    switch (d) {
+      case 64: return dispatch_d<64>(x, causal != 0, fp8, stream);
+      case 128: return dispatch_d<128>(x, causal != 0, fp8, stream);
+      default: return dispatch_d<256>(x, causal != 0, fp8, stream);
+    }
+  };
+  cudaError_t e = launch(a);
+  if (e == cudaSuccess && halved) {
+    gb300::LaunchArgs second = a;
+    second.params.tail_mode = 2;
+    second.params.n_tiles = halved;
+    second.dependent = true;
+    e = launch(second);
   }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
@@ -481,6 +496,17 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   const bool synced = cudaStreamSynchronize(stream) == cudaSuccess;
   if (st != ATTN_OK) return st;
   return (ok && joined && synced) ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
+  int sms = 152;
+  DeviceInfo* di = device_info();
+  if (di) sms = di->num_sms;
+  const long long rows = gb300::rows_per_work_tile(d);
+  const long long tiles = (long long)B * H * ((N + rows - 1) / rows);
+  if (tiles >= (1LL << 31)) return 0;
+  return gb300::halved_tail_tiles(tiles, (N + 127) / 128, sms, causal != 0);
 }
 
 int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {

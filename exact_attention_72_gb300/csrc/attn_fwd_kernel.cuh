@@ -66,6 +66,11 @@ struct AttnParams {
   const int* cu_q;
   const int* cu_k;
   const int* plan;
+  // Non-causal prefill, last wave halved: in the first launch (tail_mode 1) work tiles
+  // t >= tail_first visit only KV tiles [0, tail_kvt); a second launch (tail_mode 2), one unit per
+  // such tile (unit u is tile tail_first + u), visits [tail_kvt, n_kvt) and merges its half into
+  // the O and LSE the first launch wrote. tail_mode 0: every tile visits all KV tiles.
+  int tail_mode, tail_first, tail_kvt;
   uint32_t* status;         // device status word (first failure)
   unsigned long long timeout_ns;
   int debug_skip_load;      // fault injection: CTA 0 never loads V_0 of its first tile
@@ -199,8 +204,15 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
     c.mb = p.n_mb - 1 - t / BH;
     bh = t % BH;
   } else {
-    c.mb = t % p.n_mb;
-    bh = t / p.n_mb;
+    int tile = t;
+    if (p.tail_mode == 2) {
+      tile += p.tail_first;
+      c.j0 = p.tail_kvt;
+    } else if (p.tail_mode == 1 && t >= p.tail_first) {
+      c.j1 = p.tail_kvt;
+    }
+    c.mb = tile % p.n_mb;
+    bh = tile / p.n_mb;
   }
   c.b = bh / p.H;
   c.h = bh % p.H;
@@ -221,8 +233,8 @@ __device__ __forceinline__ int kv_tiles_for(const TileCoord& tc, int qt, const A
   const int pos0 = q_tile_pos0<C>(tc, qt, p);
   if constexpr (C::VARLEN) return varlen_kv_tiles(pos0, tc.nq, tc.nk, C::CAUSAL);
   if (pos0 >= p.N) return 0;
-  if (C::SPLIT) return tc.j1 - tc.j0;
-  return C::CAUSAL ? (pos0 / C::BN + 1) : p.n_kvt;
+  if (C::SPLIT || !C::CAUSAL) return tc.j1 - tc.j0;
+  return pos0 / C::BN + 1;
 }
 
 // Optional event trace for pipeline analysis (off unless compiled with -DGB300_ATTN_TRACE):
@@ -344,9 +356,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // Split mode: the combine kernel is launched as a programmatic dependent; let its CTAs be
-  // scheduled now (they wait for this grid to finish before reading anything).
-  if constexpr (C::SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Split mode: the combine kernel is launched as a programmatic dependent; a halved last wave:
+  // the launch of the second halves is. Let its CTAs be scheduled now (they read this grid's
+  // results only after waiting for it to finish).
+  constexpr bool kDense = !C::CAUSAL && !C::SPLIT && !C::VARLEN;
+  if (C::SPLIT || (kDense && p.tail_mode == 1)) griddep_launch_dependents();
   const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
   const uint32_t sKV = smem_base + C::Q_BYTES;
@@ -940,9 +954,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // Varlen: a row whose keys were all masked (its max never left -inf) gets O = 0 and
         // LSE = -inf; its accumulator holds no meaningful value.
         const bool empty_row = C::VARLEN && m == -INFINITY;
-        const float inv_l = out_scale / l;
+        float inv_l = out_scale / l;
         __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.o) +
                               ((size_t)(tc.bo * p.N + tc.q_base + (valid ? row : 0)) * p.H + tc.h) * C::D;
+        float* lse_dst = p.lse + ((size_t)tc.bo * p.H + tc.h) * p.N + tc.q_base + (valid ? row : 0);
+        float lse_out = lse_row;
+        // Second KV half of a halved tile: the first launch wrote this row's O_a (bf16) and LSE_a
+        // over keys [0, tail_kvt). With this half's O_b and LSE_b over the rest, the row over all
+        // keys is LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b (the
+        // split-KV combine for two ranges). Wait for the first grid to finish before reading.
+        const bool merge = kDense && p.tail_mode == 2;
+        float w_a = 0.0f;
+        if (merge) {
+          griddep_wait();
+          if (valid) {
+            const float a2 = __ldcg(lse_dst) * 1.4426950408889634f;   // LSE_a in log2 units
+            const float b2 = m + log2f(l);
+            const float mx = fmaxf(a2, b2);
+            const float ea = ex2(a2 - mx), eb = ex2(b2 - mx);
+            const float inv = 1.0f / (ea + eb);
+            w_a = ea * inv;
+            inv_l *= eb * inv;
+            lse_out = (mx + log2f(ea + eb)) * 0.69314718055994531f;
+          }
+        }
 #pragma unroll 1
         for (int c0 = 0; c0 < C::D; c0 += 32) {
           uint32_t ov[32];
@@ -950,10 +985,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           tmem_ld_wait();
           reg_fence32(ov);
           uint32_t pk[16];
+          if (merge && valid) {
+            // O_a of these 32 columns: 16 bf16 pairs, the lower-addressed element in the low half.
+            const uint4* src = reinterpret_cast<const uint4*>(orow + c0);
 #pragma unroll
-          for (int c = 0; c < 32; c += 2)
-            pk[c >> 1] = empty_row ? 0u
-                                   : pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
+            for (int v4 = 0; v4 < 4; ++v4) {
+              const uint4 u = __ldcg(src + v4);
+              const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int c = 8 * v4 + 2 * i;
+                pk[c >> 1] = pack_bf16x2(fmaf(__uint_as_float(ov[c]), inv_l, __uint_as_float(wds[i] << 16) * w_a),
+                                         fmaf(__uint_as_float(ov[c + 1]), inv_l,
+                                              __uint_as_float(wds[i] & 0xFFFF0000u) * w_a));
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; c += 2)
+              pk[c >> 1] = empty_row ? 0u
+                                     : pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
+          }
           if (valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
@@ -961,7 +1013,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           }
         }
-        if (valid) p.lse[((size_t)tc.bo * p.H + tc.h) * p.N + tc.q_base + row] = empty_row ? -INFINITY : lse_row;
+        if (valid) *lse_dst = empty_row ? -INFINITY : lse_out;
       }
     }
   }
@@ -975,6 +1027,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   __syncthreads();
   tc_fence_after();
   if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
+  // A second-half launch never finishes before the first launch, even where a failed wait kept
+  // its epilogue from waiting, so work queued after it on the stream sees both.
+  if (kDense && p.tail_mode == 2) griddep_wait();
 }
 
 }  // namespace gb300

@@ -11,6 +11,7 @@ struct LaunchArgs {
   CUtensorMap tm_q, tm_k, tm_v;
   AttnParams params;
   int num_sms;
+  bool dependent;   // launch as a programmatic dependent of the previous kernel on the stream
 };
 
 // Per-instance launcher: grid = min(work tiles, SMs), one persistent CTA per SM. SPLIT selects
@@ -60,6 +61,17 @@ cudaError_t launch_quantize_e4m3(const QuantLaunch& q, cudaStream_t stream);
 
 // Rows of queries one CTA work tile covers for head dim d (two 128-row tiles for d <= 128).
 inline int rows_per_work_tile(int d) { return d <= 128 ? 256 : 128; }
+
+// Non-causal prefill: work tiles of the last wave whose KV range is halved across two launches
+// (0: none). The last wave of `tiles` over `sms` persistent CTAs holds 1..sms tiles; when it would
+// leave more than half of the SMs idle, its tiles are cut in two at KV tile n_kvt / 2, the second
+// halves running as a dependent launch on the idle SMs. Each half keeps at least eight KV tiles,
+// so the halves' own pipeline fill and the merge stay small beside what they save.
+inline int halved_tail_tiles(long long tiles, int n_kvt, int sms, bool causal) {
+  if (causal || n_kvt < 16 || sms < 2 || tiles < 1) return 0;
+  const long long rem = tiles - (tiles - 1) / sms * sms;
+  return rem <= sms / 2 ? (int)rem : 0;
+}
 // Split-KV mode always runs one 128-row Q tile per CTA.
 inline int rows_per_split_work_tile(int) { return 128; }
 

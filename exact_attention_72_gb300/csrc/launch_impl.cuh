@@ -21,8 +21,23 @@ cudaError_t launch_attn_fwd(LaunchArgs& a, cudaStream_t stream) {
   }
   // Varlen: n_tiles is the host's upper bound; the kernel reads the plan's own count.
   const int grid = a.params.n_tiles < a.num_sms ? a.params.n_tiles : a.num_sms;
-  kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.params);
-  return cudaGetLastError();
+  if (!a.dependent) {
+    kernel<<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.params);
+    return cudaGetLastError();
+  }
+  // Programmatic dependent: its CTAs may start on SMs the previous grid has left, before that
+  // grid ends; the kernel waits (griddepcontrol.wait) before reading the previous grid's output.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a.tm_q, a.tm_k, a.tm_v, a.params);
 }
 
 }  // namespace gb300

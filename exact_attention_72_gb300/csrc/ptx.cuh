@@ -355,3 +355,13 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 }  // namespace gb300
+
+namespace gb300 {
+// Programmatic dependent launch. launch_dependents: this CTA allows the grid launched after it on
+// the stream with programmatic serialization to be scheduled. wait: block until every grid this
+// one depends on has completed and its memory writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+}  // namespace gb300

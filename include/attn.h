@@ -64,6 +64,16 @@ typedef enum {
  * Alignment: q, k, v, o must be 16-byte aligned (tensor-memory-accelerator copies and 16-byte
  * stores); lse 4-byte aligned. o and lse must not overlap q, k, v or each other.
  *
+ * Launches: one persistent kernel, one CTA per SM, each CTA walking work tiles of 256 (d <= 128)
+ * or 128 (d == 256) query rows of one (batch, head). Non-causal calls whose last wave of work
+ * tiles would leave more than half of the SMs idle (see attn_fwd_halved_tail_tiles) make a
+ * second launch: the first launch covers keys [0, K/2) of those last tiles (K = ceil(N / 128)
+ * key tiles) and writes their O and LSE as usual; the second, a programmatic dependent launch
+ * whose CTAs start on the SMs the first one leaves idle, covers keys [K/2, K), waits for the
+ * first launch to finish, and merges the two halves into o and lse
+ * (LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b). The first half's
+ * O passes through o in bf16, so those rows carry one extra bf16 rounding of that part.
+ *
  * Errors: argument problems return ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED synchronously
  * and launch nothing. A failed launch returns ATTN_ERR_CUDA. A kernel that gives up a bounded
  * internal wait finishes early and records it in a device status word: read it with
@@ -73,6 +83,16 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        int B, int H, int Hkv, int N, int d, float scale, int causal,
                        attn_dtype_t dtype, const float* descale_q, const float* descale_k,
                        const float* descale_v, cudaStream_t stream);
+
+/*
+ * attn_fwd_halved_tail_tiles — how many work tiles of an attn_fwd call (and of the fp8 variants
+ * with the same shape) have their key range halved across two launches: the tiles of the last
+ * wave, when causal == 0, ceil(N / 128) >= 16 and that wave holds at most half as many tiles as
+ * the device has SMs (work tiles: B * H * ceil(N / R), R = 256 for d <= 128, 128 for d == 256).
+ * 0 means one launch. Host-only; uses 152 SMs when no device can be queried; returns 0 for
+ * invalid sizes.
+ */
+int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal);
 
 /*
  * attn_fwd_fp8_scaled — attn_fwd for e4m3 q, k, v with descale factors that vary by batch and

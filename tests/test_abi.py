@@ -183,3 +183,18 @@ def test_split_heuristic_bounds(lib):
     assert binding.attn_splitkv_num_splits(4, 32, 8, 16, 8192, 128) == 4
     assert binding.attn_splitkv_num_splits(64, 64, 8, 1, 512, 128) == 1
     assert binding.attn_splitkv_num_splits(1, 8, 1, 1, 16384, 128) == 128
+
+
+def test_halved_tail_rule(lib):
+    """The last wave is halved along the keys only for non-causal calls whose last wave would
+    leave more than half of the 152 SMs idle and whose halves keep at least eight key tiles."""
+    f = binding.attn_fwd_halved_tail_tiles
+    assert f(2, 8, 4096, 256, False) == 56      # 512 tiles: three waves of 152, then 56
+    assert f(1, 16, 8192, 128, False) == 56     # 16 heads x 32 blocks of 256 rows
+    assert f(1, 16, 16384, 64, False) == 0      # 1024 tiles: last wave of 112 > 76
+    assert f(2, 32, 8192, 128, True) == 0       # causal: longest-first deal instead
+    assert f(1, 8, 2048, 128, False) == 64      # one wave of 64 tiles
+    assert f(1, 8, 1920, 128, False) == 0       # 15 key tiles: halves too short
+    assert f(1, 2, 256, 64, False) == 0
+    assert f(0, 8, 4096, 128, False) == 0
+    assert f(1, 8, 4096, 96, False) == 0

@@ -18,9 +18,10 @@ def _built(cuda_device):
     binding.attn_debug_set(timeout_ns=1_000_000_000)   # a correct launch never waits this long
 
 
-@pytest.mark.parametrize("d,causal", [(128, True), (256, False), (64, False)])
-def test_skipped_copy_times_out_and_context_survives(d, causal):
-    w = inputs.Workload("fault", B=1, H=4, Hkv=2, N=512, d=d, causal=causal, seed=3)
+# The last case has its keys halved across two launches; CTA 0 of each skips a copy.
+@pytest.mark.parametrize("d,causal,N", [(128, True, 512), (256, False, 512), (64, False, 512), (128, False, 2048)])
+def test_skipped_copy_times_out_and_context_survives(d, causal, N):
+    w = inputs.Workload("fault", B=1, H=4, Hkv=2, N=N, d=d, causal=causal, seed=3)
     x = inputs.make_inputs(w)
     q, k, v, _ = to_device(x)
     binding.attn_clear_status()

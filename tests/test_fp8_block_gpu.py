@@ -132,6 +132,8 @@ BCASES = [
     dict(B=2, H=2, Hkv=2, N=300, causal=False, rot=False, seed=7002),
     dict(B=1, H=4, Hkv=1, N=640, causal=True, rot=True, seed=7003),
     dict(B=1, H=2, Hkv=2, N=200, causal=False, rot=True, seed=7004),
+    # 17 key tiles, 36 work tiles: the last wave's keys are halved across two launches
+    dict(B=1, H=4, Hkv=2, N=2100, causal=False, rot=False, seed=7005),
 ]
 
 

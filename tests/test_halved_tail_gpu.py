@@ -1,0 +1,88 @@
+"""GPU parity of the halved last wave (non-causal prefill).
+
+When the last wave of work tiles would leave more than half of the SMs idle, attn_fwd cuts those
+tiles' keys in two: the first launch covers keys [0, K/2) and writes O and LSE, a dependent launch
+covers [K/2, K) and merges. Every case below makes the library halve some tiles (asserted through
+attn_fwd_halved_tail_tiles) and compares every row of the halved heads, and of a head that was not
+halved, with the fp64 oracle.
+"""
+import pytest
+import torch
+
+from exact_attention_72_gb300 import binding, inputs
+from parity_util import all_heads, check_convex_hull, compare_heads, oracle_heads, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    from exact_attention_72_gb300 import build
+    build.build()
+    binding.attn_debug_set(timeout_ns=1_000_000_000)   # a correct launch never waits this long
+
+
+def case(name, **kw):
+    base = dict(B=1, H=8, Hkv=2, N=2048, d=128, causal=False, seed=91)
+    base.update(kw)
+    return inputs.Workload(name, **base)
+
+
+CASES = [
+    # one wave of 64 tiles, every tile halved at key tile 8 of 16 (GQA)
+    case("one_wave_gqa"),
+    # ragged keys: 16 key tiles, the last one 80 keys long, in the second half
+    case("ragged_n2000", H=4, Hkv=4, N=2000, seed=92),
+    case("d64", H=4, Hkv=1, N=4096, d=64, seed=93),
+    # d = 256 (128-row tiles): 17 key tiles, halves of 8 and 9, ragged query and key tails
+    case("d256_ragged", H=3, Hkv=3, N=2100, d=256, seed=94),
+    case("fp8_per_tensor", H=4, Hkv=2, N=2304, dtype="fp8_e4m3", seed=95),
+    case("outliers", H=4, Hkv=1, N=2048, seed=96, k_outlier_frac=0.005),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_halved_tiles_match_oracle(w):
+    assert binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) > 0
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
+
+
+def test_second_wave_tail():
+    """160 tiles on 152 SMs: 152 whole tiles, then 8 halved ones (all of head 19)."""
+    w = case("two_waves", H=20, Hkv=4, N=2048, seed=97)
+    assert binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) == 8
+    x = inputs.make_inputs(w)
+    o, lse = run_cuda(w, x)
+    compare_heads(w, o, lse, oracle_heads(w, x, [(0, 0), (0, 18), (0, 19)]))
+    check_convex_hull(w, x, o)
+
+
+def test_halved_repeatable_bitwise():
+    w = CASES[0]
+    x = inputs.make_inputs(w)
+    o1, l1 = run_cuda(w, x)
+    o2, l2 = run_cuda(w, x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_halved_matches_whole_tiles_within_rounding():
+    """The same heads computed as whole tiles (19 heads: 152 tiles, one full wave, no halving) and
+    as halved tiles (the first 8 heads alone: 64 tiles) agree to within the extra bf16 rounding."""
+    whole = case("whole", H=19, Hkv=19, N=2048, seed=98)            # 152 tiles: no halving
+    assert binding.attn_fwd_halved_tail_tiles(whole.B, whole.H, whole.N, whole.d, False) == 0
+    x = inputs.make_inputs(whole)
+    o_w, l_w = run_cuda(whole, x)
+    # the first 8 heads alone: 64 tiles, all halved
+    sub = case("sub", H=8, Hkv=8, N=2048, seed=98)
+    assert binding.attn_fwd_halved_tail_tiles(sub.B, sub.H, sub.N, sub.d, False) == 64
+    q, k, v = (t[:, :, :8].contiguous().cuda() for t in (x.q, x.k, x.v))
+    o_h, l_h = binding.attn_fwd(q, k, v, causal=False, scale=sub.scale)
+    assert binding.attn_get_status()[0] == binding.ATTN_OK
+    torch.cuda.synchronize()
+    a, b = o_w[:, :, :8].float(), o_h.float()
+    # a bf16 rounding (relative error <= 2^-8) of O_a, plus the final rounding on each side
+    bound = 4 * 2.0 ** -8 * max(float(a.abs().max()), float(b.abs().max()))
+    assert float((a - b).abs().max()) <= bound
+    assert float((l_w[:, :8] - l_h).abs().max()) <= 1e-4
