@@ -356,7 +356,7 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   const int halved = gb300::halved_tail_tiles(p.n_tiles, p.n_kvt, a.num_sms, causal != 0);
   p.tail_mode = halved ? 1 : 0;
   p.tail_first = p.n_tiles - halved;
-  p.tail_kvt = p.n_kvt / 2;
+  p.tail_kvt = gb300::halved_tail_cut(p.n_kvt);
   auto launch = [&](gb300::LaunchArgs& x) -> cudaError_t {
     switch (d) {
       case 64: return dispatch_d<64>(x, causal != 0, fp8, stream);

@@ -67,11 +67,11 @@ typedef enum {
  * Launches: one persistent kernel, one CTA per SM, each CTA walking work tiles of 256 (d <= 128)
  * or 128 (d == 256) query rows of one (batch, head). Non-causal calls whose last wave of work
  * tiles would leave more than half of the SMs idle (see attn_fwd_halved_tail_tiles) make a
- * second launch: the first launch covers keys [0, K/2) of those last tiles (K = ceil(N / 128)
- * key tiles) and writes their O and LSE as usual; the second, a programmatic dependent launch
- * whose CTAs start on the SMs the first one leaves idle, covers keys [K/2, K), waits for the
- * first launch to finish, and merges the two halves into o and lse
- * (LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b). The first half's
+ * second launch: the first launch covers keys [0, 128 C) of those last tiles, C = floor(K / 2)
+ * (K = ceil(N / 128) key tiles), and writes their O and LSE as usual; the second, a
+ * programmatic dependent launch whose CTAs start on the SMs the first one leaves idle, covers
+ * keys [128 C, N), waits for the first launch to finish, and merges the two parts into o and lse
+ * (LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b). The first part's
  * O passes through o in bf16, so those rows carry one extra bf16 rounding of that part.
  *
  * Errors: argument problems return ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED synchronously

@@ -1,8 +1,8 @@
 """GPU parity of the halved last wave (non-causal prefill).
 
 When the last wave of work tiles would leave more than half of the SMs idle, attn_fwd cuts those
-tiles' keys in two: the first launch covers keys [0, K/2) and writes O and LSE, a dependent launch
-covers [K/2, K) and merges. Every case below makes the library halve some tiles (asserted through
+tiles' keys in two: the first launch covers key tiles [0, K/2) and writes O and LSE, a dependent
+launch covers the rest and merges. Every case below makes the library halve some tiles (asserted through
 attn_fwd_halved_tail_tiles) and compares every row of the halved heads, and of a head that was not
 halved, with the fp64 oracle.
 """
@@ -29,12 +29,12 @@ def case(name, **kw):
 
 
 CASES = [
-    # one wave of 64 tiles, every tile halved at key tile 8 of 16 (GQA)
+    # one wave of 64 tiles, every tile cut at key tile 8 of 16 (GQA)
     case("one_wave_gqa"),
-    # ragged keys: 16 key tiles, the last one 80 keys long, in the second half
+    # ragged keys: 16 key tiles, the last one 80 keys long, in the second part
     case("ragged_n2000", H=4, Hkv=4, N=2000, seed=92),
     case("d64", H=4, Hkv=1, N=4096, d=64, seed=93),
-    # d = 256 (128-row tiles): 17 key tiles, halves of 8 and 9, ragged query and key tails
+    # d = 256 (128-row tiles): 17 key tiles, parts of 8 and 9, ragged query and key tails
     case("d256_ragged", H=3, Hkv=3, N=2100, d=256, seed=94),
     case("fp8_per_tensor", H=4, Hkv=2, N=2304, dtype="fp8_e4m3", seed=95),
     case("outliers", H=4, Hkv=1, N=2048, seed=96, k_outlier_frac=0.005),
