@@ -43,6 +43,9 @@ HOST_SHAPES = [
     dict(B=2, H=8, Hkv=4, N=300, d=128, causal=False),     # two batches x two KV-head chunks, ragged N
     dict(B=5, H=2, Hkv=1, N=256, d=64, causal=True),       # uneven batch chunks
     dict(B=1, H=6, Hkv=3, N=200, d=256, causal=False),     # three KV-head chunks
+    # keys of every tile halved across two launches, in the device call and in each of the four
+    # chunks (two launches per chunk on the host path's two compute streams)
+    dict(B=1, H=8, Hkv=4, N=2048, d=128, causal=False),
 ]
 
 

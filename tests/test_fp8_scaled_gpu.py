@@ -61,6 +61,7 @@ CASES = [
     dict(B=1, H=4, Hkv=2, N=384, causal=True, seed=4101),
     dict(B=2, H=4, Hkv=4, N=300, causal=False, seed=4102),
     dict(B=2, H=8, Hkv=2, N=640, causal=True, seed=4103),
+    dict(B=1, H=8, Hkv=4, N=2048, causal=False, seed=4104),   # every tile's keys halved
 ]
 
 
