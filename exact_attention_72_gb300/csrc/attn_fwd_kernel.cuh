@@ -105,7 +105,18 @@ struct AttnCfg {
   static constexpr int PV_ROWS = 32 / ELT;                // V rows consumed per PV k-step
   static constexpr int P_COLS = BN * ELT / 4;             // TMEM columns holding one P row
   static constexpr int S_COL0 = 0, S_COL1 = 128;          // two S buffers
-  static constexpr int O_COL = 256;                       // O tile qt at O_COL + qt * D
+  // Two Q tiles at d = 64 leave room in TMEM for a third 128-column S buffer. The S products of
+  // both tiles then rotate through three buffers (the k-th S of the CTA in buffer k % 3), issued
+  // by a warp of their own (the otherwise idle twelfth warp), so a tile's S_{j+1} is issued as
+  // soon as a buffer is free, not behind its PV_j, and is ready when its softmax finishes step j.
+  static constexpr bool S3 = (NQ == 2 && D == 64);
+  // S-ready, P-ready and PV-done barriers: one per S buffer (one Q tile) or per Q tile (two); in
+  // three-buffer mode three per Q tile, the tile's g-th S product using index g % 3. A tile can
+  // then have up to three S products (or P halves, or PVs) outstanding without two of them
+  // sharing a barrier phase window.
+  static constexpr int N_SBAR = S3 ? 6 : 2;
+  static constexpr int N_OBAR = S3 ? 6 : NQ;
+  static constexpr int O_COL = S3 ? 384 : 256;            // O tile qt at O_COL + qt * D
   static constexpr int TMEM_COLS = 512;
   // Roles: warps [0, 4 NQ) softmax (one warpgroup per Q tile), then one MMA-issuer warp per Q
   // tile, then the TMA warp. With two Q tiles each tile has its own issuer, so one issuer's
@@ -113,6 +124,7 @@ struct AttnCfg {
   static constexpr int MMA_WARPS = NQ;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;            // one warpgroup per Q tile
   static constexpr int WARP_MMA = SOFTMAX_WARPS, WARP_LOAD = SOFTMAX_WARPS + MMA_WARPS;
+  static constexpr int WARP_S = WARP_LOAD + 1;            // three-buffer mode: the S issuer
   // Two Q tiles: 12 warps (softmax x8, MMA x2, load, one idle) so the third warpgroup can hand
   // registers to the softmax warpgroups with setmaxnreg. The launch gives 384 x 168 = 64,512
   // registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The host checks the
@@ -135,7 +147,8 @@ struct AttnCfg {
 
 // Wait-site codes recorded in the status word when a bounded wait gives up.
 enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
-                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9, SITE_S_TURN = 10 };
+                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9, SITE_S_TURN = 10,
+                  SITE_S_FREE = 12 };
 
 struct TileCoord {
   int b, h, mb;     // h: query head (prefill) or kv head (split-KV)
@@ -237,6 +250,14 @@ __device__ __forceinline__ int kv_tiles_for(const TileCoord& tc, int qt, const A
   return pos0 / C::BN + 1;
 }
 
+// Three-buffer mode: the position of Q tile qt's S_j among all S products of the CTA, in issue
+// order, for a work tile whose two Q tiles visit n0 and n1 KV tiles, given the count issued before
+// the work tile. The two issuers alternate turns (S0_j, then S1_j) and skip the turns of S
+// products their tile does not need, so that order is fixed. S number k lives in buffer k % 3.
+__device__ __forceinline__ uint32_t s_number(uint32_t sbase, int qt, int j, int n0, int n1) {
+  return sbase + (uint32_t)(min(j, n0) + min(j, n1) + ((qt == 1 && j < n0) ? 1 : 0));
+}
+
 // Optional event trace for pipeline analysis (off unless compiled with -DGB300_ATTN_TRACE):
 // in CTA 0, each warp's recording lane appends (event, a, b, clock64) to its own 1024-entry slot.
 #ifdef GB300_ATTN_TRACE
@@ -336,7 +357,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // kv_empty / q_empty take one arrival per MMA-issuer warp (a tcgen05.commit after the MMAs
   // that read the stage, or a plain arrive for a stage that warp's Q tile does not need).
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain[C::MMA_WARPS];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain[C::MMA_WARPS + (C::S3 ? 1 : 0)];
   // s_turn[q]: issuer q may take its next S turn. The two issuers alternate S issues
   // (S0_j, S1_j, S0_{j+1}, ...), which keeps the two Q tiles' softmax phases staggered so the
   // tensor core always has the other tile's GEMMs to run.
@@ -349,7 +370,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // One pair per S buffer: with one Q tile the softmax may run a step ahead of the MMA warp,
   // and per-buffer barriers keep each barrier within one phase of its waiter (a buffer is
   // reused only after the PV that read it has been issued).
-  __shared__ __align__(8) uint64_t bar_s_full[2], bar_p_half[2][2], bar_o_done[C::NQ], bar_o_full[C::NQ];
+  // s_free[b] (three-buffer mode): the PV that read S buffer b has completed, so b can take a new S.
+  __shared__ __align__(8) uint64_t bar_s_full[C::N_SBAR], bar_p_half[C::N_SBAR][2], bar_o_done[C::N_OBAR], bar_o_full[C::NQ];
+  __shared__ __align__(8) uint64_t bar_s_free[C::S3 ? 3 : 1];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
 
@@ -370,22 +393,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     abort_flag = 0u;
     mbar_init(smem_addr(&bar_q_full), 1);
     mbar_init(smem_addr(&bar_q_empty), C::MMA_WARPS);
-    for (int i = 0; i < C::MMA_WARPS; ++i) mbar_init(smem_addr(&bar_drain[i]), 1);
+    for (int i = 0; i < C::MMA_WARPS + (C::S3 ? 1 : 0); ++i) mbar_init(smem_addr(&bar_drain[i]), 1);
     mbar_init(smem_addr(&bar_s_turn[0]), 1);
     mbar_init(smem_addr(&bar_s_turn[1]), 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(smem_addr(&bar_kv_full[i]), 1);
       mbar_init(smem_addr(&bar_kv_empty[i]), C::MMA_WARPS);
     }
-    for (int i = 0; i < 2; ++i) {
+    if constexpr (C::S3)
+      for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&bar_s_free[i]), 1);
+    for (int i = 0; i < C::N_SBAR; ++i) {
       mbar_init(smem_addr(&bar_s_full[i]), 1);
       mbar_init(smem_addr(&bar_p_half[i][0]), 128);
       mbar_init(smem_addr(&bar_p_half[i][1]), 128);
     }
-    for (int i = 0; i < C::NQ; ++i) {
-      mbar_init(smem_addr(&bar_o_done[i]), 1);
-      mbar_init(smem_addr(&bar_o_full[i]), 1);
-    }
+    for (int i = 0; i < C::N_OBAR; ++i) mbar_init(smem_addr(&bar_o_done[i]), 1);
+    for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_o_full[i]), 1);
     fence_mbar_init();
     mbar_arrive(smem_addr(&bar_s_turn[0]));   // issuer 0 takes the first S turn
   }
@@ -581,6 +604,47 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
         return true;
       };
+      if constexpr (C::S3) {
+        // Three S buffers: the S issuer warp issues every S; this warp issues its Q tile's PVs.
+        // PV_j reads P_j from S buffer k % 3 (k: S number of S_j); its completion frees that
+        // buffer (s_free) and is signalled on o_done for rescales. Barriers of this tile's g-th S
+        // product: index 3 myq + g % 3, phase g / 3.
+        uint32_t sbase = 0;   // S products of both Q tiles before the current work tile
+        uint32_t g = 0;       // S products of this Q tile before the current work tile
+        for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+          const TileCoord tc = decode_tile<C>(t, p);
+          const int n0 = kv_tiles_for<C>(tc, 0, p), n1 = kv_tiles_for<C>(tc, 1, p);
+          const int n = myq ? n1 : n0;
+          const int nmax = n0 > n1 ? n0 : n1;
+          if (C::VARLEN && nmax == 0) continue;
+          const uint32_t sb = sbase, gb = g;
+          sbase += (uint32_t)(n0 + n1);
+          g += (uint32_t)n;
+          const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
+          for (int j = 0; ok && j < nmax; ++j) {
+            const uint32_t pos_v = base + 2 * j + 1;
+            if (!wait_kv(pos_v)) { ok = false; break; }
+            if (j < n) {
+              const uint32_t gj = gb + j;
+              const uint32_t par = (gj / 3u) & 1u;
+              const uint32_t bi = 3u * myq + gj % 3u;
+              const uint32_t b = s_number(sb, myq, j, n0, n1) % 3u;
+              const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
+              if (!mbar_wait(smem_addr(&bar_p_half[bi][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv_half<C, 0>(d_o, tmem + b * 128u, b_v, j > 0);
+              if (!mbar_wait(smem_addr(&bar_p_half[bi][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv_half<C, 1>(d_o, tmem + b * 128u, b_v, true);
+              tc_commit(smem_addr(&bar_s_free[b]));
+              tc_commit(smem_addr(&bar_o_done[bi]));
+              if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
+            }
+            release(&bar_kv_empty[pos_v % C::NS], j < n);
+          }
+          ring = base + 2 * nmax;
+        }
+      } else {
       for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int n = kv_tiles_for<C>(tc, myq, p);
@@ -628,10 +692,62 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         ring = base + 2 * nmax;
       }
+      }
       // Every MMA this warp issued must finish before TMEM is released.
       tc_commit(smem_addr(&bar_drain[myq]));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain[myq]), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
+    }
+  } else if (C::S3 && warp == C::WARP_S) {
+    // ------------------------------------------------------------------ S issuer, three S buffers
+    if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
+    if (lane == 0) {
+      // S products in the order S0_0, S1_0, S0_1, S1_1, ... (skipping those a Q tile does not
+      // need), the k-th into buffer k % 3 once the PV of the (k-3)-th has read that buffer.
+      uint32_t ring = 0, nq_loads = 0, sbase = 0, g0 = 0, g1 = 0;
+      bool ok = true;
+      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+        const TileCoord tc = decode_tile<C>(t, p);
+        const int n0 = kv_tiles_for<C>(tc, 0, p), n1 = kv_tiles_for<C>(tc, 1, p);
+        const int nmax = n0 > n1 ? n0 : n1;
+        if (C::VARLEN && nmax == 0) continue;
+        const uint32_t sb = sbase, gb0 = g0, gb1 = g1;
+        sbase += (uint32_t)(n0 + n1);
+        g0 += (uint32_t)n0;
+        g1 += (uint32_t)n1;
+        if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
+        ++nq_loads;
+        const uint32_t base = ring;  // K_j at base + 2j
+        for (int j = 0; ok && j < nmax; ++j) {
+          const uint32_t pos_k = base + 2 * j;
+          if (!mbar_wait(smem_addr(&bar_kv_full[pos_k % C::NS]), (pos_k / C::NS) & 1, ctl, SITE_KV_FULL)) { ok = false; break; }
+          for (int qt = 0; ok && qt < 2; ++qt) {
+            if (j >= (qt ? n1 : n0)) continue;
+            const uint32_t k = s_number(sb, qt, j, n0, n1);
+            const uint32_t b = k % 3u;
+            if (k >= 3u && !mbar_wait(smem_addr(&bar_s_free[b]), ((k / 3u) - 1u) & 1u, ctl, SITE_S_FREE)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk<C>(tmem + b * 128u, sQ + qt * C::TILE_BYTES, sKV + (pos_k % C::NS) * C::TILE_BYTES);
+            const uint32_t gj = (qt ? gb1 : gb0) + j;
+            tc_commit(smem_addr(&bar_s_full[3u * qt + gj % 3u]));
+          }
+          if (!ok) break;
+          // K_j's stage and, after the last S, Q: both arrivals of each come from this warp.
+          tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
+          tc_commit(smem_addr(&bar_kv_empty[pos_k % C::NS]));
+          if (j + 1 == nmax) {
+            tc_commit(smem_addr(&bar_q_empty));
+            tc_commit(smem_addr(&bar_q_empty));
+          }
+        }
+        ring = base + 2 * nmax;
+      }
+      tc_commit(smem_addr(&bar_drain[C::MMA_WARPS]));
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(smem_addr(&bar_drain[C::MMA_WARPS]), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
   } else if (C::NQ == 1 && warp == C::WARP_MMA) {
     // ------------------------------------------------------------------ tcgen05 issuer, one Q tile
@@ -721,10 +837,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
+    uint32_t sbase = 0, g = 0;      // three buffers: S products of the CTA / of this Q tile so far
     bool ok = true;
     for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
       const TileCoord tc = decode_tile<C>(t, p);
       const int n = kv_tiles_for<C>(tc, qt, p);
+      int n0 = 0, n1 = 0;
+      uint32_t sb = 0, gb = 0;
+      if constexpr (C::S3) {
+        n0 = kv_tiles_for<C>(tc, 0, p);
+        n1 = kv_tiles_for<C>(tc, 1, p);
+        sb = sbase;
+        gb = g;
+        sbase += (uint32_t)(n0 + n1);
+        g += (uint32_t)n;
+      }
       const int row0 = q_tile_pos0<C>(tc, qt, p);   // prefill: first query row of the tile
       const int Nk = tc.nk;                         // keys of this sequence
       if (n == 0) {
@@ -760,8 +887,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float m = -INFINITY;   // running max of s * x (log2 units), used as the exponent shift
       float l = 0.0f;        // running sum of exp2(s * x - m)
       for (int j = 0; j < n; ++j) {
-        const int buf = C::NQ == 2 ? qt : (j & 1);
-        const uint32_t s_col = buf ? C::S_COL1 : C::S_COL0;
+        // buf: index of this S's barriers; s_col: its TMEM buffer (three buffers: S number % 3)
+        const int buf = C::S3 ? 3 * qt + (int)((gb + j) % 3u) : (C::NQ == 2 ? qt : (j & 1));
+        const uint32_t s_col = C::S3 ? (s_number(sb, qt, j, n0, n1) % 3u) * 128u : (buf ? C::S_COL1 : C::S_COL0);
         // Scales of the two 64-key halves of this tile (they differ only with K block descales;
         // read before the wait so the load latency hides behind it).
         float s_lo = s, s_hi = s;
@@ -770,10 +898,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           s_lo = s_q * __ldg(dk_row + kb * p.dk_sn);
           s_hi = s_q * __ldg(dk_row + min(kb + 1, n_kblk - 1) * p.dk_sn);
         }
-        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), s_cnt[buf] & 1, ctl, SITE_S_FULL);
+        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), C::S3 ? ((gb + j) / 3u) & 1u : s_cnt[buf] & 1, ctl, SITE_S_FULL);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (r == 0) ATTN_TRACE(4, qt, j);
-        ++s_cnt[buf];
+        if constexpr (!C::S3) ++s_cnt[buf];
         tc_fence_after();
         uint32_t sr[128];
         const uint32_t tS = tmem + lane_base + s_col;
@@ -885,8 +1013,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // Rescale O before any half of P_j is released: PV_j must accumulate onto the
             // rescaled O, and O must not be touched while PV_{j-1} is still accumulating into
             // it. Two Q tiles: S_j's commit already covered PV_{j-1} (same issuing thread), so O
-            // is settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV.
-            if constexpr (C::NQ == 1) {
+            // is settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV. Three S
+            // buffers: S_j comes from another warp, so wait for PV_{j-1} as well.
+            if constexpr (C::S3) {
+              const uint32_t gp = gb + j - 1;   // this tile's PV_{j-1}
+              w = mbar_wait(smem_addr(&bar_o_done[3 * qt + gp % 3u]), (gp / 3u) & 1u, ctl, SITE_O_DONE);
+              if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+            } else if constexpr (C::NQ == 1) {
               w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
