@@ -1,0 +1,277 @@
+"""Executable model of the synchronisation protocol of the d = 64 forward kernel (two Q tiles per
+CTA, three rotating S buffers in tensor memory, a dedicated S-issuer warp).
+
+This is test infrastructure: a model of the kernel's warp roles and mbarriers, not the kernel. It
+runs the roles as Python generators under random interleavings and checks three things:
+
+* every parity wait sees its barrier at the intended phase or one past it, since a parity wait
+  cannot tell phases two apart (hardware semantics: the wait returns once the phase with the
+  awaited parity has completed);
+* no tensor-memory S buffer is overwritten before the softmax has read it and the PV has read the
+  P written over it, and no PV reads a buffer that holds anything but its own P;
+* the O accumulator is touched by a rescale only after the tile's previous PV has completed, and
+  read by the epilogue only after all of the tile's PVs.
+
+Roles, as in the kernel:
+  producer   loads Q once per work tile, then K_j, V_j through a ring of NS stages;
+  S issuer   issues S products in the order S0_0, S1_0, S0_1, S1_1, ..., skipping those a Q tile
+             does not need. S number k goes to buffer k % 3 once the PV of number k - 3 has
+             completed (s_free). It releases each K stage and, after the last S, Q;
+  PV issuer  one per Q tile: waits for the two P halves of its tile's S_j, issues PV_j, and commits
+             s_free (the buffer), o_done (for rescales), and o_full after the tile's last PV;
+  softmax    one per Q tile: waits for S_j, maybe rescales O (after waiting for PV_{j-1}), writes
+             P_j over S_j, and at the end of the work tile waits for o_full.
+  tensor pipe executes MMAs and commits in issue order: one shared in-order queue, or (a weaker
+             model) one queue per issuing warp.
+
+Each Q tile has M S-ready, P-ready and PV-done barriers, its g-th S product using index g % M and
+phase g // M. The kernel uses M = 3.
+"""
+import random
+
+NS = 8   # K/V ring stages of the d = 64 instance
+
+
+class ProtocolError(Exception):
+    pass
+
+
+class Bar:
+    """An mbarrier: `expected` arrivals complete a phase."""
+
+    def __init__(self, name, expected, pre=0):
+        self.name, self.expected, self.done, self.arr = name, expected, 0, 0
+        for _ in range(pre):
+            self.arrive()
+
+    def arrive(self):
+        self.arr += 1
+        if self.arr == self.expected:
+            self.done += 1
+            self.arr = 0
+
+
+def wait(bar, parity, intended):
+    """Poll until the phase with this parity has completed, checking the phase window."""
+    while True:
+        if bar.done not in (intended, intended + 1):
+            raise ProtocolError(f"phase window broken on {bar.name}: done={bar.done} awaited={intended}")
+        if (bar.done & 1) != parity:
+            return
+        yield
+
+
+def s_number(sbase, qt, j, n0, n1):
+    """Position of Q tile qt's S_j among the CTA's S products (n0, n1: KV tiles of the two tiles)."""
+    return sbase + min(j, n0) + min(j, n1) + (1 if (qt == 1 and j < n0) else 0)
+
+
+def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, skip_rescale_wait=False):
+    """Runs the work tiles [(n0, n1), ...] of one CTA to completion under a random schedule."""
+    rnd = random.Random(seed)
+    q_full, q_empty = Bar("q_full", 1), Bar("q_empty", 2)
+    kv_full = [Bar(f"kv_full{i}", 1) for i in range(NS)]
+    kv_empty = [Bar(f"kv_empty{i}", 2) for i in range(NS)]
+    s_full = [Bar(f"s_full{i}", 1) for i in range(2 * M)]
+    p_half = [[Bar(f"p_half{i}.{h}", 1) for h in range(2)] for i in range(2 * M)]
+    o_done = [Bar(f"o_done{i}", 1) for i in range(2 * M)]
+    s_free = [Bar(f"s_free{i}", 1) for i in range(3)]
+    o_full = [Bar(f"o_full{i}", 1) for i in range(2)]
+    tmem = [None, None, None]                 # ("S", k) or ("P", k)
+    pv_done = set()                           # S numbers whose PV has completed
+    pv_complete = {0: set(), 1: set()}        # (work tile, j) per Q tile
+    queues = {0: [], 1: [], 2: []}            # per issuing warp (2: the S issuer)
+    shared = []
+
+    def enqueue(iss, op):
+        (shared if shared_pipe else queues[iss]).append((iss, op))
+
+    def commit(iss, bar):
+        enqueue(iss, ("commit", bar))
+
+    def producer():
+        ring, nq = 0, 0
+        for (n0, n1) in tiles:
+            nmax = max(n0, n1)
+            if nmax == 0:
+                continue
+            if nq > 0:
+                yield from wait(q_empty, (nq - 1) & 1, nq - 1)
+            nq += 1
+            yield
+            q_full.arrive()
+            for _ in range(2 * nmax):
+                slot = ring % NS
+                if ring >= NS:
+                    yield from wait(kv_empty[slot], (ring // NS - 1) & 1, ring // NS - 1)
+                yield
+                kv_full[slot].arrive()
+                ring += 1
+
+    def s_issuer():
+        ring, nq, sbase, g = 0, 0, 0, [0, 0]
+        for (n0, n1) in tiles:
+            nmax = max(n0, n1)
+            if nmax == 0:
+                continue
+            sb, gb = sbase, list(g)
+            sbase += n0 + n1
+            g[0] += n0
+            g[1] += n1
+            yield from wait(q_full, nq & 1, nq)
+            nq += 1
+            base = ring
+            for j in range(nmax):
+                pos_k = base + 2 * j
+                yield from wait(kv_full[pos_k % NS], (pos_k // NS) & 1, pos_k // NS)
+                for qt in range(2):
+                    if j < (n1 if qt else n0):
+                        k = s_number(sb, qt, j, n0, n1)
+                        if k >= 3 and not skip_s_free:
+                            yield from wait(s_free[k % 3], (k // 3 - 1) & 1, k // 3 - 1)
+                        enqueue(2, ("S", k, k % 3))
+                        commit(2, s_full[M * qt + (gb[qt] + j) % M])
+                commit(2, kv_empty[pos_k % NS])
+                commit(2, kv_empty[pos_k % NS])
+                if j + 1 == nmax:
+                    commit(2, q_empty)
+                    commit(2, q_empty)
+                yield
+            ring = base + 2 * nmax
+
+    def pv_issuer(myq):
+        ring, sbase, g = 0, 0, 0
+        for ti, (n0, n1) in enumerate(tiles):
+            n, nmax = (n1 if myq else n0), max(n0, n1)
+            if nmax == 0:
+                continue
+            sb, gb = sbase, g
+            sbase += n0 + n1
+            g += n
+            base = ring
+            for j in range(nmax):
+                pos_v = base + 2 * j + 1
+                yield from wait(kv_full[pos_v % NS], (pos_v // NS) & 1, pos_v // NS)
+                if j < n:
+                    gj = gb + j
+                    k = s_number(sb, myq, j, n0, n1)
+                    for h in range(2):
+                        yield from wait(p_half[M * myq + gj % M][h], (gj // M) & 1, gj // M)
+                    enqueue(myq, ("PV", k, k % 3, myq, ti, j))
+                    commit(myq, s_free[k % 3])
+                    commit(myq, o_done[M * myq + gj % M])
+                    if j + 1 == n:
+                        commit(myq, o_full[myq])
+                    commit(myq, kv_empty[pos_v % NS])
+                else:
+                    kv_empty[pos_v % NS].arrive()
+                yield
+            ring = base + 2 * nmax
+
+    def softmax(qt):
+        sbase, g, tiles_done = 0, 0, 0
+        for ti, (n0, n1) in enumerate(tiles):
+            n = n1 if qt else n0
+            sb, gb = sbase, g
+            sbase += n0 + n1
+            g += n
+            if n == 0:
+                continue
+            for j in range(n):
+                gj = gb + j
+                k = s_number(sb, qt, j, n0, n1)
+                yield from wait(s_full[M * qt + gj % M], (gj // M) & 1, gj // M)
+                if tmem[k % 3] != ("S", k):
+                    raise ProtocolError(f"softmax {qt} expected S{k} in buffer {k % 3}, found {tmem[k % 3]}")
+                yield
+                if j > 0 and rnd.random() < rescale_p:
+                    if not skip_rescale_wait:
+                        gp = gj - 1
+                        yield from wait(o_done[M * qt + gp % M], (gp // M) & 1, gp // M)
+                    if (ti, j - 1) not in pv_complete[qt]:
+                        raise ProtocolError("O rescaled while PV_{j-1} may still accumulate into it")
+                if tmem[k % 3] != ("S", k):
+                    raise ProtocolError(f"S{k} overwritten before its P was written")
+                tmem[k % 3] = ("P", k)
+                p_half[M * qt + gj % M][0].arrive()
+                yield
+                p_half[M * qt + gj % M][1].arrive()
+            yield from wait(o_full[qt], tiles_done & 1, tiles_done)
+            if any((ti, j) not in pv_complete[qt] for j in range(n)):
+                raise ProtocolError("epilogue read O before the tile's last PV completed")
+            tiles_done += 1
+
+    def execute(op):
+        if op[0] == "S":
+            _, k, b = op
+            prev = tmem[b]
+            if prev is not None and (prev != ("P", k - 3) or (k - 3) not in pv_done):
+                raise ProtocolError(f"S{k} overwrites buffer {b} holding {prev}")
+            tmem[b] = ("S", k)
+        elif op[0] == "PV":
+            _, k, b, qt, ti, j = op
+            if tmem[b] != ("P", k):
+                raise ProtocolError(f"PV{k} reads buffer {b} holding {tmem[b]}")
+            pv_done.add(k)
+            pv_complete[qt].add((ti, j))
+        else:
+            op[1].arrive()
+
+    def pipe(q):
+        while True:
+            if q:
+                execute(q.pop(0)[1])
+            yield
+
+    procs = {"producer": producer(), "s_issuer": s_issuer(), "pv0": pv_issuer(0), "pv1": pv_issuer(1),
+             "softmax0": softmax(0), "softmax1": softmax(1)}
+    finite = set(procs)
+    if shared_pipe:
+        procs["pipe"] = pipe(shared)
+    else:
+        for i in range(3):
+            procs[f"pipe{i}"] = pipe(queues[i])
+    steps = 0
+    while finite:
+        name = rnd.choice(list(procs))
+        try:
+            next(procs[name])
+        except StopIteration:
+            del procs[name]
+            finite.discard(name)
+        steps += 1
+        if steps > 1_000_000:
+            raise ProtocolError("no progress: " + ", ".join(sorted(finite)))
+
+
+def random_tiles(rnd, kind):
+    """Work tiles (n0, n1) of one CTA: equal counts (non-causal), one more KV tile for the second
+    Q tile (causal), or any pair including empty Q tiles (ragged batches)."""
+    out = []
+    for _ in range(rnd.randint(1, 10)):
+        if kind == "noncausal":
+            n = rnd.randint(1, 9)
+            out.append((n, n))
+        elif kind == "causal":
+            n0 = rnd.randint(1, 8)
+            out.append((n0, n0 + 1))
+        else:
+            out.append((rnd.randint(0, 6), rnd.randint(0, 6)))
+    return out
+
+
+SCHEDULES = ((True, 0.3), (False, 0.3), (True, 1.0), (False, 1.0))
+
+
+def sweep(n_cases, case_seed, **kw):
+    """Runs n_cases random tile lists under every schedule; returns the first failure or None."""
+    rnd = random.Random(case_seed)
+    for i in range(n_cases):
+        kind = ("noncausal", "causal", "ragged")[i % 3]
+        tiles = random_tiles(rnd, kind)
+        for shared, rp in SCHEDULES:
+            try:
+                run(tiles, seed=i * 7 + shared + int(rp * 10), shared_pipe=shared, rescale_p=rp, **kw)
+            except ProtocolError as e:
+                return f"{kind} {tiles}: {e}"
+    return None
