@@ -82,6 +82,13 @@ CASES = [
     vw("more_keys_noncausal", [16, 1, 130, 64], [700, 33, 400, 64], causal=False),
     vw("more_queries", [300, 129, 40], [100, 129, 3]),
     vw("d64_gqa", [333, 64, 517], H=8, Hkv=2, d=64),
+    # d = 64 (three rotating S buffers): work tiles whose first Q tile sees no key while the
+    # second does (bottom-right mask, more queries than keys), empty sequences, sequences with
+    # one Q tile, and many short sequences
+    vw("d64_more_queries", [300, 129, 40], [100, 129, 3], d=64, seed=8010),
+    vw("d64_empty_and_more_keys", [0, 200, 0, 77, 16, 130], [5, 200, 0, 0, 700, 400], d=64, seed=8011),
+    vw("d64_many_short_noncausal", inputs.varlen_lengths(40, 1, 90, 8012), H=2, Hkv=1, d=64, causal=False,
+       seed=8012),
     vw("d256", [333, 64, 200], H=2, Hkv=1, d=256),
     vw("d256_more_queries", [260, 5], [130, 300], H=2, Hkv=2, d=256),
     vw("fp8_causal", [250, 600, 90], dtype="fp8_e4m3"),
