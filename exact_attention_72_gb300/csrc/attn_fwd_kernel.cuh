@@ -16,7 +16,8 @@
 //     (mojostudio.in), section 2, the producer's multi-stage TMA pipeline with expected
 //     transaction bytes);
 //   * warp MMA (one thread) issues tcgen05.mma: S = Q K_j^T into tensor memory (TMEM), and
-//     O += P V_j with P read from TMEM (aliasing S) and V from shared memory;
+//     O += P V_j with P read from TMEM (aliasing S) and V from shared memory; at d = 64 a warp of
+//     its own issues the S products into three rotating TMEM buffers (see AttnCfg::S3);
 //   * one softmax warpgroup per Q tile (one thread per query row) reads S from TMEM, masks,
 //     takes the row max, evaluates exp2 with the scale folded in, accumulates the row sum,
 //     writes P back to TMEM and rescales O in TMEM when the running max moves;
@@ -125,10 +126,10 @@ struct AttnCfg {
   static constexpr int SOFTMAX_WARPS = 4 * NQ;            // one warpgroup per Q tile
   static constexpr int WARP_MMA = SOFTMAX_WARPS, WARP_LOAD = SOFTMAX_WARPS + MMA_WARPS;
   static constexpr int WARP_S = WARP_LOAD + 1;            // three-buffer mode: the S issuer
-  // Two Q tiles: 12 warps (softmax x8, MMA x2, load, one idle) so the third warpgroup can hand
-  // registers to the softmax warpgroups with setmaxnreg. The launch gives 384 x 168 = 64,512
-  // registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The host checks the
-  // compiled register count before launching (an over-subscribed increase would never return).
+  // Two Q tiles: 12 warps (softmax x8, MMA x2, load, and the S issuer at d = 64, else idle) so the
+  // third warpgroup can hand registers to the softmax warpgroups with setmaxnreg. The launch gives
+  // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The
+  // host checks the compiled register count first (an over-subscribed increase never returns).
   static constexpr bool REG_SPLIT = (NQ == 2);
   // With a two-stage ring (d = 256: 64 KB tiles) K_j always takes stage 0 and V_j stage 1. Then
   // K and V get a producer warp each (WARP_LOAD: Q and K, WARP_LOAD + 1: V), so the next K can
