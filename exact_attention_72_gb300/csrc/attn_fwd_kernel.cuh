@@ -96,11 +96,18 @@ struct AttnCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes (one TMA box)
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one Q, K or V tile
   static constexpr int Q_BYTES = NQ * TILE_BYTES;
+  // e4m3 with two Q tiles: P goes to shared memory (one 16 KB tile per Q tile, laid out like a Q
+  // tile) and the PV product reads it from there. The S buffer in TMEM is then free as soon as the
+  // softmax has loaded S_j, so S_{j+1} can be issued into it while the softmax still works on
+  // step j. (bf16 at d = 128 has no shared memory to spare for P, nor shared-memory bandwidth:
+  // its PV would read twice as many bytes per cycle as the e4m3 one.)
+  static constexpr bool PSMEM = FP8_ && (D_ <= 128 && !SPLIT_);
+  static constexpr int P_BYTES = PSMEM ? Q_BYTES : 0;
   static constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
   static constexpr int RESERVE = 1024 + 1024;             // alignment slack + static shared
-  static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES) / TILE_BYTES;
+  static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES - P_BYTES) / TILE_BYTES;
   static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;      // K/V ring stages
-  static constexpr int SMEM_BYTES = Q_BYTES + NS * TILE_BYTES + 1024;
+  static constexpr int SMEM_BYTES = Q_BYTES + P_BYTES + NS * TILE_BYTES + 1024;
   static constexpr int KSTEPS_QK = D * ELT / 32;          // one MMA k-step covers 32 bytes of K
   static constexpr int KSTEPS_PV = BN * ELT / 32;
   static constexpr int PV_ROWS = 32 / ELT;                // V rows consumed per PV k-step
@@ -335,6 +342,23 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint3
   }
 }
 
+// Half H of O += P V with P in shared memory (e4m3, laid out like a Q tile: 128 rows of 128
+// bytes, 128-byte swizzle, 32 bytes per k-step) and V MN-major as below.
+template <class C, int H>
+__device__ __forceinline__ void issue_pv_half_ss(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr,
+                                                 bool accumulate_first) {
+  constexpr int KH = C::KSTEPS_PV / 2;
+  const uint64_t a0 = make_sdesc_sw128(a_addr, 16, 1024);
+  const uint64_t b0 = make_sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+#pragma unroll
+  for (int i = 0; i < KH; ++i) {
+    const int kk = H * KH + i;
+    const uint32_t acc = (H > 0 || i > 0) ? 1u : (accumulate_first ? 1u : 0u);
+    mma_f16_or_f8<C::FP8>(d_tmem, a0 + (uint64_t)((kk * 32) >> 4),
+                          b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4), C::IDESC_PV, acc);
+  }
+}
+
 // Half H of O += P V: the k-steps covering keys [64 H, 64 H + 64) of the tile. P comes from
 // TMEM (8 columns per k-step), V from shared memory (MN-major, PV_ROWS rows per k-step).
 template <class C, int H>
@@ -374,6 +398,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // s_free[b] (three-buffer mode): the PV that read S buffer b has completed, so b can take a new S.
   __shared__ __align__(8) uint64_t bar_s_full[C::N_SBAR], bar_p_half[C::N_SBAR][2], bar_o_done[C::N_OBAR], bar_o_full[C::NQ];
   __shared__ __align__(8) uint64_t bar_s_free[C::S3 ? 3 : 1];
+  // s_read[q] (P in shared memory): the softmax warps of Q tile q have loaded S from TMEM.
+  __shared__ __align__(8) uint64_t bar_s_read[C::NQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
 
@@ -387,7 +413,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (C::SPLIT || (kDense && p.tail_mode == 1)) griddep_launch_dependents();
   const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
-  const uint32_t sKV = smem_base + C::Q_BYTES;
+  const uint32_t sP = smem_base + C::Q_BYTES;   // P tiles (e4m3, two Q tiles); empty otherwise
+  const uint32_t sKV = sP + C::P_BYTES;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
 
   if (tid == 0) {
@@ -403,6 +430,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if constexpr (C::S3)
       for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&bar_s_free[i]), 1);
+    if constexpr (C::PSMEM)
+      for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_s_read[i]), 4);
     for (int i = 0; i < C::N_SBAR; ++i) {
       mbar_init(smem_addr(&bar_s_full[i]), 1);
       mbar_init(smem_addr(&bar_p_half[i][0]), 128);
@@ -605,7 +634,69 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
         return true;
       };
-      if constexpr (C::S3) {
+      if constexpr (C::PSMEM) {
+        // P in shared memory: S_{j+1} goes into this tile's S buffer as soon as the softmax has
+        // loaded S_j (s_read), in this issuer's turn, before PV_j. PV_j reads P_j from shared
+        // memory; its completion (o_done) lets the softmax overwrite P and rescale O.
+        uint32_t sr_cnt = 0;         // S loads of this Q tile's softmax waited for
+        bool read_pending = false;   // an S was issued whose load has not been waited for
+        // Before an S goes into this tile's buffer, the softmax must have loaded the one before.
+        auto wait_read = [&]() -> bool {
+          if (!read_pending) return true;
+          if (!mbar_wait(smem_addr(&bar_s_read[myq]), sr_cnt & 1, ctl, SITE_S_FULL)) return false;
+          ++sr_cnt;
+          read_pending = false;
+          return true;
+        };
+        for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+          const TileCoord tc = decode_tile<C>(t, p);
+          const int n = kv_tiles_for<C>(tc, myq, p);
+          int nmax = 0;
+          for (int qt = 0; qt < C::NQ; ++qt) {
+            const int nq = kv_tiles_for<C>(tc, qt, p);
+            nmax = nq > nmax ? nq : nmax;
+          }
+          if (C::VARLEN && nmax == 0) continue;
+          if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
+          ++nq_loads;
+          const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
+          if (!wait_kv(base)) { ok = false; break; }
+          if (n > 0 && !wait_read()) { ok = false; break; }
+          if (!s_turn(n > 0, sKV + (base % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+          read_pending = read_pending || n > 0;
+          release(&bar_kv_empty[base % C::NS], n > 0);
+          if (nmax == 1) release(&bar_q_empty, n > 0);
+          for (int j = 0; ok && j < nmax; ++j) {
+            if (j + 1 < nmax) {
+              const uint32_t pos_k = base + 2 * (j + 1);
+              if (!wait_kv(pos_k)) { ok = false; break; }
+              if (j + 1 < n && !wait_read()) { ok = false; break; }
+              if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+              read_pending = read_pending || j + 1 < n;
+              release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
+              if (j + 2 == nmax) release(&bar_q_empty, n > 0);
+            }
+            const uint32_t pos_v = base + 2 * j + 1;
+            if (!wait_kv(pos_v)) { ok = false; break; }
+            if (j < n) {
+              const uint32_t par = p_cnt & 1;
+              const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
+              const uint32_t a_p = sP + myq * C::TILE_BYTES;
+              if (!mbar_wait(smem_addr(&bar_p_half[myq][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv_half_ss<C, 0>(d_o, a_p, b_v, j > 0);
+              if (!mbar_wait(smem_addr(&bar_p_half[myq][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
+              tc_fence_after();
+              issue_pv_half_ss<C, 1>(d_o, a_p, b_v, true);
+              ++p_cnt;
+              tc_commit(smem_addr(&bar_o_done[myq]));
+              if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
+            }
+            release(&bar_kv_empty[pos_v % C::NS], j < n);
+          }
+          ring = base + 2 * nmax;
+        }
+      } else if constexpr (C::S3) {
         // Three S buffers: the S issuer warp issues every S; this warp issues its Q tile's PVs.
         // PV_j reads P_j from S buffer k % 3 (k: S number of S_j); its completion frees that
         // buffer (s_free) and is signalled on o_done for rescales. Barriers of this tile's g-th S
@@ -915,6 +1006,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         reg_fence32(sr + 32);
         reg_fence32(sr + 64);
         reg_fence32(sr + 96);
+        if constexpr (C::PSMEM) {
+          // S is in registers: the issuer may put S_{j+1} into this buffer now.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&bar_s_read[qt]));
+        }
         if (r == 0) ATTN_TRACE(5, qt, j);
         float x[128];
 #pragma unroll
@@ -960,10 +1057,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         };
         auto store_half = [&](int h, const uint32_t* pk) {
-          if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
-          else tmem_st_32cols(tS + h * 32, pk);
-          tmem_st_wait();
-          tc_fence_before();
+          if constexpr (C::PSMEM) {
+            // Row r of this tile's P in shared memory: 128 bytes, 16-byte piece c at c ^ (r % 8)
+            // (128-byte swizzle, the layout a TMA copy of a Q tile leaves).
+            const uint32_t row = sP + qt * C::TILE_BYTES + r * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              st_shared_v4(row + ((uint32_t)((h * 4 + i) ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2],
+                           pk[4 * i + 3]);
+            fence_proxy_async_smem();
+          } else {
+            if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
+            else tmem_st_32cols(tS + h * 32, pk);
+            tmem_st_wait();
+            tc_fence_before();
+          }
           mbar_arrive(smem_addr(&bar_p_half[buf][h]));
           if (r == 0) ATTN_TRACE(7 + h, qt, j);
         };
@@ -1002,6 +1110,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
         }
         if (r == 0) ATTN_TRACE(6, qt, j);
+        if constexpr (C::PSMEM) {
+          // S_j was issued before PV_{j-1}: wait for that PV before P_j overwrites P_{j-1} in
+          // shared memory (and before any rescale of O).
+          if (j > 0) {
+            w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          }
+        }
         float alpha = 1.0f;
         bool rescale = false;
         if (m_tile > m + 8.0f) {
