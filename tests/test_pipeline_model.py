@@ -1,11 +1,12 @@
-"""CPU checks of the d = 64 forward kernel's synchronisation protocol (three rotating S buffers,
-a dedicated S-issuer warp), on the executable model in pipeline_model.py.
+"""CPU checks of the forward kernel's synchronisation protocols on the executable models in
+pipeline_model.py: d = 64 (three rotating S buffers, a dedicated S-issuer warp) and e4m3 with P
+in shared memory.
 
 The protocol as built (three barriers per Q tile) passes random schedules. Each check below it
 shows the model failing when one piece of the protocol is removed, so the passing run means
 something.
 """
-from pipeline_model import sweep
+from pipeline_model import sweep, sweep_psmem
 
 
 def test_protocol_as_built_passes_random_schedules():
@@ -28,3 +29,19 @@ def test_missing_buffer_free_wait_is_caught():
 def test_missing_rescale_wait_is_caught():
     failure = sweep(100, case_seed=4, M=3, skip_rescale_wait=True)
     assert failure is not None and "rescaled" in failure
+
+
+def test_psmem_protocol_as_built_passes_random_schedules():
+    assert sweep_psmem(400, case_seed=5) is None
+
+
+def test_psmem_missing_read_wait_is_caught():
+    # S_{j+1} must wait until the softmax has loaded S_j from the tile's one TMEM buffer
+    failure = sweep_psmem(100, case_seed=6, skip_read_wait=True)
+    assert failure is not None and "before the softmax loaded it" in failure
+
+
+def test_psmem_missing_pv_wait_is_caught():
+    # P_j must wait for PV_{j-1}, which reads the same shared-memory P tile (and O for rescales)
+    failure = sweep_psmem(100, case_seed=7, skip_pv_wait=True)
+    assert failure is not None and ("before its PV read it" in failure or "rescaled" in failure)
