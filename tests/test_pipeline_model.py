@@ -2,9 +2,9 @@
 pipeline_model.py: d = 64 (three rotating S buffers, a dedicated S-issuer warp) and e4m3 with P
 in shared memory.
 
-The protocol as built (three barriers per Q tile) passes random schedules. Each check below it
-shows the model failing when one piece of the protocol is removed, so the passing run means
-something.
+Both protocols as built (d = 64 with three barriers per Q tile) pass random schedules. The
+other checks show each model failing when one piece of its protocol is removed, so the passing
+runs mean something.
 """
 from pipeline_model import sweep, sweep_psmem
 
