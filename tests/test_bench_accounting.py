@@ -1,0 +1,23 @@
+"""bench.py's kernel-launch accounting (the `gpu_launches` key) against the library's own launch
+rules, on the CPU: a non-causal forward whose last wave is halved makes two launches, split-KV
+decode two (forward + combine), the block-scaled chain five quantiser launches plus the forward."""
+import bench
+from exact_attention_72_gb300 import binding, inputs
+
+
+def test_forward_launch_counts_follow_the_halving_rule():
+    for w in inputs.WORKLOADS.values():
+        halved = binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) > 0
+        assert bench.launches_per_step(w) == (2 if halved else 1), w.name
+    assert bench.launches_per_step(inputs.WORKLOADS["noncausal_bf16_n4096_d256"]) == 2
+    assert bench.launches_per_step(inputs.WORKLOADS["fp8_noncausal_n8192_d128"]) == 2
+    assert bench.launches_per_step(inputs.WORKLOADS["causal_gqa_bf16_n8192_d128"]) == 1
+    assert bench.launches_per_step(inputs.WORKLOADS["noncausal_bf16_n16384_d64"]) == 1
+
+
+def test_decode_and_block_scaled_counts():
+    for w in inputs.DECODE_WORKLOADS.values():
+        assert bench.launches_per_step(w) == 2
+    w = inputs.FP8_BLOCK_WORKLOADS["fp8_block_hadamard_noncausal_n8192_d128"]
+    # q and k quantised in one launch each, v in three (maxima, codes, descales), forward in two
+    assert bench.launches_per_step(w) == 1 + 1 + 3 + 2
