@@ -10,7 +10,8 @@ bf16 by default). Prints ONE JSON line on rank 0:
   e2e        the same metric through attn_fwd_host (pinned host buffers, H2D of q/k/v and D2H
              of o/lse inside the timed region);
   roofline   tensor-core bound: achieved TFLOP/s of the attention kernel against the measured
-             dense bf16 peak (e4m3: x2 nominal ratio);
+             dense bf16 peak (e4m3: x2 nominal ratio). A non-causal call whose last wave is halved
+             along the keys runs the kernel as two launches; the step time covers both;
   cpu_baseline  the fp64 oracle on a bounded sample, on this host's cores (rank 0, N=1 only);
   clocks     nvidia-smi SM clock samples taken during the timed region.
 --impl reference times the oracle itself (CPU) on bounded samples of the same workload.
