@@ -198,3 +198,11 @@ def test_halved_tail_rule(lib):
     assert f(1, 2, 256, 64, False) == 0
     assert f(0, 8, 4096, 128, False) == 0
     assert f(1, 8, 4096, 96, False) == 0
+    # the half-the-SMs boundary (d = 256: 128-row tiles): 4 heads x 19 blocks = 76 tiles are
+    # halved, 4 x 20 = 80 are not; 16 key tiles is the shortest range that is cut
+    assert f(1, 4, 2432, 256, False) == 76
+    assert f(1, 4, 2560, 256, False) == 0
+    assert f(1, 4, 2048, 256, False) == 64
+    assert f(1, 4, 1920, 256, False) == 0
+    # a second wave of exactly 76 tiles (152 + 76 = 228 = 12 heads x 19 blocks) is halved
+    assert f(1, 12, 2432, 256, False) == 76
