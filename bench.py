@@ -6,7 +6,10 @@ bf16 by default). Prints ONE JSON line on rank 0:
   value      device-timed TFLOP/s (4*B*H*N^2*d, halved for causal), summed over ranks, with
              inputs resident in HBM; CUDA events around each launch on the launching stream,
              L2 flushed (256 MiB write, then a 256 MiB read that drains the dirty lines) before
-             every step, outside the events;
+             every step, outside the events. The timed region is --repeats (default 5) repeats
+             of exactly --steps steps, each bracketed by a barrier and a synchronize; value,
+             ms_per_step and the roofline come from the median repeat, and every repeat's
+             ms per step is listed;
   e2e        the same metric through attn_fwd_host (pinned host buffers, H2D of q/k/v and D2H
              of o/lse inside the timed region);
   roofline   tensor-core bound: achieved TFLOP/s of the attention kernel against the measured
@@ -59,6 +62,8 @@ def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--repeats", type=int, default=5,
+                    help="timed repeats of --steps steps each; the reported figures are the median repeat's")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None, help="name from exact_attention_72_gb300.inputs.WORKLOADS")
@@ -112,7 +117,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError as e:
             self.error = str(e)
@@ -214,6 +219,38 @@ def credited_flops(w, rows, N):
     if w.causal:
         return 4.0 * w.d * sum(int(r) + 1 for r in rows)
     return 4.0 * w.d * N * len(rows)
+
+
+def timed_repeats(args, dist, stream, flush, step, with_mid=False):
+    """args.repeats repeats of exactly args.steps timed steps. Each repeat is bracketed by a
+    barrier and a synchronize on both sides; every step is preceded by an L2 flush outside its
+    CUDA events. step(i, mid) runs step i and, when with_mid is set, records the event `mid`
+    inside it. Returns (durations [R][K] in ms, start-to-mid durations or None, per-repeat
+    totals taken as the max over ranks, index of the median repeat, host start, host end)."""
+    import torch
+    R, K = max(1, args.repeats), args.steps
+    reps = []
+    t_host0 = None
+    for r in range(R):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 if with_mid else 2)] for _ in range(K)]
+        barrier(dist)
+        torch.cuda.synchronize()
+        if t_host0 is None:
+            t_host0 = time.time()
+        for i in range(K):
+            flush(i)
+            ev[i][0].record(stream)
+            step(i, ev[i][2] if with_mid else None)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        reps.append(ev)
+    t_host1 = time.time()
+    durs = [[e[0].elapsed_time(e[1]) for e in ev] for ev in reps]
+    mids = [[e[0].elapsed_time(e[2]) for e in ev] for ev in reps] if with_mid else None
+    totals = [max_over_ranks(dist, sum(d)) for d in durs]
+    med = sorted(range(R), key=lambda r: totals[r])[R // 2]
+    return durs, mids, totals, med, t_host0, t_host1
 
 
 def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
@@ -350,17 +387,15 @@ def run_ours(args, w, x):
         dq = torch.empty((w.B, w.H, -(-w.N // 128)), dtype=torch.float32, device=dev)
         dk = torch.empty((w.B, w.Hkv, -(-w.N // 64)), dtype=torch.float32, device=dev)
         dv = torch.empty((w.B, w.Hkv, 1), dtype=torch.float32, device=dev)
-    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)] if block else None
-
-    def step(i=None):
+    def step(i=None, mid=None):
         if decode:
             binding.attn_fwd_splitkv(q, k, v, w.splits, scale=w.scale, workspace=ws, out=o, lse=lse, **kw)
         elif block:
             binding.quantize_e4m3(q, 128, signs, out=q8, descale=dq)
             binding.quantize_e4m3(k, 64, signs, out=k8, descale=dk)
             binding.quantize_e4m3(v, w.N, out=v8, descale=dv)
-            if i is not None:
-                mids[i].record(stream)
+            if mid is not None:
+                mid.record(stream)
             binding.attn_fwd_fp8_blockscaled(q8, k8, v8, w.causal, dq, dk, dv.view(w.B, w.Hkv), scale=w.scale,
                                              out=o, lse=lse)
         else:
@@ -376,27 +411,16 @@ def run_ours(args, w, x):
 
     sampler = ClockSampler(local)
     sampler.wait_first()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize()
-    t_host0 = time.time()
-    for i in range(args.steps):
-        flush(i)
-        starts[i].record(stream)
-        step(i)
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    t_host1 = time.time()
+    durs_all, mids_all, totals, med, t_host0, t_host1 = timed_repeats(args, dist, stream, flush, step,
+                                                                     with_mid=block)
     time.sleep(0.12)
     sampler.stop()
-    durs = [s.elapsed_time(e) for s, e in zip(starts, ends)]   # ms per step
+    durs = durs_all[med]   # ms per step, median repeat
     prepass = None
     if block:
         # the attention launch alone (the roofline's kernel), and the quantisation before it
-        pre = [s.elapsed_time(m) for s, m in zip(starts, mids)]
-        durs_attn = [m.elapsed_time(e) for m, e in zip(mids, ends)]
+        pre = mids_all[med]
+        durs_attn = [d_ - m_ for d_, m_ in zip(durs, pre)]
         pre_ms = statistics.fmean(pre)
         qkv_bytes = (w.B * w.N * (w.H + 2 * w.Hkv) * w.d) * 3 + 4 * (dq.numel() + dk.numel() + dv.numel())
         hbm, hbm_src = hbm_peak()
@@ -406,8 +430,7 @@ def run_ours(args, w, x):
     st, detail = binding.attn_get_status()
     if st != binding.ATTN_OK:
         raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
-    local_ms = sum(durs)
-    total_ms = max_over_ranks(dist, local_ms)
+    total_ms = totals[med]
     value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
     kdurs = durs_attn if block else durs
     mean_ms = statistics.fmean(kdurs)
@@ -447,9 +470,10 @@ def run_ours(args, w, x):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+            "repeats": len(totals), "repeat_ms_per_step": [t / args.steps for t in totals],
             "config": config_of(w),
             "roofline": roofline,
-            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * launches_per_step(w), "clocks": clocks,
+            "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": args.steps * len(totals) * launches_per_step(w), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -622,7 +646,7 @@ def run_bwd_ours(args, w, x):
     stream = torch.cuda.current_stream()
     flops = BWD_FLOP_FACTOR * w.flops
 
-    def step():
+    def step(i=None, mid=None):
         binding.attn_bwd(q, k, v, o, lse, do, w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
 
     for i in range(max(args.warmup, 0)):
@@ -634,26 +658,14 @@ def run_bwd_ours(args, w, x):
         raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
     sampler = ClockSampler(local)
     sampler.wait_first()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize()
-    t_host0 = time.time()
-    for i in range(args.steps):
-        flush(i)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    t_host1 = time.time()
+    durs_all, _, totals, med, t_host0, t_host1 = timed_repeats(args, dist, stream, flush, step)
     time.sleep(0.12)
     sampler.stop()
-    durs = [a_.elapsed_time(b_) for a_, b_ in zip(starts, ends)]
+    durs = durs_all[med]
     st, detail = binding.attn_get_status()
     if st != binding.ATTN_OK:
         raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
-    total_ms = max_over_ranks(dist, sum(durs))
+    total_ms = totals[med]
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     mean_ms = statistics.fmean(durs)
     achieved = flops / (mean_ms * 1e-3) / 1e12
@@ -704,8 +716,9 @@ def run_bwd_ours(args, w, x):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "repeats": len(totals), "repeat_ms_per_step": [t / args.steps for t in totals],
             "config": bwd_config(w), "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": args.steps * 3, "clocks": clocks,
+            "gpu_launches": args.steps * len(totals) * 3, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -807,7 +820,7 @@ def run_varlen_ours(args, w, x):
     plan = binding.attn_varlen_plan(cu_q, cu_k, w.H, w.total_q, w.total_k, w.d, w.causal)
     p1.record(stream)
 
-    def step():
+    def step(i=None, mid=None):
         binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, plan, w.causal, scale=w.scale, out=o, lse=lse, **kw)
 
     for i in range(max(args.warmup, 0)):
@@ -820,26 +833,14 @@ def run_varlen_ours(args, w, x):
         raise RuntimeError(f"device status {st} ({detail:#x}) after warm-up")
     sampler = ClockSampler(local)
     sampler.wait_first()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    barrier(dist)
-    torch.cuda.synchronize()
-    t_host0 = time.time()
-    for i in range(args.steps):
-        flush(i)
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    t_host1 = time.time()
+    durs_all, _, totals, med, t_host0, t_host1 = timed_repeats(args, dist, stream, flush, step)
     time.sleep(0.12)
     sampler.stop()
-    durs = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    durs = durs_all[med]
     st, detail = binding.attn_get_status()
     if st != binding.ATTN_OK:
         raise RuntimeError(f"device status {st} ({detail:#x}) after the timed region")
-    total_ms = max_over_ranks(dist, sum(durs))
+    total_ms = totals[med]
     value = w.flops * args.steps * world / (total_ms * 1e-3) / 1e12
     mean_ms = statistics.fmean(durs)
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
@@ -890,8 +891,9 @@ def run_varlen_ours(args, w, x):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3" if fp8 else "bf16", "data": "synthetic",
+            "repeats": len(totals), "repeat_ms_per_step": [t / args.steps for t in totals],
             "config": varlen_config(w), "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": args.steps, "clocks": clocks,
+            "gpu_launches": args.steps * len(totals), "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -76,7 +76,9 @@ def lib() -> ctypes.CDLL:
     L.attn_fwd_host_workspace_bytes.restype = sz
     L.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
     L.attn_get_status.restype = i
-    L.attn_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.attn_get_status.argtypes = [vp]
+    L.attn_get_status_detail.restype = i
+    L.attn_get_status_detail.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.attn_clear_status.restype = i
     L.attn_clear_status.argtypes = []
     L.attn_status_string.restype = ctypes.c_char_p
@@ -451,9 +453,9 @@ def attn_fwd_host_workspace_bytes(B: int, H: int, Hkv: int, N: int, d: int, dtyp
 
 
 def attn_get_status(stream=None) -> tuple[int, int]:
-    """(status, raw status word) after synchronizing ``stream``."""
+    """(status, raw status word) after synchronizing ``stream`` (C: attn_get_status_detail)."""
     detail = ctypes.c_uint32(0)
-    st = lib().attn_get_status(_stream_handle(stream), ctypes.byref(detail))
+    st = lib().attn_get_status_detail(_stream_handle(stream), ctypes.byref(detail))
     return st, detail.value
 
 

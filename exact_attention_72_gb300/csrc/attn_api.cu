@@ -11,6 +11,7 @@
 #include <cuda_runtime.h>
 
 #include "attn.h"
+#include "context_id.h"
 #include "launch.h"
 
 // First failure recorded by any kernel of this library on the device (0 = none).
@@ -46,14 +47,17 @@ EncodeTiledFn encode_fn() {
 
 constexpr int kMaxChunks = 10;   // eight even chunks, the first and last of them halved
 
+// Per-device state, valid for one CUDA context (see context_id.h): the SM count, the device
+// address of the status word and the host-buffer pipeline's streams and events. When the current
+// context is not the one the state was made for (first use, or a new primary context after
+// cudaDeviceReset) it is looked up again; a lookup that fails is not cached, so a later call retries.
 struct DeviceInfo {
-  std::once_flag once;
+  std::mutex mu;
+  unsigned long long ctx = 0;   // context id the fields below belong to (0: none yet)
   int num_sms = 0;
   uint32_t* status = nullptr;
-  bool ok = false;
-  // Host-buffer pipeline (attn_fwd_host): created once per device on first use.
-  std::once_flag pipe_once;
-  bool pipe_ok = false;
+  // Host-buffer pipeline (attn_fwd_host): created on first use in each context.
+  unsigned long long pipe_ctx = 0;
   cudaStream_t s_in = nullptr, s_out = nullptr, s_comp[2] = {nullptr, nullptr};
   cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[kMaxChunks] = {}, ev_k[kMaxChunks] = {};
   std::mutex pipe_mutex;   // one host-buffer call at a time per device (shared streams/events)
@@ -64,30 +68,38 @@ DeviceInfo* device_info() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceInfo* di = &g_dev[dev];
-  std::call_once(di->once, [di, dev] {
-    void* p = nullptr;
-    di->ok = cudaDeviceGetAttribute(&di->num_sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
-             cudaGetSymbolAddress(&p, g_attn_status) == cudaSuccess;
-    di->status = static_cast<uint32_t*>(p);
-  });
-  return di->ok ? di : nullptr;
+  const unsigned long long id = gb300::current_context_id();
+  std::lock_guard<std::mutex> lock(di->mu);
+  if (id != 0 && id == di->ctx) return di;
+  int sms = 0;
+  void* p = nullptr;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaGetSymbolAddress(&p, g_attn_status) != cudaSuccess)
+    return nullptr;
+  di->num_sms = sms;
+  di->status = static_cast<uint32_t*>(p);
+  // The lookup has initialised the context if it did not exist yet; key the state on it. (With no
+  // readable id the state is looked up again on every call.)
+  di->ctx = gb300::current_context_id();
+  return di;
 }
 
+// Streams and events of the host-buffer pipeline for the current context; called with
+// di->pipe_mutex held. Handles made for an earlier context died with it and are not destroyed.
 bool pipeline_ready(DeviceInfo* di) {
-  std::call_once(di->pipe_once, [di] {
-    bool ok = true;
-    ok = ok && cudaStreamCreateWithFlags(&di->s_in, cudaStreamNonBlocking) == cudaSuccess;
-    ok = ok && cudaStreamCreateWithFlags(&di->s_out, cudaStreamNonBlocking) == cudaSuccess;
-    for (int i = 0; i < 2; ++i) ok = ok && cudaStreamCreateWithFlags(&di->s_comp[i], cudaStreamNonBlocking) == cudaSuccess;
-    ok = ok && cudaEventCreateWithFlags(&di->ev_start, cudaEventDisableTiming) == cudaSuccess;
-    ok = ok && cudaEventCreateWithFlags(&di->ev_end, cudaEventDisableTiming) == cudaSuccess;
-    for (int i = 0; i < kMaxChunks; ++i) {
-      ok = ok && cudaEventCreateWithFlags(&di->ev_in[i], cudaEventDisableTiming) == cudaSuccess;
-      ok = ok && cudaEventCreateWithFlags(&di->ev_k[i], cudaEventDisableTiming) == cudaSuccess;
-    }
-    di->pipe_ok = ok;
-  });
-  return di->pipe_ok;
+  if (di->ctx != 0 && di->pipe_ctx == di->ctx) return true;
+  bool ok = true;
+  ok = ok && cudaStreamCreateWithFlags(&di->s_in, cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaStreamCreateWithFlags(&di->s_out, cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; i < 2; ++i) ok = ok && cudaStreamCreateWithFlags(&di->s_comp[i], cudaStreamNonBlocking) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&di->ev_start, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&di->ev_end, cudaEventDisableTiming) == cudaSuccess;
+  for (int i = 0; i < kMaxChunks; ++i) {
+    ok = ok && cudaEventCreateWithFlags(&di->ev_in[i], cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&di->ev_k[i], cudaEventDisableTiming) == cudaSuccess;
+  }
+  di->pipe_ctx = ok ? di->ctx : 0;
+  return ok;
 }
 
 // attn_fwd_host work split: chunks of whole batches (B >= kHostChunks) or, for fewer batches, one
@@ -245,9 +257,9 @@ attn_status_t check_shape(int B, int H, int Hkv, int N, int d, float scale, attn
   if (H % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP8_E4M3) return ATTN_ERR_INVALID_ARG;
-  // The row max is taken on unscaled scores (needs scale > 0); scale == 0 would turn masked
-  // entries into NaN (-inf * 0).
-  if (scale <= 0.0f) return ATTN_ERR_UNSUPPORTED;
+  // Masked scores are -inf before scaling; scale == 0 would turn them into NaN (-inf * 0). A
+  // negative scale is run as |scale| times -Q K^T (the MMA negates Q).
+  if (scale == 0.0f) return ATTN_ERR_UNSUPPORTED;
   if (!supported_dim(d, dtype)) return ATTN_ERR_UNSUPPORTED;
   const long long rows = gb300::rows_per_work_tile(d);
   const long long tiles = (long long)B * H * ((N + rows - 1) / rows);
@@ -338,7 +350,8 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   p.H = H;
   p.Hkv = Hkv;
   p.N = N;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.qk_negate = scale < 0.0f ? gb300::kIdescNegateA : 0u;
   p.n_mb = (N + rows - 1) / rows;
   p.n_tiles = B * H * p.n_mb;
   p.Nk = N;
@@ -430,8 +443,9 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   if (!aligned(workspace, 256) || workspace_bytes < attn_fwd_host_workspace_bytes(B, H, Hkv, N, d, dtype))
     return ATTN_ERR_INVALID_ARG;
   DeviceInfo* di = device_info();
-  if (!di || !pipeline_ready(di)) return ATTN_ERR_CUDA;
+  if (!di) return ATTN_ERR_CUDA;
   std::lock_guard<std::mutex> lock(di->pipe_mutex);
+  if (!pipeline_ready(di)) return ATTN_ERR_CUDA;
   const size_t elt = fp8 ? 1 : 2;
   const int G = H / Hkv;
   HostChunk ch[kMaxChunks];
@@ -588,7 +602,8 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   p.n_kvt = n_kvt;
   p.part_o = part_o;
   p.part_lse = part_lse;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.qk_negate = scale < 0.0f ? gb300::kIdescNegateA : 0u;
   p.n_mb = (int)(((long long)Nq * G + rows - 1) / rows);
   const long long tiles = (long long)B * Hkv * S * p.n_mb;
   if (tiles >= (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
@@ -680,7 +695,8 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
   p.N = total_q;
   p.Nk = total_k;
   p.G = H / Hkv;
-  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
+  p.qk_negate = scale < 0.0f ? gb300::kIdescNegateA : 0u;
   // Launch bound and read limit: the tiles a valid plan can hold, and no more than the buffer has.
   const size_t held = (plan_bytes - (size_t)gb300::plan_tiles_offset(B) * 4) / 8;
   const long long bound = varlen_tile_bound(B, H, total_q, d);
@@ -828,7 +844,9 @@ attn_status_t attn_quantize_e4m3(const void* x, void* x8, float* descale, int B,
   return gb300::launch_quantize_e4m3(q, stream) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail) {
+attn_status_t attn_get_status(cudaStream_t stream) { return attn_get_status_detail(stream, nullptr); }
+
+attn_status_t attn_get_status_detail(cudaStream_t stream, uint32_t* detail) {
   if (detail) *detail = 0;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return ATTN_ERR_CUDA;
   uint32_t v = 0;

@@ -53,7 +53,11 @@ struct AttnParams {
   const float* descale_v;
   int dq_sb, dq_sh, dq_sm, dk_sb, dk_sh, dk_sn, dv_sb, dv_sh;
   int B, H, Hkv, N;         // N: query rows per (batch, head) (prefill: also the key count)
-  float scale_log2;         // scale * log2(e)
+  float scale_log2;         // |scale| * log2(e)
+  // 0, or the instruction-descriptor bit that negates the A operand (Q) of S = Q K^T: with a
+  // negative scale the kernel computes S = -Q K^T and scales it by |scale|, so every score the
+  // softmax sees is scale * q . k and its row maximum is still a maximum.
+  uint32_t qk_negate;
   int n_mb;                 // query blocks (NQ x 128 rows) per (batch, head) / per (batch, kv head)
   int n_tiles;              // work tiles in the launch
   // Split-KV (decode) mode: Nk keys in n_kvt tiles of 128, split into n_splits ranges; query
@@ -176,7 +180,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
     // Plan entry: (sequence, head << 16 | query block), longest first.
     const int2 e = reinterpret_cast<const int2*>(p.plan + p.plan[5])[t];
     c.b = e.x;
-    c.h = e.y >> 16;
+    c.h = (int)((uint32_t)e.y >> 16);
     c.mb = e.y & 0xFFFF;
     c.bo = 0;
     const bool b_ok = c.b >= 0 && c.b < p.B;
@@ -186,7 +190,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
     c.nk = b_ok ? __ldg(p.cu_k + c.b + 1) - c.k_base : 0;
     // Rows outside the packed tensors (offsets that changed since the plan was built) make the
     // tile empty for every role, so nothing is read or written out of bounds.
-    if (!(b_ok && c.h < p.H && c.q_base >= 0 && c.nq >= 0 && c.q_base + c.nq <= p.N && c.k_base >= 0 && c.nk >= 0 &&
+    if (!(b_ok && c.h >= 0 && c.h < p.H && c.q_base >= 0 && c.nq >= 0 && c.q_base + c.nq <= p.N && c.k_base >= 0 && c.nk >= 0 &&
           c.k_base + c.nk <= p.Nk)) {
       atomicCAS(p.status, 0u, kStatusBadPlan);
       c.b = c.h = 0;
@@ -331,19 +335,22 @@ __device__ __forceinline__ int s_buf_idx(int qt, int j) {
 // S = Q K^T for one 128 x 128 tile: KSTEPS_QK MMAs, each reading 32 bytes of every Q and K row.
 // Descriptors are built once; a k-step only adds its byte offset (>> 4) to the start-address
 // field, which cannot carry out because every shared-memory address is below 2^18.
+// idesc: C::IDESC_QK, or (forward with a negative scale) that with the negate-A bit.
 template <class C>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr,
+                                         uint32_t idesc = C::IDESC_QK) {
   const uint64_t a0 = make_sdesc_sw128(a_addr, 16, 1024);
   const uint64_t b0 = make_sdesc_sw128(b_addr, 16, 1024);
 #pragma unroll
   for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
     const uint64_t off = (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
-    mma_f16_or_f8<C::FP8>(d_tmem, a0 + off, b0 + off, C::IDESC_QK, kk > 0 ? 1u : 0u);
+    mma_f16_or_f8<C::FP8>(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// Half H of O += P V with P in shared memory (e4m3, laid out like a Q tile: 128 rows of 128
-// bytes, 128-byte swizzle, 32 bytes per k-step) and V MN-major as below.
+// Half H of O += P V with P in shared memory, laid out like a Q tile (K-major, 128-byte swizzle:
+// each row's keys in 128-byte chunks of CHUNK_BYTES-strided 128-row blocks, 32 bytes per k-step;
+// one chunk per row for e4m3, two for bf16), and V MN-major as below.
 template <class C, int H>
 __device__ __forceinline__ void issue_pv_half_ss(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr,
                                                  bool accumulate_first) {
@@ -354,7 +361,7 @@ __device__ __forceinline__ void issue_pv_half_ss(uint32_t d_tmem, uint32_t a_add
   for (int i = 0; i < KH; ++i) {
     const int kk = H * KH + i;
     const uint32_t acc = (H > 0 || i > 0) ? 1u : (accumulate_first ? 1u : 0u);
-    mma_f16_or_f8<C::FP8>(d_tmem, a0 + (uint64_t)((kk * 32) >> 4),
+    mma_f16_or_f8<C::FP8>(d_tmem, a0 + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
                           b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4), C::IDESC_PV, acc);
   }
 }
@@ -628,7 +635,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++turns;
         if (issue) {
           tc_fence_after();
-          issue_qk<C>(d_s, a_q, k_addr);
+          issue_qk<C>(d_s, a_q, k_addr, C::IDESC_QK | p.qk_negate);
           tc_commit(smem_addr(&bar_s_full[myq]));
         }
         mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
@@ -776,6 +783,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (j + 1 < nmax) {
             const uint32_t pos_k = pos_v + 1;
             if (!wait_kv(pos_k)) { ok = false; break; }
+            ATTN_TRACE(18, myq, j + 1);
             if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
             ATTN_TRACE(14, myq, j + 1);
             release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
@@ -822,7 +830,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               break;
             }
             tc_fence_after();
-            issue_qk<C>(tmem + b * 128u, sQ + qt * C::TILE_BYTES, sKV + (pos_k % C::NS) * C::TILE_BYTES);
+            issue_qk<C>(tmem + b * 128u, sQ + qt * C::TILE_BYTES, sKV + (pos_k % C::NS) * C::TILE_BYTES,
+                        C::IDESC_QK | p.qk_negate);
             const uint32_t gj = (qt ? gb1 : gb0) + j;
             tc_commit(smem_addr(&bar_s_full[3u * qt + gj % 3u]));
           }
@@ -854,7 +863,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       };
       // S_j into S buffer j % 2, then signal the softmax.
       auto qk = [&](int j, uint32_t k_slot) {
-        issue_qk<C>(tmem + s_buf_col<C>(0, j), sQ, sKV + k_slot * C::TILE_BYTES);
+        issue_qk<C>(tmem + s_buf_col<C>(0, j), sQ, sKV + k_slot * C::TILE_BYTES, C::IDESC_QK | p.qk_negate);
         tc_commit(smem_addr(&bar_s_full[s_buf_idx<C>(0, j)]));
       };
       // O += P_j V_j, issued in two halves as the softmax hands P over.
@@ -1058,13 +1067,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         };
         auto store_half = [&](int h, const uint32_t* pk) {
           if constexpr (C::PSMEM) {
-            // Row r of this tile's P in shared memory: 128 bytes, 16-byte piece c at c ^ (r % 8)
-            // (128-byte swizzle, the layout a TMA copy of a Q tile leaves).
-            const uint32_t row = sP + qt * C::TILE_BYTES + r * 128;
+            // Row r of this tile's P in shared memory, the layout a TMA copy of a Q tile leaves: 128
+            // bytes per row and chunk, 16-byte piece c of row r at c ^ (r % 8) (128-byte swizzle).
+            // e4m3: the half's 64 bytes are pieces 4h .. 4h + 3 of the row's one chunk; bf16: the
+            // half's 128 bytes are all eight pieces of chunk h.
+            if constexpr (C::FP8) {
+              const uint32_t row = sP + qt * C::TILE_BYTES + r * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_shared_v4(row + ((uint32_t)((h * 4 + i) ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2],
-                           pk[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                st_shared_v4(row + ((uint32_t)((h * 4 + i) ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1],
+                             pk[4 * i + 2], pk[4 * i + 3]);
+            } else {
+              const uint32_t row = sP + qt * C::TILE_BYTES + h * C::CHUNK_BYTES + r * 128;
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                st_shared_v4(row + ((uint32_t)(i ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2],
+                             pk[4 * i + 3]);
+            }
             fence_proxy_async_smem();
           } else {
             if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
@@ -1078,6 +1097,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t pk[PKN];
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
+        if (r == 0) ATTN_TRACE(16, qt, j);
         // Row max: eight independent chains of 3-input max (per 64-key half for fp8, whose halves
         // may carry different K descales; the scales are positive, so max commutes with them).
         float m_tile;
@@ -1160,6 +1180,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         store_half(0, pk);
         exp_half(1, f2_pack(-m, -m), pk, acc0, acc1);
+        if (r == 0) ATTN_TRACE(17, qt, j);
         store_half(1, pk);
         float l0, l1, l2, l3;
         f2_unpack(acc0, l0, l1);

@@ -198,6 +198,8 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, int M, int
   return (1u << 4) | (ab_format << 7) | (ab_format << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Bit 13 of the instruction descriptor negates the A operand (floating-point kinds).
+constexpr uint32_t kIdescNegateA = 1u << 13;
 constexpr uint32_t kFmtBF16 = 1;
 constexpr uint32_t kFmtE4M3 = 0;
 

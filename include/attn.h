@@ -54,8 +54,11 @@ typedef enum {
  *   lse    [B, H, N]       float32 output, LSE_i = ln sum_j exp(scale * q_i . k_j) over the
  *                          keys row i may see (all keys, or j <= i when causal)
  *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16, d == 128 for fp8.
- *   scale  finite float > 0 multiplying the raw dot products (usually 1/sqrt(d)); it does not
- *          include the fp8 descales. scale <= 0 returns ATTN_ERR_UNSUPPORTED.
+ *   scale  finite, nonzero float multiplying the raw dot products (usually 1/sqrt(d)); it does
+ *          not include the fp8 descales. A negative scale is allowed (the kernel computes
+ *          |scale| * (-Q) K^T, so the softmax's running maximum is taken over the scaled scores
+ *          either way). scale == 0 returns ATTN_ERR_UNSUPPORTED: masked scores are -inf before
+ *          scaling, and 0 * -inf has no value.
  *   causal nonzero: key j is visible to query i iff j <= i (top-left aligned).
  *   descale_q/k/v  fp8 only: DEVICE pointers to one float each; the value the kernel uses
  *          for an element x8 is x8 * descale. Ignored (may be NULL) for bf16.
@@ -308,10 +311,13 @@ int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d);
  * every GPU that loads the library holds it until the process exits). The pages have no
  * counterpart to this entry point: it exists for callers of this library.
  *   Arguments, layouts and errors as attn_fwd_splitkv, without workspace arguments. Returns
- *   ATTN_ERR_UNSUPPORTED when attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits) exceeds
- *   ATTN_SPLITKV_STATIC_SCRATCH_BYTES. Allocates nothing, on the device or elsewhere.
- *   The first call on a device looks up the array's device address (cudaGetSymbolAddress with
- *   that device current); make that first call before any stream capture.
+ *   ATTN_ERR_UNSUPPORTED when attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, S) exceeds
+ *   ATTN_SPLITKV_STATIC_SCRATCH_BYTES, where S = min(num_splits, ceil(Nk / 128)) is the number of
+ *   splits that run. Allocates nothing, on the device or elsewhere.
+ *   The first call in a CUDA context looks up the array's device address (cudaGetSymbolAddress
+ *   with the device current) and keeps it for that context; make that first call before any
+ *   stream capture. cudaDeviceReset ends the context: the first call after it, in the new
+ *   context, looks the address up again (and should again come before any stream capture).
  *   All calls share the one array, and each call overwrites it: calls whose kernels overlap on
  *   the GPU (different streams, or different host threads) race and corrupt each other's results.
  *   Serialize them, e.g. by using one stream. Nothing in the array needs to start at zero: each
@@ -328,10 +334,15 @@ attn_status_t attn_fwd_splitkv_static(const void* q, const void* k, const void* 
  * library on the current device gave up a bounded wait since the last attn_clear_status,
  * ATTN_ERR_INVALID_ARG if a varlen forward was handed a plan that does not match it (or that the
  * plan builder marked invalid), ATTN_ERR_CUDA if the synchronization failed, else ATTN_OK.
- * `detail` (may be NULL) receives the raw status word (0, 0x40000000 | wait-site code, or
- * 0x2000000C for a rejected plan).
  */
-attn_status_t attn_get_status(cudaStream_t stream, uint32_t* detail);
+attn_status_t attn_get_status(cudaStream_t stream);
+
+/*
+ * attn_get_status_detail — attn_get_status that also stores the raw device status word in
+ * `detail` (may be NULL): 0, 0x40000000 | the code of the wait site that gave up, or 0x2000000C
+ * for a rejected varlen plan. 0 is stored when the synchronization fails.
+ */
+attn_status_t attn_get_status_detail(cudaStream_t stream, uint32_t* detail);
 
 /* attn_clear_status — resets the current device's status word to 0 (synchronous). */
 attn_status_t attn_clear_status(void);

@@ -27,12 +27,12 @@ def to_device(x: inputs.AttnInputs, device="cuda"):
     return q, k, v, desc
 
 
-def run_cuda(w: inputs.Workload, x: inputs.AttnInputs):
+def run_cuda(w: inputs.Workload, x: inputs.AttnInputs, scale=None):
     q, k, v, desc = to_device(x)
     kw = {}
     if desc is not None:
         kw = dict(descale_q=desc[0], descale_k=desc[1], descale_v=desc[2])
-    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, **kw)
+    o, lse = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale if scale is None else scale, **kw)
     st, detail = binding.attn_get_status()
     assert st == binding.ATTN_OK, f"device status {st} detail {detail:#x}"
     return o, lse
@@ -45,14 +45,17 @@ def head_f64(t: torch.Tensor, b: int, h: int, descale: float) -> np.ndarray:
     return a
 
 
-def oracle_heads(w: inputs.Workload, x: inputs.AttnInputs, heads, rows=None):
-    """Oracle O/LSE for the listed (b, h) heads; returns {(b, h): (O [rows, d], LSE [rows])}."""
+def oracle_heads(w: inputs.Workload, x: inputs.AttnInputs, heads, rows=None, scale=None):
+    """Oracle O/LSE for the listed (b, h) heads; returns {(b, h): (O [rows, d], LSE [rows])}.
+
+    ``scale`` defaults to the workload's 1/sqrt(d)."""
     out = {}
     g = w.H // w.Hkv
+    sc = w.scale if scale is None else scale
     for (b, h) in heads:
         kh = h // g
         out[(b, h)] = oracle.attention_head(head_f64(x.q, b, h, x.descale_q), head_f64(x.k, b, kh, x.descale_k),
-                                            head_f64(x.v, b, kh, x.descale_v), w.scale, w.causal, rows=rows)
+                                            head_f64(x.v, b, kh, x.descale_v), sc, w.causal, rows=rows)
     return out
 
 

@@ -25,8 +25,16 @@ def declared_functions():
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    for n in ("attn_fwd", "attn_fwd_host", "attn_get_status", "attn_status_string"):
+    for n in ("attn_fwd", "attn_fwd_host", "attn_get_status", "attn_get_status_detail", "attn_status_string"):
         assert n in names
+
+
+def test_get_status_has_the_one_argument_form():
+    """attn_get_status takes the stream alone; the raw word comes from attn_get_status_detail."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    assert re.search(r"attn_status_t\s+attn_get_status\s*\(\s*cudaStream_t\s+stream\s*\)\s*;", text)
+    assert re.search(r"attn_status_t\s+attn_get_status_detail\s*\(\s*cudaStream_t\s+stream\s*,\s*uint32_t\s*\*\s*detail\s*\)",
+                     text)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -61,8 +69,7 @@ def test_validation_rejects_bad_arguments(lib):
     assert _call(lib, dtype=7) == INV
     assert _call(lib, d=96) == UNS                        # head dim without an instance
     assert _call(lib, d=64, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # fp8 only for d=128
-    assert _call(lib, scale=-0.5) == UNS
-    assert _call(lib, scale=0.0) == UNS
+    assert _call(lib, scale=0.0) == UNS                  # 0 * (-inf) for masked scores
     assert _call(lib, dtype=1) == INV                     # fp8 without descales
     assert _call(lib, q=4097) == INV                      # misaligned (TMA needs 16 bytes)
     assert _call(lib, o=16392) == INV

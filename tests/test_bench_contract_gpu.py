@@ -36,8 +36,12 @@ def check_line(d, e2e=True):
     if e2e:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
-    assert d["gpu_launches"] >= d["steps"]
+    assert d["gpu_launches"] >= d["steps"] * d["repeats"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
+    # the reported step time is the median of the repeats' step times
+    reps = sorted(d["repeat_ms_per_step"])
+    assert len(reps) == d["repeats"] >= 1
+    assert abs(d["ms_per_step"] - reps[len(reps) // 2]) <= 1e-9 * max(1.0, d["ms_per_step"])
 
 
 def test_forward_line():

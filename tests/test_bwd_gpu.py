@@ -100,3 +100,28 @@ def test_backward_is_deterministic():
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+LONG = [
+    # 32 key tiles x 4 query heads per kv head: long dQ rings and many zig-zag turns (causal)
+    (1, 4096, 8, 2, 128, True),
+    # 64 key tiles per query tile, every one visited (non-causal)
+    (1, 8192, 2, 1, 128, False),
+]
+
+
+@pytest.mark.parametrize("B,N,H,Hkv,d,causal", LONG, ids=lambda v: str(v))
+def test_backward_long_sequences(B, N, H, Hkv, d, causal):
+    """Every element of dQ, dK and dV at N >= 4096 against the oracle (every head: a kv head's dK
+    and dV sum over all of its query heads)."""
+    q, k, v, do = draw(B, N, H, Hkv, d, 9300 + N + int(causal))
+    scale = d ** -0.5
+    f = lambda t: t.double().numpy()
+    o_ref, lse_ref = oracle.attention_forward(f(q), f(k), f(v), scale, causal)
+    o = torch.tensor(o_ref, dtype=torch.float32).to(torch.bfloat16)
+    lse = torch.tensor(lse_ref, dtype=torch.float32)
+    dq, dk, dv = binding.attn_bwd(q.cuda(), k.cuda(), v.cuda(), o.cuda(), lse.cuda(), do.cuda(), causal, scale=scale)
+    st, detail = binding.attn_get_status()
+    assert st == binding.ATTN_OK, hex(detail)
+    dq_ref, dk_ref, dv_ref, _ = oracle.attention_backward(f(q), f(k), f(v), f(do), scale, causal)
+    print("dq", compare("dq", dq, dq_ref), "dk", compare("dk", dk, dk_ref), "dv", compare("dv", dv, dv_ref))

@@ -42,11 +42,11 @@ def pin_hand_worked(attn):
 
 
 def pin_brute_force(attn):
-    """Pure-Python loops with math.exp / math.fsum on tiny inputs (no numpy arithmetic)."""
-    for causal in (False, True):
+    """Pure-Python loops with math.exp / math.fsum on tiny inputs (no numpy arithmetic), for a
+    positive and a negative scale (the definition holds for any finite nonzero scale)."""
+    for causal, scale in ((False, 0.7), (True, 0.7), (False, -0.55), (True, -0.55)):
         B, N, H, Hkv, d = 1, 5, 4, 2, 3
         q, k, v = rand_qkv(B, N, H, Hkv, d, seed=7 + causal)
-        scale = 0.7
         o, lse = attn(q, k, v, scale, causal)
         for h in range(H):
             kh = h // (H // Hkv)
