@@ -71,6 +71,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline time box")
+    ap.add_argument("--oracle-full", action="store_true",
+                    help="with --impl reference: run the oracle once over the whole workload (every head, every "
+                         "row) and report its wall time, not the bounded per-step samples")
     return ap.parse_args(argv)
 
 
@@ -311,6 +314,53 @@ def fp8_block_signs(w):
     """Random signs of the Hadamard rotation of the block-scaled e4m3 workload."""
     from exact_attention_72_gb300 import inputs
     return inputs.hadamard_signs(w.d, w.seed + 7)
+
+
+def cpu_model() -> str:
+    """CPU model of this host (lscpu's model name, else /proc/cpuinfo's)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_reference_full(args, w, x):
+    """The oracle over the whole workload, timed once on this host's cores (rank 0 only)."""
+    import numpy as np
+    import torch
+    import oracle
+    rank, _, _ = rank_info()
+    if rank != 0:
+        return
+    torch.set_num_threads(cores_used())
+    g = w.H // w.Hkv
+    t_all = 0.0
+    for b in range(w.B):
+        for h in range(w.H):
+            def f64(t, hh, sc):
+                a = t[b, :, hh, :].float().double().numpy()
+                return a * np.float64(np.float32(sc)) if t.element_size() == 1 else a
+            q, k, v = f64(x.q, h, x.descale_q), f64(x.k, h // g, x.descale_k), f64(x.v, h // g, x.descale_v)
+            t0 = time.perf_counter()
+            oracle.attention_head(q, k, v, w.scale, w.causal)
+            t_all += time.perf_counter() - t0
+    line = {"impl": "reference", "metric": METRIC, "value": w.flops / t_all / 1e12, "unit": "TFLOP/s",
+            "oracle_full": {"wall_s": t_all, "gflops": w.flops / t_all / 1e9, "cores": cores_used(),
+                            "cpu_model": cpu_model(), "flops_credited": w.flops,
+                            "what": "oracle.attention_head over every (batch, head) and every query row, fp64"},
+            "config": config_of(w)}
+    print(json.dumps(line), flush=True)
 
 
 def cores_used() -> int:
@@ -931,7 +981,7 @@ def main(argv=None):
         return 0
     x = inputs.make_inputs(w)
     if args.impl == "reference":
-        run_reference(args, w, x)
+        (run_reference_full if args.oracle_full else run_reference)(args, w, x)
     else:
         run_ours(args, w, x)
     return 0

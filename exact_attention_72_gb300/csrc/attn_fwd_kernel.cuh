@@ -441,8 +441,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_s_read[i]), 4);
     for (int i = 0; i < C::N_SBAR; ++i) {
       mbar_init(smem_addr(&bar_s_full[i]), 1);
-      mbar_init(smem_addr(&bar_p_half[i][0]), 128);
-      mbar_init(smem_addr(&bar_p_half[i][1]), 128);
+      // One arrival per softmax warp (P in TMEM) or per softmax thread (P in shared memory, where
+      // each thread's generic-proxy stores are fenced for the tensor core by that thread).
+      mbar_init(smem_addr(&bar_p_half[i][0]), C::PSMEM ? 128 : 4);
+      mbar_init(smem_addr(&bar_p_half[i][1]), C::PSMEM ? 128 : 4);
     }
     for (int i = 0; i < C::N_OBAR; ++i) mbar_init(smem_addr(&bar_o_done[i]), 1);
     for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_o_full[i]), 1);
@@ -630,15 +632,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t d_o = tmem + C::O_COL + myq * C::D;
       const uint32_t a_q = sQ + myq * C::TILE_BYTES;
       // One S turn: wait for this issuer's turn, issue S (if this Q tile needs it), pass the turn.
+      // With P in shared memory (e4m3) S_{j+1} waits only for the softmax to have loaded S_j; there
+      // the turns cost 3% (C5), so they are skipped.
       auto s_turn = [&](bool issue, uint32_t k_addr) -> bool {
-        if (!mbar_wait(smem_addr(&bar_s_turn[myq]), turns & 1, ctl, SITE_S_TURN)) return false;
-        ++turns;
+        if constexpr (!C::PSMEM) {
+          if (!mbar_wait(smem_addr(&bar_s_turn[myq]), turns & 1, ctl, SITE_S_TURN)) return false;
+          ++turns;
+        }
         if (issue) {
           tc_fence_after();
           issue_qk<C>(d_s, a_q, k_addr, C::IDESC_QK | p.qk_negate);
           tc_commit(smem_addr(&bar_s_full[myq]));
         }
-        mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
+        if constexpr (!C::PSMEM) mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
         return true;
       };
       if constexpr (C::PSMEM) {
@@ -779,14 +785,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ++p_cnt;
             if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
           }
-          release(&bar_kv_empty[pos_v % C::NS], j < n);
           if (j + 1 < nmax) {
             const uint32_t pos_k = pos_v + 1;
             if (!wait_kv(pos_k)) { ok = false; break; }
             ATTN_TRACE(18, myq, j + 1);
             if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
             ATTN_TRACE(14, myq, j + 1);
-            release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
+          }
+          // Stage releases after S_{j+1}'s issue, off the path from P_j to S_{j+1}: V_j's stage is
+          // then freed when S_{j+1} completes instead of PV_j, which the ring's depth absorbs.
+          release(&bar_kv_empty[pos_v % C::NS], j < n);
+          if (j + 1 < nmax) {
+            release(&bar_kv_empty[(pos_v + 1) % C::NS], j + 1 < n);
             if (j + 2 == nmax) release(&bar_q_empty, n > 0);
           }
         }
@@ -935,7 +945,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int qt = warp >> 2;                  // Q tile of this warpgroup
     const int r = ((warp & 3) << 5) + lane;    // row within the Q tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) << 5) << 16;
-    uint32_t s_cnt[2] = {0u, 0u};   // S tiles consumed per S buffer
+    // S tiles consumed per S buffer. Two Q tiles: one buffer per warpgroup, so a single counter
+    // (an array indexed by the warpgroup's tile would live in local memory).
+    uint32_t s_cnt0 = 0u, s_cnt1 = 0u;
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
     uint32_t sbase = 0, g = 0;      // three buffers: S products of the CTA / of this Q tile so far
@@ -999,10 +1011,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           s_lo = s_q * __ldg(dk_row + kb * p.dk_sn);
           s_hi = s_q * __ldg(dk_row + min(kb + 1, n_kblk - 1) * p.dk_sn);
         }
-        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), C::S3 ? ((gb + j) / 3u) & 1u : s_cnt[buf] & 1, ctl, SITE_S_FULL);
+        const uint32_t s_cnt = (C::NQ == 2 || buf == 0) ? s_cnt0 : s_cnt1;
+        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), C::S3 ? ((gb + j) / 3u) & 1u : s_cnt & 1, ctl, SITE_S_FULL);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (r == 0) ATTN_TRACE(4, qt, j);
-        if constexpr (!C::S3) ++s_cnt[buf];
+        if constexpr (!C::S3) {
+          if (C::NQ == 2 || buf == 0) ++s_cnt0;
+          else ++s_cnt1;
+        }
         tc_fence_after();
         uint32_t sr[128];
         const uint32_t tS = tmem + lane_base + s_col;
@@ -1091,7 +1107,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             tmem_st_wait();
             tc_fence_before();
           }
-          mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+          if constexpr (C::PSMEM) {
+            mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+          } else {
+            // Every lane's TMEM stores are complete and fenced; once the warp has converged, one
+            // lane arrives for it.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&bar_p_half[buf][h]));
+          }
           if (r == 0) ATTN_TRACE(7 + h, qt, j);
         };
         uint32_t pk[PKN];
