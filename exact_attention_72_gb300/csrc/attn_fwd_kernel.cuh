@@ -315,10 +315,32 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  return (lo & 0xFFFFu) | (hi << 16);
+// f16 pairs (low half = first element): packing from fp32 (round to nearest), 2^x per element,
+// add, unpacking to fp32, and the e4m3 pair (saturating, round to nearest) of an f16 pair.
+__device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t h2) {
+  uint32_t r;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(r) : "r"(h2));
+  return r;
+}
+__device__ __forceinline__ uint32_t f16x2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ void f16x2_unpack(uint32_t h2, float& lo, float& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.f32.f16 %0, l;\n cvt.f32.f16 %1, h;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
+__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h2) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+  return r;
 }
 
 // TMEM column of the S buffer S_j of Q tile qt uses (two Q tiles: one buffer each; one Q tile:
@@ -1064,18 +1086,38 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         constexpr int PKN = C::FP8 ? 16 : 32;   // packed 32-bit P words per half
         auto exp_half = [&](int h, uint64_t nm2, uint32_t* pk, uint64_t& acc0, uint64_t& acc1) {
           const uint64_t s2 = h ? s2_hi : s2_lo;
+          if constexpr (C::FP8) {
+            // e4m3 P keeps 3 mantissa bits, so the exponentials run in f16 pairs (one exp-unit
+            // operation per two scores; inputs to 11 bits, |t| <= 8 here) and P is packed from
+            // f16. The half's 64 terms are summed per lane in f16 (16 terms of at most 2^8 each)
+            // and then added to the fp32 row sum.
+            uint32_t hs0 = 0u, hs1 = 0u;
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
-            const int cc = h * 64 + c;
-            float t0, t1, t2, t3;
-            f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
-            f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
-            const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
-            acc0 = f2_add(acc0, f2_pack(p0, p1));
-            acc1 = f2_add(acc1, f2_pack(p2, p3));
-            if (C::FP8) {
-              pk[c >> 2] = pack_e4m3x4(p0, p1, p2, p3);
-            } else {
+            for (int c = 0; c < 64; c += 4) {
+              const int cc = h * 64 + c;
+              float t0, t1, t2, t3;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
+              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
+              const uint32_t h01 = ex2_f16x2(f16x2_pack(t0, t1)), h23 = ex2_f16x2(f16x2_pack(t2, t3));
+              hs0 = f16x2_add(hs0, h01);
+              hs1 = f16x2_add(hs1, h23);
+              pk[c >> 2] = e4m3x2_from_f16x2(h01) | (e4m3x2_from_f16x2(h23) << 16);
+            }
+            float a0, a1, b0, b1;
+            f16x2_unpack(hs0, a0, a1);
+            f16x2_unpack(hs1, b0, b1);
+            acc0 = f2_add(acc0, f2_pack(a0, a1));
+            acc1 = f2_add(acc1, f2_pack(b0, b1));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+              const int cc = h * 64 + c;
+              float t0, t1, t2, t3;
+              f2_unpack(f2_fma(f2_pack(x[cc], x[cc + 1]), s2, nm2), t0, t1);
+              f2_unpack(f2_fma(f2_pack(x[cc + 2], x[cc + 3]), s2, nm2), t2, t3);
+              const float p0 = ex2(t0), p1 = ex2(t1), p2 = ex2(t2), p3 = ex2(t3);
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+              acc1 = f2_add(acc1, f2_pack(p2, p3));
               pk[c >> 1] = pack_bf16x2(p0, p1);
               pk[(c >> 1) + 1] = pack_bf16x2(p2, p3);
             }
