@@ -57,7 +57,8 @@ struct DeviceInfo {
   int num_sms = 0;
   uint32_t* status = nullptr;
   // Host-buffer pipeline (attn_fwd_host): created on first use in each context.
-  unsigned long long pipe_ctx = 0;
+  bool pipe_made = false;
+  unsigned long long pipe_ctx = 0;   // context id the pipeline was made in
   cudaStream_t s_in = nullptr, s_out = nullptr, s_comp[2] = {nullptr, nullptr};
   cudaEvent_t ev_start = nullptr, ev_end = nullptr, ev_in[kMaxChunks] = {}, ev_k[kMaxChunks] = {};
   std::mutex pipe_mutex;   // one host-buffer call at a time per device (shared streams/events)
@@ -85,9 +86,11 @@ DeviceInfo* device_info() {
 }
 
 // Streams and events of the host-buffer pipeline for the current context; called with
-// di->pipe_mutex held. Handles made for an earlier context died with it and are not destroyed.
+// di->pipe_mutex held. They are made once and made again only when the context id changes (with
+// no readable id they are kept); handles made for an earlier context died with it and are not
+// destroyed.
 bool pipeline_ready(DeviceInfo* di) {
-  if (di->ctx != 0 && di->pipe_ctx == di->ctx) return true;
+  if (di->pipe_made && di->pipe_ctx == di->ctx) return true;
   bool ok = true;
   ok = ok && cudaStreamCreateWithFlags(&di->s_in, cudaStreamNonBlocking) == cudaSuccess;
   ok = ok && cudaStreamCreateWithFlags(&di->s_out, cudaStreamNonBlocking) == cudaSuccess;
@@ -98,7 +101,8 @@ bool pipeline_ready(DeviceInfo* di) {
     ok = ok && cudaEventCreateWithFlags(&di->ev_in[i], cudaEventDisableTiming) == cudaSuccess;
     ok = ok && cudaEventCreateWithFlags(&di->ev_k[i], cudaEventDisableTiming) == cudaSuccess;
   }
-  di->pipe_ctx = ok ? di->ctx : 0;
+  di->pipe_made = ok;
+  di->pipe_ctx = di->ctx;
   return ok;
 }
 
