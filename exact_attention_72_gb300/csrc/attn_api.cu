@@ -237,8 +237,8 @@ bool make_map_q_packed(CUtensorMap* m, const void* base, bool fp8, int d, int Nq
 
 template <int D>
 cudaError_t dispatch_split(gb300::LaunchArgs& a, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128) {
-    if (fp8) return gb300::launch_attn_fwd<128, false, true, true>(a, s);
+  if constexpr (D == 128 || D == 256) {
+    if (fp8) return gb300::launch_attn_fwd<D, false, true, true>(a, s);
   }
   return gb300::launch_attn_fwd<D, false, false, true>(a, s);
 }
@@ -251,7 +251,7 @@ size_t splitkv_part_o_bytes(int B, int H, int Nq, int d, int S) {
 
 bool supported_dim(int d, attn_dtype_t dtype) {
   if (dtype == ATTN_DTYPE_BF16) return d == 64 || d == 128 || d == 256;
-  if (dtype == ATTN_DTYPE_FP8_E4M3) return d == 128;
+  if (dtype == ATTN_DTYPE_FP8_E4M3) return d == 128 || d == 256;
   return false;
 }
 
@@ -274,8 +274,8 @@ attn_status_t check_shape(int B, int H, int Hkv, int N, int d, float scale, attn
 
 template <int D>
 cudaError_t dispatch_d(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128) {
-    if (fp8) return causal ? gb300::launch_attn_fwd<128, true, true>(a, s) : gb300::launch_attn_fwd<128, false, true>(a, s);
+  if constexpr (D == 128 || D == 256) {
+    if (fp8) return causal ? gb300::launch_attn_fwd<D, true, true>(a, s) : gb300::launch_attn_fwd<D, false, true>(a, s);
   }
   return causal ? gb300::launch_attn_fwd<D, true, false>(a, s) : gb300::launch_attn_fwd<D, false, false>(a, s);
 }
@@ -290,10 +290,10 @@ namespace {
 
 template <int D>
 cudaError_t dispatch_varlen(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128) {
+  if constexpr (D == 128 || D == 256) {
     if (fp8)
-      return causal ? gb300::launch_attn_fwd<128, true, true, false, true>(a, s)
-                    : gb300::launch_attn_fwd<128, false, true, false, true>(a, s);
+      return causal ? gb300::launch_attn_fwd<D, true, true, false, true>(a, s)
+                    : gb300::launch_attn_fwd<D, false, true, false, true>(a, s);
   }
   return causal ? gb300::launch_attn_fwd<D, true, false, false, true>(a, s)
                 : gb300::launch_attn_fwd<D, false, false, false, true>(a, s);

@@ -94,10 +94,13 @@ GB300_DECLARE_LAUNCH(256, false, false)
 GB300_DECLARE_LAUNCH(256, true, false)
 GB300_DECLARE_LAUNCH(128, false, true)
 GB300_DECLARE_LAUNCH(128, true, true)
+GB300_DECLARE_LAUNCH(256, false, true)
+GB300_DECLARE_LAUNCH(256, true, true)
 GB300_DECLARE_SPLIT(64, false)
 GB300_DECLARE_SPLIT(128, false)
 GB300_DECLARE_SPLIT(256, false)
 GB300_DECLARE_SPLIT(128, true)
+GB300_DECLARE_SPLIT(256, true)
 GB300_DECLARE_VARLEN(64, false, false)
 GB300_DECLARE_VARLEN(64, true, false)
 GB300_DECLARE_VARLEN(128, false, false)
@@ -106,5 +109,7 @@ GB300_DECLARE_VARLEN(256, false, false)
 GB300_DECLARE_VARLEN(256, true, false)
 GB300_DECLARE_VARLEN(128, false, true)
 GB300_DECLARE_VARLEN(128, true, true)
+GB300_DECLARE_VARLEN(256, false, true)
+GB300_DECLARE_VARLEN(256, true, true)
 
 }  // namespace gb300

@@ -53,7 +53,7 @@ typedef enum {
  *   o      [B, N, H,   d]  bfloat16 output
  *   lse    [B, H, N]       float32 output, LSE_i = ln sum_j exp(scale * q_i . k_j) over the
  *                          keys row i may see (all keys, or j <= i when causal)
- *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16, d == 128 for fp8.
+ *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16, d in {128, 256} for fp8.
  *   scale  finite, nonzero float multiplying the raw dot products (usually 1/sqrt(d)); it does
  *          not include the fp8 descales. A negative scale is allowed (the kernel computes
  *          |scale| * (-Q) K^T, so the softmax's running maximum is taken over the scaled scores
@@ -106,7 +106,7 @@ int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal);
  * heads differ in magnitude: "flash-attention-3" (ai.thesatyajit.com), "FP8 is a different
  * kernel" (descale pointers with strides).
  *   descale arrays: DEVICE fp32, large enough for every (b, head) the strides address.
- *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128).
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128 or 256).
  */
 attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int H, int Hkv, int N, int d, float scale,
@@ -201,7 +201,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  *   Descales must be positive and finite. attn_quantize_e4m3 writes codes and descales in these
  *   layouts (block_rows 128 for q, 64 for k, N for v). q and k may both be rotated by the same
  *   orthogonal matrix: the scores do not change.
- *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128).
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128 or 256).
  */
 attn_status_t attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
                                        float* lse, int B, int H, int Hkv, int N, int d,

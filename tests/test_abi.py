@@ -68,7 +68,7 @@ def test_validation_rejects_bad_arguments(lib):
     assert _call(lib, scale=float("inf")) == INV
     assert _call(lib, dtype=7) == INV
     assert _call(lib, d=96) == UNS                        # head dim without an instance
-    assert _call(lib, d=64, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # fp8 only for d=128
+    assert _call(lib, d=64, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # e4m3 only for d = 128 and 256
     assert _call(lib, scale=0.0) == UNS                  # 0 * (-inf) for masked scores
     assert _call(lib, dtype=1) == INV                     # fp8 without descales
     assert _call(lib, q=4097) == INV                      # misaligned (TMA needs 16 bytes)
@@ -123,7 +123,7 @@ def test_fp8_scaled_validation(lib):
     assert call(dq=0) == INV                         # descale pointers are required
     assert call(dv=0) == INV
     assert call(N=0) == INV
-    assert call(d=64) == UNS                         # e4m3 is built for d = 128 only
+    assert call(d=64) == UNS                         # e4m3 is built for d = 128 and 256
 
 
 def test_quantize_and_blockscaled_validation(lib):

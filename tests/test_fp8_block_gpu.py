@@ -134,12 +134,14 @@ BCASES = [
     dict(B=1, H=2, Hkv=2, N=200, causal=False, rot=True, seed=7004),
     # 17 key tiles, 36 work tiles: the last wave's keys are halved across two launches
     dict(B=1, H=4, Hkv=2, N=2100, causal=False, rot=False, seed=7005),
+    # head dim 256 (one Q tile per work tile)
+    dict(B=1, H=2, Hkv=1, N=300, causal=True, rot=True, seed=7006, d=256),
 ]
 
 
 @pytest.mark.parametrize("c", BCASES, ids=lambda c: f"B{c['B']}H{c['H']}N{c['N']}c{int(c['causal'])}r{int(c['rot'])}")
 def test_blockscaled_forward_parity(c):
-    B, H, Hkv, N, d = c["B"], c["H"], c["Hkv"], c["N"], 128
+    B, H, Hkv, N, d = c["B"], c["H"], c["Hkv"], c["N"], c.get("d", 128)
     q = bf16_draw((B, N, H, d), c["seed"], 0.002).double().numpy()
     k = bf16_draw((B, N, Hkv, d), c["seed"] + 1, 0.002).double().numpy()
     v = bf16_draw((B, N, Hkv, d), c["seed"] + 2, 0.002).double().numpy()

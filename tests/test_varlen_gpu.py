@@ -93,6 +93,7 @@ CASES = [
     vw("d256_more_queries", [260, 5], [130, 300], H=2, Hkv=2, d=256),
     vw("fp8_causal", [250, 600, 90], dtype="fp8_e4m3"),
     vw("fp8_noncausal", [250, 600, 90], [100, 600, 300], causal=False, dtype="fp8_e4m3"),
+    vw("fp8_d256_causal", [300, 129, 40], H=2, Hkv=1, d=256, dtype="fp8_e4m3"),
     vw("many_short", inputs.varlen_lengths(40, 1, 90, 8001), H=2, Hkv=1),
 ]
 
