@@ -356,6 +356,7 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   p.N = N;
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.qk_negate = scale < 0.0f ? gb300::kIdescNegateA : 0u;
+  p.o_v8 = aligned(o, 32) ? 1 : 0;
   p.n_mb = (N + rows - 1) / rows;
   p.n_tiles = B * H * p.n_mb;
   p.Nk = N;
@@ -699,6 +700,7 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
   p.N = total_q;
   p.Nk = total_k;
   p.G = H / Hkv;
+  p.o_v8 = aligned(o, 32) ? 1 : 0;
   p.scale_log2 = std::fabs(scale) * 1.4426950408889634f;
   p.qk_negate = scale < 0.0f ? gb300::kIdescNegateA : 0u;
   // Launch bound and read limit: the tiles a valid plan can hold, and no more than the buffer has.

@@ -76,6 +76,7 @@ struct AttnParams {
   // such tile (unit u is tile tail_first + u), visits [tail_kvt, n_kvt) and merges its half into
   // the O and LSE the first launch wrote. tail_mode 0: every tile visits all KV tiles.
   int tail_mode, tail_first, tail_kvt;
+  int o_v8;                 // o is 32-byte aligned: each lane writes its row 32 bytes at a time
   uint32_t* status;         // device status word (first failure)
   unsigned long long timeout_ns;
   int debug_skip_load;      // fault injection: CTA 0 never loads V_0 of its first tile
@@ -1314,18 +1315,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             lse_out = (mx + log2f(ea + eb)) * 0.69314718055994531f;
           }
         }
+        // 64 columns per round: two TMEM loads behind one wait, then the row's 128 bytes of bf16
+        // in 32-byte stores (one whole sector per lane) where o allows it.
 #pragma unroll 1
-        for (int c0 = 0; c0 < C::D; c0 += 32) {
-          uint32_t ov[32];
+        for (int c0 = 0; c0 < C::D; c0 += 64) {
+          uint32_t ov[64];
           tmem_ld_32cols(tO + c0, ov);
+          tmem_ld_32cols(tO + c0 + 32, ov + 32);
           tmem_ld_wait();
           reg_fence32(ov);
-          uint32_t pk[16];
+          reg_fence32(ov + 32);
+          uint32_t pk[32];
           if (merge && valid) {
-            // O_a of these 32 columns: 16 bf16 pairs, the lower-addressed element in the low half.
+            // O_a of these 64 columns: 32 bf16 pairs, the lower-addressed element in the low half.
             const uint4* src = reinterpret_cast<const uint4*>(orow + c0);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
+            for (int v4 = 0; v4 < 8; ++v4) {
               const uint4 u = __ldcg(src + v4);
               const uint32_t wds[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -1338,15 +1343,20 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < 32; c += 2)
+            for (int c = 0; c < 64; c += 2)
               pk[c >> 1] = empty_row ? 0u
                                      : pack_bf16x2(__uint_as_float(ov[c]) * inv_l, __uint_as_float(ov[c + 1]) * inv_l);
           }
           if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+            if (p.o_v8) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+              for (int v8 = 0; v8 < 4; ++v8) st_global_v8(orow + c0 + 16 * v8, pk + 8 * v8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+              for (int v4 = 0; v4 < 8; ++v4)
+                dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
           }
         }
         if (valid) *lse_dst = empty_row ? -INFINITY : lse_out;

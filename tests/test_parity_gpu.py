@@ -108,3 +108,33 @@ def test_full_size_sampled_heads(w):
     stats = compare_heads(w, o, lse, oracle_heads(w, x, heads))
     check_convex_hull(w, x, o)
     print(w.name, stats)
+
+
+def _shifted_out(shape):
+    """A bf16 output view that is 16- but not 32-byte aligned."""
+    n = int(np.prod(shape))
+    buf = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(shape)
+    assert out.data_ptr() % 32 == 16
+    return out
+
+
+ALIGN_CASES = [SMALL[0], SMALL[1], SMALL[4], SMALL[7], SMALL[9],
+               # non-causal, one sparse wave: the halved last wave's merge reads and rewrites o
+               small("halved_gqa", B=1, H=8, Hkv=2, N=2048, d=128, seed=79)]
+
+
+@pytest.mark.parametrize("w", ALIGN_CASES, ids=lambda w: w.name)
+def test_output_alignment_paths_agree(w):
+    """An o that is only 16-byte aligned takes 16-byte stores instead of 32-byte ones: same bits."""
+    from exact_attention_72_gb300 import binding
+    from parity_util import to_device
+    x = inputs.make_inputs(w)
+    q, k, v, desc = to_device(x)
+    kw = {} if desc is None else dict(descale_q=desc[0], descale_k=desc[1], descale_v=desc[2])
+    o_a, l_a = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, **kw)
+    assert o_a.data_ptr() % 32 == 0
+    o_b, l_b = binding.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, out=_shifted_out(o_a.shape), **kw)
+    st, detail = binding.attn_get_status()
+    assert st == binding.ATTN_OK, (st, hex(detail))
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)

@@ -185,3 +185,22 @@ def test_plan_reused_across_calls():
     o2, lse2, _ = run_varlen(w, x2, plan=plan)
     check(w, x1, o1, lse1)
     check(w, x2, o2, lse2)
+
+
+@pytest.mark.parametrize("w", [CASES[2], CASES[6], CASES[10]], ids=lambda w: w.name)
+def test_output_alignment_paths_agree(w):
+    """An o that is only 16-byte aligned takes 16-byte stores instead of 32-byte ones: same bits
+    (empty rows included)."""
+    x = inputs.make_varlen_inputs(w)
+    o_a, l_a, plan = run_varlen(w, x)
+    assert o_a.data_ptr() % 32 == 0
+    buf = torch.empty(o_a.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    out = buf[8:].view(o_a.shape)
+    assert out.data_ptr() % 32 == 16
+    cu_q = torch.tensor(w.cu_q, dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device="cuda")
+    o_b, l_b = binding.attn_fwd_varlen(x.q.cuda(), x.k.cuda(), x.v.cuda(), cu_q, cu_k, plan, w.causal,
+                                       scale=w.scale, out=out)
+    st, detail = binding.attn_get_status()
+    assert st == binding.ATTN_OK, (st, hex(detail))
+    assert torch.equal(o_a, o_b) and torch.equal(l_a, l_b)
