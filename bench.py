@@ -535,8 +535,8 @@ def launches_per_step(w):
     from exact_attention_72_gb300 import binding
     if w.name in DECODE_NAMES:
         return 2                                  # split-KV forward + combine
-    # a non-causal forward whose last wave is halved along the keys makes a second launch
-    fwd = 2 if binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) > 0 else 1
+    # a non-causal forward that cuts some tiles' keys across two launches makes a second launch
+    fwd = 2 if binding.attn_fwd_tail_units(w.B, w.H, w.N, w.d, w.causal, fp8=w.dtype != "bf16") else 1
     if w.dtype == "fp8_block":
         v_launches = 1 if w.N <= 128 else 3       # one block per head: maxima, codes, descales
         return 1 + 1 + v_launches + fwd           # quantise q, k, v; block-scaled forward

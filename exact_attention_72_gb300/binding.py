@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.attn_splitkv_num_splits.argtypes = [i, i, i, i, i, i]
     L.attn_fwd_halved_tail_tiles.restype = i
     L.attn_fwd_halved_tail_tiles.argtypes = [i, i, i, i, i]
+    L.attn_fwd_tail_units.restype = i
+    L.attn_fwd_tail_units.argtypes = [i, i, i, i, i, i, vp, vp, i]
     L.attn_fwd_host.restype = i
     L.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, vp, vp, vp, sz, vp]
     L.attn_fwd_splitkv.restype = i
@@ -349,8 +351,22 @@ def attn_quantize_e4m3_descale_count(B: int, N: int, Hx: int, block_rows: int) -
 
 
 def attn_fwd_halved_tail_tiles(B: int, H: int, N: int, d: int, causal: bool) -> int:
-    """Work tiles of an attn_fwd call whose key range the library halves across two launches."""
+    """Work tiles of an attn_fwd call whose key range the library cuts across two launches."""
     return int(lib().attn_fwd_halved_tail_tiles(B, H, N, d, int(bool(causal))))
+
+
+def attn_fwd_tail_units(B: int, H: int, N: int, d: int, causal: bool, fp8: bool = False):
+    """The cut tiles of an attn_fwd call (bf16, or e4m3 with fp8 set), in the second launch's
+    order: [(work tile, first key tile of the second part), ...]."""
+    code = ATTN_DTYPE_FP8_E4M3 if fp8 else ATTN_DTYPE_BF16
+    n = int(lib().attn_fwd_tail_units(B, H, N, d, int(bool(causal)), code, None, None, 0))
+    if n == 0:
+        return []
+    t = (ctypes.c_int * n)()
+    k = (ctypes.c_int * n)()
+    got = lib().attn_fwd_tail_units(B, H, N, d, int(bool(causal)), code, t, k, n)
+    assert got == n
+    return list(zip(t, k))
 
 
 def attn_splitkv_num_splits(B: int, H: int, Hkv: int, Nq: int, Nk: int, d: int) -> int:

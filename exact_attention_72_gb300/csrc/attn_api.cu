@@ -369,12 +369,9 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   p.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
   p.debug_skip_load = g_skip_load;
   a.num_sms = di->num_sms;
-  // A last wave that would leave more than half of the SMs idle is halved along the keys: the
-  // first launch takes the first halves, a dependent launch the second halves and the merge.
-  const int halved = gb300::halved_tail_tiles(p.n_tiles, p.n_kvt, a.num_sms, causal != 0);
-  p.tail_mode = halved ? 1 : 0;
-  p.tail_first = p.n_tiles - halved;
-  p.tail_kvt = gb300::halved_tail_cut(p.n_kvt);
+  // A last wave that would leave SMs idle has its tiles' keys cut: the first launch takes the
+  // first parts, a dependent launch the rest and the merge.
+  const int halved = gb300::plan_tail(p, p.n_tiles, p.n_kvt, a.num_sms, causal != 0, !fp8 && d <= 128);
   auto launch = [&](gb300::LaunchArgs& x) -> cudaError_t {
     switch (d) {
       case 64: return dispatch_d<64>(x, causal != 0, fp8, stream);
@@ -385,7 +382,7 @@ attn_status_t prefill_forward(const void* q, const void* k, const void* v, void*
   cudaError_t e = launch(a);
   if (e == cudaSuccess && halved) {
     gb300::LaunchArgs second = a;
-    second.params.tail_mode = 2;
+    second.params.tail_mode = p.tail_mode == 3 ? 4 : 2;
     second.params.n_tiles = halved;
     second.dependent = true;
     e = launch(second);
@@ -517,15 +514,27 @@ attn_status_t attn_fwd_host(const void* q, const void* k, const void* v, void* o
   return (ok && joined && synced) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal) {
+int attn_fwd_tail_units(int B, int H, int N, int d, int causal, attn_dtype_t dtype, int* tiles, int* kv0,
+                        int cap) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128 && d != 256)) return 0;
+  if (dtype != ATTN_DTYPE_BF16 && dtype != ATTN_DTYPE_FP8_E4M3) return 0;
   int sms = 152;
   DeviceInfo* di = device_info();
   if (di) sms = di->num_sms;
   const long long rows = gb300::rows_per_work_tile(d);
-  const long long tiles = (long long)B * H * ((N + rows - 1) / rows);
-  if (tiles >= (1LL << 31)) return 0;
-  return gb300::halved_tail_tiles(tiles, (N + 127) / 128, sms, causal != 0);
+  const long long n_tiles = (long long)B * H * ((N + rows - 1) / rows);
+  if (n_tiles >= (1LL << 31)) return 0;
+  gb300::AttnParams p;
+  const int n = gb300::plan_tail(p, n_tiles, (N + 127) / 128, sms, causal != 0, dtype == ATTN_DTYPE_BF16 && d <= 128);
+  for (int u = 0; u < n && u < cap; ++u) {
+    if (tiles) tiles[u] = p.tail_tab[u].x;
+    if (kv0) kv0[u] = p.tail_tab[u].y;
+  }
+  return n;
+}
+
+int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal) {
+  return attn_fwd_tail_units(B, H, N, d, causal, ATTN_DTYPE_BF16, nullptr, nullptr, 0);
 }
 
 int attn_splitkv_num_splits(int B, int H, int Hkv, int Nq, int Nk, int d) {

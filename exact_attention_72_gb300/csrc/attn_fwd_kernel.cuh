@@ -41,6 +41,9 @@
 
 namespace gb300 {
 
+// Most units a second (dependent) launch of a non-causal prefill can take.
+constexpr int kMaxTailUnits = 256;
+
 struct AttnParams {
   void* o;                  // bf16 [B, N, H, D]
   float* lse;               // fp32 [B, H, N]
@@ -71,11 +74,23 @@ struct AttnParams {
   const int* cu_q;
   const int* cu_k;
   const int* plan;
-  // Non-causal prefill, last wave halved: in the first launch (tail_mode 1) work tiles
-  // t >= tail_first visit only KV tiles [0, tail_kvt); a second launch (tail_mode 2), one unit per
-  // such tile (unit u is tile tail_first + u), visits [tail_kvt, n_kvt) and merges its half into
-  // the O and LSE the first launch wrote. tail_mode 0: every tile visits all KV tiles.
+  // Non-causal prefill whose last wave would leave SMs idle: some work tiles have their key range
+  // cut in two. The first launch covers the first part of each such tile and writes its O and LSE
+  // as usual; a second, dependent launch covers the rest of the keys and merges it into what the
+  // first launch wrote.
+  //   tail_mode 1, first launch (last wave halved): tiles t >= tail_first visit only KV tiles
+  //     [0, tail_kvt); tail_mode 2, its second launch: unit u is tile tail_first + u from KV tile
+  //     tail_kvt on.
+  //   tail_mode 3, first launch (share deal, bf16 at d <= 128): tiles below bal_main go
+  //     round-robin in whole rounds; the KV tiles of the rest, taken tile by tile, are dealt in
+  //     gridDim.x equal shares (see bal_share), so every CTA ends the launch pair with the same
+  //     number of KV tiles; tail_mode 4, its second launch: unit u is tile tail_tab[u].x from KV
+  //     tile tail_tab[u].y on.
+  // tail_mode 0: every tile visits all KV tiles.
   int tail_mode, tail_first, tail_kvt;
+  int bal_main;             // tail_mode 3: tiles dealt in whole rounds (a multiple of gridDim.x)
+  long long bal_wtail;      // tail_mode 3: KV tiles of the remaining tiles
+  int2 tail_tab[kMaxTailUnits];   // tail_mode 4: (tile, first KV tile) per unit
   int o_v8;                 // o is 32-byte aligned: each lane writes its row 32 bytes at a time
   uint32_t* status;         // device status word (first failure)
   unsigned long long timeout_ns;
@@ -107,6 +122,8 @@ struct AttnCfg {
   // step j. (bf16 at d = 128 has no shared memory to spare for P, nor shared-memory bandwidth:
   // its PV would read twice as many bytes per cycle as the e4m3 one.)
   static constexpr bool PSMEM = FP8_ && (D_ <= 128 && !SPLIT_);
+  // Non-causal bf16 prefill at d <= 128 may take the share deal of its last tiles (tail_mode 3).
+  static constexpr bool SHARES = !CAUSAL_ && !SPLIT_ && !VARLEN_ && !FP8_ && D_ <= 128;
   static constexpr int P_BYTES = PSMEM ? Q_BYTES : 0;
   static constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
   static constexpr int RESERVE = 1024 + 1024;             // alignment slack + static shared
@@ -140,15 +157,17 @@ struct AttnCfg {
   static constexpr int WARP_S = WARP_LOAD + 1;            // three-buffer mode: the S issuer
   // Two Q tiles: 12 warps (softmax x8, MMA x2, load, and the S issuer at d = 64, else idle) so the
   // third warpgroup can hand registers to the softmax warpgroups with setmaxnreg. The launch gives
-  // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them. The
-  // host checks the compiled register count first (an over-subscribed increase never returns).
+  // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them, or
+  // at d = 64 (whose softmax gains from the room: 0.99 -> 0.97 ms on the 16k-key workload)
+  // 256 x 216 + 128 x 72 = 64,512. The host checks the compiled register count first (an
+  // over-subscribed increase never returns).
   static constexpr bool REG_SPLIT = (NQ == 2);
   // With a two-stage ring (d = 256: 64 KB tiles) K_j always takes stage 0 and V_j stage 1. Then
   // K and V get a producer warp each (WARP_LOAD: Q and K, WARP_LOAD + 1: V), so the next K can
   // load as soon as S has read the last one, without queueing behind V's wait for PV.
   static constexpr bool TWO_LOADERS = (NS == 2);
   static constexpr int THREADS = REG_SPLIT ? 384 : (SOFTMAX_WARPS + MMA_WARPS + 1 + (TWO_LOADERS ? 1 : 0)) * 32;
-  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_OTHER = 96;
+  static constexpr uint32_t REGS_SOFTMAX = D == 64 ? 216 : 200, REGS_OTHER = D == 64 ? 72 : 96;
   static constexpr int REGS_NEEDED = SOFTMAX_WARPS * 32 * REGS_SOFTMAX + 128 * REGS_OTHER;
   static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, 128, BN, false, false);
@@ -170,6 +189,21 @@ struct TileCoord {
   int q_base, k_base;   // first q / k row of the sequence in the packed tensors (varlen)
   int nq, nk, n_kvt;    // query rows, keys and 128-key tiles of this sequence
 };
+
+// Balanced tail (tail_mode 3), this CTA's share of the W = bal_wtail KV tiles that follow the
+// whole rounds: [s0, s1) with s0 = floor(c W / G), s1 = floor((c + 1) W / G), the KV tiles of tail
+// tile i being i K .. i K + K - 1 (K = n_kvt). The first launch runs tail tiles ta .. te: those
+// that start inside the share, whole, and tile te, cut at KV tile je when the share ends inside
+// it (je = K otherwise). The part of a tile before s0 belongs to the previous share; the part
+// from s0 on, when s0 falls inside a tile, is a second-launch unit. Every share is at least K
+// long, so te >= ta and no tile is cut twice.
+__device__ __forceinline__ void bal_share(const AttnParams& p, int& ta, int& te, int& je) {
+  const long long G = gridDim.x, c = blockIdx.x, K = p.n_kvt;
+  const long long s0 = c * p.bal_wtail / G, s1 = (c + 1) * p.bal_wtail / G;
+  ta = (int)((s0 + K - 1) / K);
+  te = (int)((s1 - 1) / K);
+  je = (int)(s1 - (long long)te * K);
+}
 
 // Work tile t -> (batch, head, query block). Causal tiles go longest first: every head's last
 // query block, then every head's second-to-last, and so on. Non-causal tiles keep a head's
@@ -237,6 +271,17 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const AttnParams& p) {
     } else if (p.tail_mode == 1 && t >= p.tail_first) {
       c.j1 = p.tail_kvt;
     }
+    if constexpr (C::SHARES) {
+      if (p.tail_mode == 4) {
+        const int2 e = p.tail_tab[t];
+        tile = e.x;
+        c.j0 = e.y;
+      } else if (p.tail_mode == 3 && t >= p.bal_main) {
+        int ta, te, je;
+        bal_share(p, ta, te, je);
+        if (t - p.bal_main == te) c.j1 = je;   // the tile this CTA's share ends in: its first part
+      }
+    }
     c.mb = tile % p.n_mb;
     bh = tile / p.n_mb;
   }
@@ -303,6 +348,22 @@ template <bool ZIGZAG>
 __device__ __forceinline__ int deal_tile(int turn) {
   const int g = (int)gridDim.x, c = (int)blockIdx.x;
   return turn * g + ((ZIGZAG && (turn & 1)) ? g - 1 - c : c);
+}
+
+// Work tile of this CTA's turn-th turn; n_tiles or more once it has none left.
+template <class C>
+__device__ __forceinline__ int next_tile(int turn, const AttnParams& p) {
+  if constexpr (C::SHARES) {
+    if (p.tail_mode == 3) {
+      const int rounds = p.bal_main / (int)gridDim.x;
+      if (turn < rounds) return turn * (int)gridDim.x + (int)blockIdx.x;
+      int ta, te, je;
+      bal_share(p, ta, te, je);
+      const int i = ta + (turn - rounds);
+      return i <= te ? p.bal_main + i : p.n_tiles;
+    }
+  }
+  return deal_tile<C::CAUSAL || C::VARLEN>(turn);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -408,7 +469,7 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, 
 template <class C>
 __global__ void __launch_bounds__(C::THREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // kv_empty / q_empty take one arrival per MMA-issuer warp (a tcgen05.commit after the MMAs
   // that read the stage, or a plain arrive for a stage that warp's Q tile does not need).
@@ -440,7 +501,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // the launch of the second halves is. Let its CTAs be scheduled now (they read this grid's
   // results only after waiting for it to finish).
   constexpr bool kDense = !C::CAUSAL && !C::SPLIT && !C::VARLEN;
-  if (C::SPLIT || (kDense && p.tail_mode == 1)) griddep_launch_dependents();
+  if (C::SPLIT || (kDense && (p.tail_mode == 1 || p.tail_mode == 3))) griddep_launch_dependents();
   const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
   const uint32_t sP = smem_base + C::Q_BYTES;   // P tiles (e4m3, two Q tiles); empty otherwise
@@ -504,7 +565,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t nq_loads = 0;  // Q loads issued so far (K warp)
       bool ok = true;
       int iter = 0;
-      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn), ++iter) {
+      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p), ++iter) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
@@ -573,7 +634,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       uint32_t nq_loads = 0;  // Q loads issued so far
       bool ok = true;
       int iter = 0;
-      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn), ++iter) {
+      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p), ++iter) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int kvh = C::SPLIT ? tc.h : tc.h / p.G;
         int nmax = 0, nq_valid = 0;
@@ -684,7 +745,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           read_pending = false;
           return true;
         };
-        for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+        for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
           const TileCoord tc = decode_tile<C>(t, p);
           const int n = kv_tiles_for<C>(tc, myq, p);
           int nmax = 0;
@@ -739,7 +800,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // product: index 3 myq + g % 3, phase g / 3.
         uint32_t sbase = 0;   // S products of both Q tiles before the current work tile
         uint32_t g = 0;       // S products of this Q tile before the current work tile
-        for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+        for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
           const TileCoord tc = decode_tile<C>(t, p);
           const int n0 = kv_tiles_for<C>(tc, 0, p), n1 = kv_tiles_for<C>(tc, 1, p);
           const int n = myq ? n1 : n0;
@@ -773,7 +834,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           ring = base + 2 * nmax;
         }
       } else {
-      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int n = kv_tiles_for<C>(tc, myq, p);
         int nmax = 0;
@@ -839,7 +900,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       // need), the k-th into buffer k % 3 once the PV of the (k-3)-th has read that buffer.
       uint32_t ring = 0, nq_loads = 0, sbase = 0, g0 = 0, g1 = 0;
       bool ok = true;
-      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int n0 = kv_tiles_for<C>(tc, 0, p), n1 = kv_tiles_for<C>(tc, 1, p);
         const int nmax = n0 > n1 ? n0 : n1;
@@ -917,7 +978,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         ++p_cnt[buf];
         return true;
       };
-      for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
         const TileCoord tc = decode_tile<C>(t, p);
         const int nmax = kv_tiles_for<C>(tc, 0, p);
         if (nmax == 0) continue;
@@ -975,7 +1036,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
     uint32_t sbase = 0, g = 0;      // three buffers: S products of the CTA / of this Q tile so far
     bool ok = true;
-    for (int turn = 0, t = deal_tile<C::CAUSAL || C::VARLEN>(0); ok && t < n_tiles; t = deal_tile<C::CAUSAL || C::VARLEN>(++turn)) {
+    for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
       const TileCoord tc = decode_tile<C>(t, p);
       const int n = kv_tiles_for<C>(tc, qt, p);
       int n0 = 0, n1 = 0;
@@ -1300,7 +1361,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // over keys [0, tail_kvt). With this half's O_b and LSE_b over the rest, the row over all
         // keys is LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b (the
         // split-KV combine for two ranges). Wait for the first grid to finish before reading.
-        const bool merge = kDense && p.tail_mode == 2;
+        const bool merge = kDense && (p.tail_mode == 2 || p.tail_mode == 4);
         float w_a = 0.0f;
         if (merge) {
           griddep_wait();
@@ -1375,7 +1436,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (warp == C::WARP_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
   // A second-half launch never finishes before the first launch, even where a failed wait kept
   // its epilogue from waiting, so work queued after it on the stream sees both.
-  if (kDense && p.tail_mode == 2) griddep_wait();
+  if (kDense && (p.tail_mode == 2 || p.tail_mode == 4)) griddep_wait();
 }
 
 }  // namespace gb300

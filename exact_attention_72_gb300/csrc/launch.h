@@ -1,5 +1,6 @@
 // Host-side launch plumbing shared by the C ABI and the kernel instantiation units.
 #pragma once
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include "attn_bwd_kernel.cuh"
@@ -62,20 +63,58 @@ cudaError_t launch_quantize_e4m3(const QuantLaunch& q, cudaStream_t stream);
 // Rows of queries one CTA work tile covers for head dim d (two 128-row tiles for d <= 128).
 inline int rows_per_work_tile(int d) { return d <= 128 ? 256 : 128; }
 
-// Non-causal prefill: work tiles of the last wave whose KV range is halved across two launches
-// (0: none). The last wave of `tiles` over `sms` persistent CTAs holds 1..sms tiles; when it would
-// leave more than half of the SMs idle, its tiles are cut in two at KV tile n_kvt / 2, the second
-// halves running as a dependent launch on the idle SMs. Each half keeps at least eight KV tiles,
-// so the halves' own pipeline fill and the merge stay small beside what they save.
-inline int halved_tail_tiles(long long tiles, int n_kvt, int sms, bool causal) {
-  if (causal || n_kvt < 16 || sms < 2 || tiles < 1) return 0;
-  const long long rem = tiles - (tiles - 1) / sms * sms;
-  return rem <= sms / 2 ? (int)rem : 0;
+// Non-causal prefill over `tiles` work tiles of n_kvt KV tiles each on `sms` persistent CTAs:
+// which tiles have their key range cut between the first launch and a dependent second launch
+// (AttnParams::tail_mode). Sets tail_mode, tail_first, tail_kvt, bal_main, bal_wtail and the
+// second launch's units (tail_tab) in p, and returns the unit count (0: one launch, tail_mode 0).
+//  * shares (bf16 at d <= 128): more than one wave, not a whole number of waves, at least 8 KV
+//    tiles: whole rounds of sms tiles go round-robin except the last whole one; the KV tiles of
+//    the tiles after them are dealt in sms equal shares (tail_mode 3; each share is at least
+//    n_kvt long). Every CTA then does the same number of KV tiles over the two launches instead
+//    of some CTAs one tile more than others. A share boundary inside a tile makes a second-launch
+//    unit (the rest of that tile). Units go longest first: the second launch's CTAs take SMs in
+//    the order the first launch's CTAs leave them, and the CTA whose share begins with the
+//    longest rest has the least work in the first launch. (e4m3 and d = 256 run their tiles in
+//    fewer, cheaper steps; there the extra partial tile per CTA cost what the balance saved.)
+//  * otherwise, a last wave that leaves more than half of the SMs idle, with at least 16 KV
+//    tiles: its tiles are cut at the middle, n_kvt / 2 (tail_mode 1). Each half keeps at least
+//    eight KV tiles, so the halves' own pipeline fill and the merge stay small beside what they
+//    save; moving the cut by up to n_kvt / 6 either way saved at most 1% on the shapes measured.
+inline int plan_tail(AttnParams& p, long long tiles, int n_kvt, int sms, bool causal, bool shares) {
+  p.tail_mode = 0;
+  p.tail_first = 0;
+  p.tail_kvt = n_kvt;
+  p.bal_main = 0;
+  p.bal_wtail = 0;
+  if (causal || sms < 2 || tiles < 1 || n_kvt < 1) return 0;
+  if (!(shares && tiles > sms && tiles % sms != 0 && n_kvt >= 8 && sms - 1 <= kMaxTailUnits)) {
+    if (n_kvt < 16) return 0;
+    const long long rem = tiles - (tiles - 1) / sms * sms;   // tiles of the last wave
+    if (rem > sms / 2 || rem > kMaxTailUnits) return 0;
+    p.tail_mode = 1;
+    p.tail_first = (int)(tiles - rem);
+    p.tail_kvt = n_kvt / 2;
+    for (int u = 0; u < (int)rem; ++u) p.tail_tab[u] = make_int2(p.tail_first + u, p.tail_kvt);
+    return (int)rem;
+  }
+  const long long main_tiles = (tiles / sms - 1) * sms;
+  const long long K = n_kvt, W = (tiles - main_tiles) * K;
+  struct Unit { int tile, j0, share; };
+  Unit u[kMaxTailUnits];
+  int n = 0;
+  for (int c = 1; c < sms; ++c) {
+    const long long s0 = (long long)c * W / sms;
+    if (s0 % K != 0) u[n++] = Unit{(int)(main_tiles + s0 / K), (int)(s0 % K), c};
+  }
+  std::sort(u, u + n, [&](const Unit& a, const Unit& b) {
+    return a.j0 != b.j0 ? a.j0 < b.j0 : a.share < b.share;   // longest rest first
+  });
+  for (int i = 0; i < n; ++i) p.tail_tab[i] = make_int2(u[i].tile, u[i].j0);
+  p.tail_mode = 3;
+  p.bal_main = (int)main_tiles;
+  p.bal_wtail = W;
+  return n;
 }
-// KV tile at which a halved tile is cut: the middle. The second launch starts cold and ends with
-// the merge, which waits for the whole first grid; on the shapes measured (d = 64, 128, 256, bf16
-// and e4m3) moving the cut by up to n_kvt / 6 either way saved at most 1% and mostly cost time.
-inline int halved_tail_cut(int n_kvt) { return n_kvt / 2; }
 // Split-KV mode always runs one 128-row Q tile per CTA.
 inline int rows_per_split_work_tile(int) { return 128; }
 

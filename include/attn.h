@@ -69,13 +69,21 @@ typedef enum {
  *
  * Launches: one persistent kernel, one CTA per SM, each CTA walking work tiles of 256 (d <= 128)
  * or 128 (d == 256) query rows of one (batch, head). Non-causal calls whose last wave of work
- * tiles would leave more than half of the SMs idle (see attn_fwd_halved_tail_tiles) make a
- * second launch: the first launch covers keys [0, 128 C) of those last tiles, C = floor(K / 2)
- * (K = ceil(N / 128) key tiles), and writes their O and LSE as usual; the second, a
- * programmatic dependent launch whose CTAs start on the SMs the first one leaves idle, covers
- * keys [128 C, N), waits for the first launch to finish, and merges the two parts into o and lse
- * (LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a + e^(LSE_b - LSE) O_b). The first part's
- * O passes through o in bf16, so those rows carry one extra bf16 rounding of that part.
+ * tiles would leave SMs idle cut the key range of some tiles in two (see attn_fwd_tail_units)
+ * and make a second launch: the first launch covers each such tile's first keys and writes its
+ * O and LSE as usual; the second, a programmatic dependent launch whose CTAs start on the SMs the
+ * first one leaves, covers the rest of the keys, waits for the first launch to finish, and merges
+ * the two parts into o and lse (LSE = ln(e^LSE_a + e^LSE_b), O = e^(LSE_a - LSE) O_a +
+ * e^(LSE_b - LSE) O_b). The first part's O passes through o in bf16, so those rows carry one
+ * extra bf16 rounding of that part. Which tiles are cut (T work tiles, G SMs, K = ceil(N / 128)
+ * key tiles):
+ *   - bf16 at d <= 128, T > G, T not a multiple of G, K >= 8: the tiles after the first
+ *     M = (floor(T / G) - 1) G go to the CTAs in G equal shares of their W = (T - M) K key
+ *     tiles (share c: [floor(c W / G), floor((c + 1) W / G)), counting key tile j of tile M + i
+ *     as i K + j), so every CTA processes the same number of key tiles; a tile a share boundary
+ *     falls inside is cut there;
+ *   - otherwise, when the last wave holds R <= G / 2 tiles and K >= 16: those R tiles, at key
+ *     tile floor(K / 2).
  *
  * Errors: argument problems return ATTN_ERR_INVALID_ARG / ATTN_ERR_UNSUPPORTED synchronously
  * and launch nothing. A failed launch returns ATTN_ERR_CUDA. A kernel that gives up a bounded
@@ -88,14 +96,25 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        const float* descale_v, cudaStream_t stream);
 
 /*
- * attn_fwd_halved_tail_tiles — how many work tiles of an attn_fwd call (and of the fp8 variants
- * with the same shape) have their key range halved across two launches: the tiles of the last
- * wave, when causal == 0, ceil(N / 128) >= 16 and that wave holds at most half as many tiles as
- * the device has SMs (work tiles: B * H * ceil(N / R), R = 256 for d <= 128, 128 for d == 256).
- * 0 means one launch. Host-only; uses 152 SMs when no device can be queried; returns 0 for
- * invalid sizes.
+ * attn_fwd_halved_tail_tiles — how many work tiles of a bf16 attn_fwd call have their key range
+ * cut in two across two launches, by the rule under attn_fwd's "Launches" (work tiles:
+ * B * H * ceil(N / R), R = 256 for d <= 128, 128 for d == 256); attn_fwd_tail_units gives the
+ * count for either dtype. 0 means one launch. Host-only; uses 152 SMs when no device can be
+ * queried; returns 0 for invalid sizes.
  */
 int attn_fwd_halved_tail_tiles(int B, int H, int N, int d, int causal);
+
+/*
+ * attn_fwd_tail_units — the cut tiles themselves of an attn_fwd call of this dtype (the e4m3
+ * entry points with per-head or block descales follow the e4m3 rule), in the second launch's
+ * order: for unit u, tiles[u] is the work tile and kv0[u] the first key tile (of 128 keys) the
+ * second launch covers for it. Work tile t of a non-causal call is query block t % n_mb of
+ * (batch, head) ((t / n_mb) / H, (t / n_mb) % H), n_mb = ceil(N / R). Writes at most cap units
+ * into the HOST arrays tiles and kv0 (either may be NULL when cap is 0) and returns the unit
+ * count (0: one launch; also for invalid sizes or dtype). Host-only.
+ */
+int attn_fwd_tail_units(int B, int H, int N, int d, int causal, attn_dtype_t dtype, int* tiles, int* kv0,
+                        int cap);
 
 /*
  * attn_fwd_fp8_scaled — attn_fwd for e4m3 q, k, v with descale factors that vary by batch and

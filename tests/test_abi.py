@@ -193,23 +193,55 @@ def test_split_heuristic_bounds(lib):
 
 
 def test_halved_tail_rule(lib):
-    """The last wave is halved along the keys only for non-causal calls whose last wave would
-    leave more than half of the 152 SMs idle and whose halves keep at least eight key tiles."""
+    """Non-causal bf16 calls at d <= 128 with more than one wave that is not a whole number of
+    waves deal the tiles after the last whole round but one in 152 equal shares of key tiles (at
+    least 8 key tiles per tile), each share boundary inside a tile cutting that tile; otherwise a
+    last wave filling at most half of the 152 SMs is halved when its tiles have at least 16 key
+    tiles."""
     f = binding.attn_fwd_halved_tail_tiles
-    assert f(2, 8, 4096, 256, False) == 56      # 512 tiles: three waves of 152, then 56
-    assert f(1, 16, 8192, 128, False) == 56     # 16 heads x 32 blocks of 256 rows
-    assert f(1, 16, 16384, 64, False) == 0      # 1024 tiles: last wave of 112 > 76
+    # 512 tiles: whole rounds 0..303, then 208 tiles of 64 key tiles in 152 shares; the boundaries
+    # floor(c W / 152) that are not multiples of 64
+    assert f(1, 16, 8192, 128, False) == 144
+    # d = 256 keeps the halved last wave: 512 tiles, three waves of 152, then 56
+    assert f(2, 8, 4096, 256, False) == 56
+    assert f(1, 16, 16384, 64, False) == 144    # 1024 tiles of 128 key tiles
     assert f(2, 32, 8192, 128, True) == 0       # causal: longest-first deal instead
-    assert f(1, 8, 2048, 128, False) == 64      # one wave of 64 tiles
+    assert f(1, 19, 8192, 128, False) == 0      # 608 tiles: four whole waves
+    assert f(1, 8, 2048, 128, False) == 64      # one wave of 64 tiles, halved
     assert f(1, 8, 1920, 128, False) == 0       # 15 key tiles: halves too short
     assert f(1, 2, 256, 64, False) == 0
     assert f(0, 8, 4096, 128, False) == 0
     assert f(1, 8, 4096, 96, False) == 0
     # the half-the-SMs boundary (d = 256: 128-row tiles): 4 heads x 19 blocks = 76 tiles are
-    # halved, 4 x 20 = 80 are not; 16 key tiles is the shortest range that is cut
+    # halved, 4 x 20 = 80 are not; 16 key tiles is the shortest range that is halved
     assert f(1, 4, 2432, 256, False) == 76
     assert f(1, 4, 2560, 256, False) == 0
     assert f(1, 4, 2048, 256, False) == 64
     assert f(1, 4, 1920, 256, False) == 0
     # a second wave of exactly 76 tiles (152 + 76 = 228 = 12 heads x 19 blocks) is halved
     assert f(1, 12, 2432, 256, False) == 76
+    # 156 tiles (39 heads x 4 blocks): 8 key tiles per tile is the shortest that is cut (shares of
+    # 8.2 key tiles), 7 is not
+    assert f(1, 39, 1024, 128, False) == 132
+    assert f(1, 39, 896, 128, False) == 0
+
+
+def test_tail_units(lib):
+    """The cut tiles in the second launch's order: halved tiles all at the middle; shares: every
+    unit in the tiles after the whole rounds, each tile once, longest second part first."""
+    units = binding.attn_fwd_tail_units(1, 8, 2048, 128, False)
+    assert units == [(t, 8) for t in range(64)]
+    # e4m3 keeps the halved last wave: 512 tiles, the last 56 cut at key tile 32
+    assert binding.attn_fwd_tail_units(1, 16, 8192, 128, False, fp8=True) == [(t, 32) for t in range(456, 512)]
+    units = binding.attn_fwd_tail_units(1, 16, 8192, 128, False)   # 512 tiles, 64 key tiles
+    assert len(units) == binding.attn_fwd_halved_tail_tiles(1, 16, 8192, 128, False) == 144
+    tiles = [t for t, _ in units]
+    kv0 = [j for _, j in units]
+    assert len(set(tiles)) == len(tiles)
+    assert all(304 <= t < 512 for t in tiles) and all(0 < j < 64 for j in kv0)
+    assert kv0 == sorted(kv0)
+    # each share of 13312 / 152 = 87.6 key tiles ends inside at most one tile, so a unit's
+    # tile is the one its boundary falls in: boundary = (t - 304) * 64 + j
+    bounds = sorted((t - 304) * 64 + j for t, j in units)
+    assert bounds == [s for s in (c * 13312 // 152 for c in range(1, 152)) if s % 64]
+    assert binding.attn_fwd_tail_units(2, 32, 8192, 128, True) == []

@@ -1,18 +1,19 @@
 """bench.py's kernel-launch accounting (the `gpu_launches` key) against the library's own launch
-rules, on the CPU: a non-causal forward whose last wave is halved makes two launches, split-KV
+rules, on the CPU: a non-causal forward that cuts tiles' keys across launches makes two, split-KV
 decode two (forward + combine), the block-scaled chain five quantiser launches plus the forward."""
 import bench
 from exact_attention_72_gb300 import binding, inputs
 
 
-def test_forward_launch_counts_follow_the_halving_rule():
+def test_forward_launch_counts_follow_the_cutting_rule():
     for w in inputs.WORKLOADS.values():
-        halved = binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) > 0
-        assert bench.launches_per_step(w) == (2 if halved else 1), w.name
+        cut = len(binding.attn_fwd_tail_units(w.B, w.H, w.N, w.d, w.causal, fp8=w.dtype != "bf16")) > 0
+        assert bench.launches_per_step(w) == (2 if cut else 1), w.name
     assert bench.launches_per_step(inputs.WORKLOADS["noncausal_bf16_n4096_d256"]) == 2
     assert bench.launches_per_step(inputs.WORKLOADS["fp8_noncausal_n8192_d128"]) == 2
     assert bench.launches_per_step(inputs.WORKLOADS["causal_gqa_bf16_n8192_d128"]) == 1
-    assert bench.launches_per_step(inputs.WORKLOADS["noncausal_bf16_n16384_d64"]) == 1
+    # 1024 tiles on 152 SMs: the last 264 dealt in equal shares of key tiles
+    assert bench.launches_per_step(inputs.WORKLOADS["noncausal_bf16_n16384_d64"]) == 2
 
 
 def test_decode_and_block_scaled_counts():

@@ -1,10 +1,11 @@
-"""GPU parity of the halved last wave (non-causal prefill).
+"""GPU parity of the non-causal tiles whose keys are cut across two launches.
 
-When the last wave of work tiles would leave more than half of the SMs idle, attn_fwd cuts those
-tiles' keys in two: the first launch covers key tiles [0, K/2) and writes O and LSE, a dependent
-launch covers the rest and merges. Every case below makes the library halve some tiles (asserted through
-attn_fwd_halved_tail_tiles) and compares every row of the halved heads, and of a head that was not
-halved, with the fp64 oracle.
+When the last wave of work tiles would leave SMs idle, attn_fwd cuts some tiles' keys in two: the
+first launch covers a tile's first key tiles and writes O and LSE, a dependent launch covers the
+rest and merges. One partial wave filling at most half of the SMs is halved; more than one wave is
+dealt in equal shares of key tiles, cutting the tiles the share boundaries fall in. Every case
+below makes the library cut some tiles (asserted through attn_fwd_tail_units) and compares every
+row of the cut heads, and of a head that was not cut, with the fp64 oracle.
 """
 import numpy as np
 import pytest
@@ -50,14 +51,46 @@ def test_halved_tiles_match_oracle(w):
     compare_heads(w, o, lse, oracle_heads(w, x, all_heads(w)))
 
 
-def test_second_wave_tail():
-    """160 tiles on 152 SMs: 152 whole tiles, then 8 halved ones (all of head 19)."""
-    w = case("two_waves", H=20, Hkv=4, N=2048, seed=97)
-    assert binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal) == 8
+def cut_heads(w):
+    """(batch, head) pairs holding a cut tile, from the library's list of cut tiles."""
+    rpt = 256 if w.d <= 128 else 128
+    n_mb = -(-w.N // rpt)
+    return sorted({divmod(t // n_mb, w.H) for t, _ in binding.attn_fwd_tail_units(w.B, w.H, w.N, w.d, w.causal)})
+
+
+SHARE_CASES = [
+    # 160 tiles of 16 key tiles on 152 SMs: shares of 16.8 key tiles over all tiles
+    case("shares_160", H=20, Hkv=4, N=2048, seed=97),
+    # 320 tiles: one whole round, then 168 tiles in shares (GQA)
+    case("shares_after_a_round", H=20, Hkv=5, N=4096, seed=101),
+    # d = 64: 160 tiles of 64 key tiles
+    case("shares_d64", H=5, Hkv=1, N=8192, d=64, seed=102),
+    # ragged: 162 tiles of 17 key tiles, the last one 52 keys long, the last query block 52 rows
+    case("shares_ragged", H=18, Hkv=6, N=2100, seed=103),
+    # shares of about 8 key tiles, every tile 8 key tiles: most tiles cut
+    case("shares_short", B=3, H=13, Hkv=13, N=1024, seed=104),
+    case("shares_outliers", H=20, Hkv=4, N=2048, seed=105, k_outlier_frac=0.005),
+]
+
+
+@pytest.mark.parametrize("w", SHARE_CASES, ids=lambda w: w.name)
+def test_shared_tail_matches_oracle(w):
+    units = binding.attn_fwd_tail_units(w.B, w.H, w.N, w.d, w.causal)
+    assert len(units) > 0 and any(j != (-(-w.N // 128)) // 2 for _, j in units)
+    heads = cut_heads(w)
     x = inputs.make_inputs(w)
     o, lse = run_cuda(w, x)
-    compare_heads(w, o, lse, oracle_heads(w, x, [(0, 0), (0, 18), (0, 19)]))
+    whole = [(0, 0)] if (0, 0) not in heads else []
+    compare_heads(w, o, lse, oracle_heads(w, x, heads + whole))
     check_convex_hull(w, x, o)
+
+
+def test_shared_tail_repeatable_bitwise():
+    w = SHARE_CASES[1]
+    x = inputs.make_inputs(w)
+    o1, l1 = run_cuda(w, x)
+    o2, l2 = run_cuda(w, x)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
 def test_halved_repeatable_bitwise():
@@ -96,13 +129,13 @@ def test_halved_rows_error_against_whole_rows(name):
     computed whole: both within the bar, and the halved rows' worst error within 2x the whole
     rows' (the figures are printed)."""
     w = inputs.WORKLOADS[name]
-    nh = binding.attn_fwd_halved_tail_tiles(w.B, w.H, w.N, w.d, w.causal)
+    units = binding.attn_fwd_tail_units(w.B, w.H, w.N, w.d, w.causal, fp8=w.dtype != "bf16")
+    nh = len(units)
     assert nh > 0
     rpt = 256 if w.d <= 128 else 128
     n_mb = -(-w.N // rpt)
-    tiles = w.B * w.H * n_mb
     halved = {}
-    for t in range(tiles - nh, tiles):   # non-causal tiles: head-major, query blocks in order
+    for t, _ in units:   # non-causal tiles: head-major, query blocks in order
         b, h = divmod(t // n_mb, w.H)
         mb = t % n_mb
         halved.setdefault((b, h), []).extend(range(mb * rpt, min(w.N, (mb + 1) * rpt)))
