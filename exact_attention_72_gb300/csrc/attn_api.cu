@@ -853,6 +853,7 @@ attn_status_t attn_quantize_e4m3(const void* x, void* x8, float* descale, int B,
   q.nspan = (int)nspan;
   q.chunk_rows = chunk_rows;
   q.grp_rows = std::min(block_rows, chunk_rows);
+  q.x8_v8 = aligned(x8, 32) ? 1 : 0;
   q.status = di->status;
   q.timeout_ns = g_timeout_ns ? g_timeout_ns : kDefaultTimeoutNs;
   q.num_sms = di->num_sms;

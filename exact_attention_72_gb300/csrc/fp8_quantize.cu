@@ -327,6 +327,217 @@ __global__ void __launch_bounds__(QCfg<D, ROT>::THREADS) quantize_kernel(const _
   }
 }
 
+// One row per thread, for d = 64 and 128 and blocks of at most 128 rows. A CTA of 128 threads
+// takes a chunk of up to 128 rows and thread r holds row r in registers (d fp32 values as pairs):
+// the Walsh-Hadamard butterflies need no shuffles, and a block's maximum takes a warp reduction
+// plus, for blocks of 64 or 128 rows, one exchange through shared memory at the chunk's single
+// CTA barrier. Three CTAs share an SM, each with its own ring of TMA stages. Each thread writes
+// its row of codes in 32-byte stores (one whole sector per lane) where x8 allows it.
+template <int D>
+struct RowCfg {
+  static constexpr int THREADS = 128;
+  static constexpr int NP = D / 2;                          // fp32 pairs per row
+  static constexpr int SLAB_BYTES = kChunkRows * 128;       // one 64-column slab of a stage
+  static constexpr int STAGE_BYTES = (D / 64) * SLAB_BYTES;
+  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+};
+
+// Row r of a stage (D bf16 values) as D/2 packed words; the 16-byte piece c of a 128-byte slab
+// line sits at c ^ (r % 8) (128-byte swizzle).
+template <int D>
+__device__ __forceinline__ void load_row(const uint8_t* stage, int r, uint32_t* w) {
+#pragma unroll
+  for (int p = 0; p < D / 8; ++p) {
+    const int slab = p >> 3, c = p & 7;
+    const uint4 t = *reinterpret_cast<const uint4*>(stage + slab * (kChunkRows * 128) + r * 128 + ((c ^ (r & 7)) << 4));
+    w[4 * p] = t.x;
+    w[4 * p + 1] = t.y;
+    w[4 * p + 2] = t.z;
+    w[4 * p + 3] = t.w;
+  }
+}
+
+// v <- v diag(sigma) H_D for a whole row in registers (pairs v[j] = (y_2j, y_2j+1)): a butterfly
+// on index bit b maps (y_e, y_{e+2^b}) with bit b of e clear to (y_e + y_{e+2^b}, y_e - y_{e+2^b});
+// bit 0 works inside each pair, bit b >= 1 on pairs j and j + 2^(b-1).
+template <int D>
+__device__ __forceinline__ void rotate_row(uint64_t* v, const float* sg) {
+  using namespace gb300;
+  constexpr int NP = D / 2;
+#pragma unroll
+  for (int j = 0; j < NP; j += 2) {
+    const float4 s4 = *reinterpret_cast<const float4*>(sg + 2 * j);   // same address in every lane
+    v[j] = f2_mul(v[j], f2_pack(s4.x, s4.y));
+    v[j + 1] = f2_mul(v[j + 1], f2_pack(s4.z, s4.w));
+  }
+#pragma unroll
+  for (int j = 0; j < NP; ++j) {
+    float a, b;
+    f2_unpack(v[j], a, b);
+    v[j] = f2_pack(a + b, a - b);
+  }
+#pragma unroll
+  for (int st = 1; st < NP; st <<= 1)
+#pragma unroll
+    for (int j = 0; j < NP; ++j)
+      if (!(j & st)) {
+        const uint64_t a = v[j], b = v[j + st];
+        v[j] = f2_add(a, b);
+        v[j + st] = f2_sub(a, b);
+      }
+}
+
+// MODE as for quantize_kernel: 0 whole blocks per chunk (codes and descales), 1 chunk maxima of
+// longer blocks (atomic max into the block's slot), 2 codes from the block maximum in the slot.
+// Row r of chunk cp as codes x / ds (the division as div_by_descale), D bytes in 32-byte stores
+// where x8 allows it.
+template <int D>
+__device__ __forceinline__ void store_row_codes(const gb300::QuantLaunch& a, const ChunkPos& cp, int r,
+                                                const uint64_t* v, const DivConsts& dc) {
+  using namespace gb300;
+  uint32_t wd[D / 4];   // four codes per word, the lowest-addressed in the low byte
+#pragma unroll
+  for (int j = 0; j < D / 2; j += 2) {
+    float a0, a1, b0, b1;
+    f2_unpack(div_by_descale(v[j], dc), a0, a1);
+    f2_unpack(div_by_descale(v[j + 1], dc), b0, b1);
+    const uint32_t lo = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a0, a1), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(b0, b1), __NV_SATFINITE, __NV_E4M3);
+    wd[j >> 1] = __byte_perm(lo, hi, 0x5410);
+  }
+  uint8_t* dst = a.x8 + ((size_t)(cp.b * a.N + cp.row_begin + r) * a.Hx + cp.h) * D;
+  if (a.x8_v8) {
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) st_global_v8(dst + 32 * i, wd + 8 * i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+      reinterpret_cast<uint4*>(dst)[i] = make_uint4(wd[4 * i], wd[4 * i + 1], wd[4 * i + 2], wd[4 * i + 3]);
+  }
+}
+
+template <int D, int MODE, bool ROT>
+__global__ void __launch_bounds__(RowCfg<D>::THREADS, 3)
+    quantize_rows_kernel(const __grid_constant__ CUtensorMap tm, const gb300::QuantLaunch a, int n_chunks) {
+  using C = RowCfg<D>;
+  using namespace gb300;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[C::STAGES];
+  __shared__ float red[2][4];                  // per-warp maxima, alternating between chunks
+  __shared__ __align__(16) float sg[ROT ? D : 4];
+  __shared__ uint32_t abort_flag;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < C::STAGES; ++i) mbar_init(smem_addr(&full[i]), 1);
+    fence_mbar_init();
+    abort_flag = 0u;
+    tma_prefetch_desc(&tm);
+  }
+  if constexpr (ROT)
+    for (int i = tid; i < D; i += C::THREADS) sg[i] = __ldg(a.signs + i);
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, a.status, a.timeout_ns};
+  const uint32_t chunk_bytes = (uint32_t)a.chunk_rows * D * 2;   // boxes past N count in full
+  auto issue = [&](int c, int stage) {
+    const ChunkPos cp = chunk_pos(c, a);
+    const uint32_t bar = smem_addr(&full[stage]);
+    mbar_arrive_expect_tx(bar, chunk_bytes);
+#pragma unroll
+    for (int sl = 0; sl < D / 64; ++sl)
+      tma_load_4d(smem_addr(smem + stage * C::STAGE_BYTES + sl * C::SLAB_BYTES), &tm, bar, 64 * sl, cp.row_begin, cp.h,
+                  cp.b);
+  };
+  if (tid == 0)
+    for (int i = 0; i < C::STAGES; ++i) {
+      const int c = blockIdx.x + i * gridDim.x;
+      if (c < n_chunks) issue(c, i);
+    }
+  // Rows reduced together: a block of grp_rows rows (a power of two) inside a 128-row chunk, or
+  // the whole chunk when the chunk is one block (rows past its end contribute 0).
+  const int span_rows =
+      (MODE == 0 && a.chunk_rows == kChunkRows && (a.grp_rows & (a.grp_rows - 1)) == 0) ? a.grp_rows : kChunkRows;
+  const int r = tid;
+  int k = 0;
+  bool ok = true;
+  for (int c = blockIdx.x; c < n_chunks; c += gridDim.x, ++k) {
+    const int stage = k % C::STAGES;
+    const bool w = mbar_wait(smem_addr(&full[stage]), (uint32_t)(k / C::STAGES) & 1u, ctl, kSiteQuantFull);
+    if (!__all_sync(0xffffffffu, w)) {
+      ok = false;
+      break;
+    }
+    const ChunkPos cp = chunk_pos(c, a);
+    const bool valid = r < cp.row_end - cp.row_begin;
+    uint32_t raw[C::NP];
+    uint64_t v[C::NP];
+    load_row<D>(smem + stage * C::STAGE_BYTES, r, raw);
+#pragma unroll
+    for (int j = 0; j < C::NP; ++j) v[j] = f2_pack(__uint_as_float(raw[j] << 16), __uint_as_float(raw[j] & 0xFFFF0000u));
+    if constexpr (ROT) rotate_row<D>(v, sg);
+    if constexpr (MODE == 2) {
+      // The block maximum the maxima launch left in the slot; the stage is read.
+      __syncthreads();
+      if (tid == 0) {
+        const int next = c + C::STAGES * gridDim.x;
+        if (next < n_chunks) issue(next, stage);
+      }
+      if (valid) {
+        const float ds2 = descale_of(a.descale[((size_t)cp.b * a.Hx + cp.h) * a.nblk + cp.row_begin / a.block_rows]);
+        store_row_codes<D>(a, cp, r, v, div_consts(ds2));
+      }
+      continue;
+    }
+    float amax = 0.0f;
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < C::NP; ++j) {
+        float lo, hi;
+        f2_unpack(v[j], lo, hi);
+        amax = fmax3(amax, fabsf(lo), fabsf(hi));
+      }
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1)
+      if (m < span_rows) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+    float* rk = red[k & 1];
+    if (lane == 0) rk[warp] = amax;
+    __syncthreads();   // every row of the stage is in registers, every warp's maximum is in rk
+    if (tid == 0) {
+      const int next = c + C::STAGES * gridDim.x;
+      if (next < n_chunks) issue(next, stage);
+    }
+    if (span_rows > 32) {
+      const int w0 = (warp * 32 / span_rows) * (span_rows / 32);
+      for (int i = 0; i < span_rows / 32; ++i) amax = fmaxf(amax, rk[w0 + i]);
+    }
+    float* slot = a.descale + ((size_t)cp.b * a.Hx + cp.h) * a.nblk;
+    if constexpr (MODE == 1) {
+      // non-negative floats order like their bit patterns
+      if (tid == 0 && cp.row_begin < cp.row_end)
+        atomicMax(reinterpret_cast<unsigned int*>(slot + cp.row_begin / a.block_rows), __float_as_uint(amax));
+      continue;
+    }
+    const float ds = descale_of(amax);
+    const int grp_row0 = (r / span_rows) * span_rows;   // first row of this thread's group
+    if (r == grp_row0 && grp_row0 < cp.row_end - cp.row_begin)
+      slot[(cp.row_begin + grp_row0) / a.block_rows] = stored_descale<D>(ds, ROT);
+    if (valid) store_row_codes<D>(a, cp, r, v, div_consts(ds));
+  }
+  if (!ok && tid == 0) {
+    // Copies this CTA issued and never consumed get a bounded time to land before it exits.
+    for (int i = 0; i < C::STAGES; ++i) {
+      const int kk = k + i;
+      if (blockIdx.x + kk * gridDim.x >= n_chunks) break;
+      const uint32_t bar = smem_addr(&full[kk % C::STAGES]);
+      const uint64_t t0 = global_timer_ns();
+      while (!mbar_try_wait(bar, (uint32_t)(kk / C::STAGES) & 1u) && global_timer_ns() - t0 < a.timeout_ns) {
+      }
+    }
+  }
+}
+
 // Block maxima -> descales, in place.
 template <int D>
 __global__ void finalize_descale_kernel(float* descale, int n, bool rotated) {
@@ -348,15 +559,37 @@ cudaError_t launch_mode(const gb300::QuantLaunch& q, int n_chunks, cudaStream_t 
   return cudaGetLastError();
 }
 
+template <int D, int MODE, bool ROT>
+cudaError_t launch_rows(const gb300::QuantLaunch& q, int n_chunks, cudaStream_t s) {
+  using C = RowCfg<D>;
+  auto kern = quantize_rows_kernel<D, MODE, ROT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, C::THREADS, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const int grid = (int)std::min<long long>(n_chunks, (long long)std::max(per_sm, 1) * q.num_sms);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, s>>>(q.tm_x, q, n_chunks);
+  return cudaGetLastError();
+}
+
 template <int D, bool ROT>
 cudaError_t launch_quantize(const gb300::QuantLaunch& q, cudaStream_t s) {
   const int n_chunks = q.B * q.Hx * q.nspan * q.cps;
-  if (q.block_rows <= kChunkRows) return launch_mode<D, 0, ROT>(q, n_chunks, s);
+  if (q.block_rows <= kChunkRows) {
+    if constexpr (D <= 128) return launch_rows<D, 0, ROT>(q, n_chunks, s);
+    else return launch_mode<D, 0, ROT>(q, n_chunks, s);
+  }
   const size_t nds = (size_t)q.B * q.Hx * q.nblk;
   cudaError_t e = cudaMemsetAsync(q.descale, 0, nds * sizeof(float), s);
   if (e != cudaSuccess) return e;
-  if ((e = launch_mode<D, 1, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
-  if ((e = launch_mode<D, 2, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
+  if constexpr (D <= 128) {
+    if ((e = launch_rows<D, 1, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
+    if ((e = launch_rows<D, 2, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
+  } else {
+    if ((e = launch_mode<D, 1, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
+    if ((e = launch_mode<D, 2, ROT>(q, n_chunks, s)) != cudaSuccess) return e;
+  }
   finalize_descale_kernel<D><<<(unsigned)((nds + 255) / 256), 256, 0, s>>>(q.descale, (int)nds, ROT);
   return cudaGetLastError();
 }

@@ -54,6 +54,7 @@ struct QuantLaunch {
   const float* signs;       // d values or null
   int B, N, Hx, d, block_rows, nblk;
   int span, cps, nspan, chunk_rows, grp_rows;
+  int x8_v8;                // x8 is 32-byte aligned: rows of codes go out in 32-byte stores
   uint32_t* status;
   unsigned long long timeout_ns;
   int num_sms;
