@@ -1103,18 +1103,30 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (C::NQ == 2 || buf == 0) ++s_cnt0;
           else ++s_cnt1;
         }
+        // Masking: keys past N (ragged tail) and, on the diagonal tile, keys after the query row.
+        const int jk = tc.j0 + j;   // KV tile index within the sequence
+        // Varlen causal masking is bottom-right aligned (query i sees keys <= i + Nk - Nq), so up
+        // to two tiles can cross the diagonal; with equal lengths only the last one does.
+        const int diag_off = C::VARLEN ? Nk - tc.nq : 0;
+        const bool diag = C::CAUSAL && (C::VARLEN ? (jk * C::BN + C::BN - 1 > row0 + diag_off) : (j == n - 1));
+        const bool tail = (jk == tc.n_kvt - 1) && (Nk % C::BN != 0);
+        const bool masked = diag || tail;
         tc_fence_after();
         uint32_t sr[128];
+        // The TMEM loads also give each lane's maximum per 32 columns: the row maximum of an
+        // unmasked tile. A masked tile's maximum must skip its masked keys and is taken below.
+        float mq0, mq1, mq2, mq3;
         const uint32_t tS = tmem + lane_base + s_col;
-        tmem_ld_32cols(tS, sr);
-        tmem_ld_32cols(tS + 32, sr + 32);
-        tmem_ld_32cols(tS + 64, sr + 64);
-        tmem_ld_32cols(tS + 96, sr + 96);
+        tmem_ld_32cols_max(tS, sr, mq0);
+        tmem_ld_32cols_max(tS + 32, sr + 32, mq1);
+        tmem_ld_32cols_max(tS + 64, sr + 64, mq2);
+        tmem_ld_32cols_max(tS + 96, sr + 96, mq3);
         tmem_ld_wait();
         reg_fence32(sr);
         reg_fence32(sr + 32);
         reg_fence32(sr + 64);
         reg_fence32(sr + 96);
+        asm volatile("" : "+f"(mq0), "+f"(mq1), "+f"(mq2), "+f"(mq3));
         if constexpr (C::PSMEM) {
           // S is in registers: the issuer may put S_{j+1} into this buffer now.
           tc_fence_before();
@@ -1125,14 +1137,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         float x[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-        // Masking: keys past N (ragged tail) and, on the diagonal tile, keys after the query row.
-        const int jk = tc.j0 + j;   // KV tile index within the sequence
-        // Varlen causal masking is bottom-right aligned (query i sees keys <= i + Nk - Nq), so up
-        // to two tiles can cross the diagonal; with equal lengths only the last one does.
-        const int diag_off = C::VARLEN ? Nk - tc.nq : 0;
-        const bool diag = C::CAUSAL && (C::VARLEN ? (jk * C::BN + C::BN - 1 > row0 + diag_off) : (j == n - 1));
-        const bool tail = (jk == tc.n_kvt - 1) && (Nk % C::BN != 0);
-        if (diag || tail) {
+        if (masked) {
           int lim = Nk - jk * C::BN;
           if (diag) lim = min(lim, (row0 + r + diag_off) - jk * C::BN + 1);
 #pragma unroll
@@ -1225,10 +1230,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
         exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
         if (r == 0) ATTN_TRACE(16, qt, j);
-        // Row max: eight independent chains of 3-input max (per 64-key half for fp8, whose halves
-        // may carry different K descales; the scales are positive, so max commutes with them).
+        // Row max (per 64-key half for fp8, whose halves may carry different K descales; the scales
+        // are positive, so max commutes with them): the loads' maxima on an unmasked tile, else
+        // eight independent chains of 3-input max over the masked scores.
         float m_tile;
-        if constexpr (C::FP8) {
+        if (!masked) {
+          if constexpr (C::FP8) m_tile = fmaxf(fmaxf(mq0, mq1) * s_lo, fmaxf(mq2, mq3) * s_hi);
+          else m_tile = fmaxf(fmaxf(mq0, mq1), fmaxf(mq2, mq3)) * s;
+        } else if constexpr (C::FP8) {
           float mh[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {

@@ -232,6 +232,16 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t* r) {
       : GB300_R8(r, 0), GB300_R8(r, 8), GB300_R8(r, 16), GB300_R8(r, 24)
       : "r"(taddr));
 }
+// The same load with the maximum of the lane's 32 fp32 values taken on the way (sm_103a's
+// tcgen05.ld.red; NaN inputs are ignored, as max.f32 does). mx is valid after tmem_ld_wait.
+__device__ __forceinline__ void tmem_ld_32cols_max(uint32_t taddr, uint32_t* r, float& mx) {
+  asm volatile(
+      "tcgen05.ld.red.sync.aligned.32x32b.x32.max.f32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, %32, [%33];"
+      : GB300_R8(r, 0), GB300_R8(r, 8), GB300_R8(r, 16), GB300_R8(r, 24), "=f"(mx)
+      : "r"(taddr));
+}
 // 16 consecutive columns (x16).
 __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t* r) {
   asm volatile(
