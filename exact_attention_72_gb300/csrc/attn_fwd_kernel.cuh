@@ -378,7 +378,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 // f16 pairs (low half = first element): packing from fp32 (round to nearest), 2^x per element,
-// add, unpacking to fp32, and the e4m3 pair (saturating, round to nearest) of an f16 pair.
+// add, unpacking to fp32, and e4m3 (saturating, round to nearest) from f16 pairs.
 __device__ __forceinline__ uint32_t f16x2_pack(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -399,9 +399,14 @@ __device__ __forceinline__ void f16x2_unpack(uint32_t h2, float& lo, float& hi) 
       : "=f"(lo), "=f"(hi)
       : "r"(h2));
 }
-__device__ __forceinline__ uint32_t e4m3x2_from_f16x2(uint32_t h2) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+// Four e4m3 values from two f16 pairs, the first pair in the low half: the two 16-bit results
+// are joined by one move instead of a shift and an or.
+__device__ __forceinline__ uint32_t e4m3x4_from_f16x2x2(uint32_t lo2, uint32_t hi2) {
+  uint32_t r;
+  asm("{\n .reg .b16 a, b;\n cvt.rn.satfinite.e4m3x2.f16x2 a, %1;\n cvt.rn.satfinite.e4m3x2.f16x2 b, %2;\n"
+      " mov.b32 %0, {a, b};\n}\n"
+      : "=r"(r)
+      : "r"(lo2), "r"(hi2));
   return r;
 }
 
@@ -1168,7 +1173,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const uint32_t h01 = ex2_f16x2(f16x2_pack(t0, t1)), h23 = ex2_f16x2(f16x2_pack(t2, t3));
               hs0 = f16x2_add(hs0, h01);
               hs1 = f16x2_add(hs1, h23);
-              pk[c >> 2] = e4m3x2_from_f16x2(h01) | (e4m3x2_from_f16x2(h23) << 16);
+              pk[c >> 2] = e4m3x4_from_f16x2x2(h01, h23);
             }
             float a0, a1, b0, b1;
             f16x2_unpack(hs0, a0, a1);
