@@ -16,8 +16,10 @@
 //     (mojostudio.in), section 2, the producer's multi-stage TMA pipeline with expected
 //     transaction bytes);
 //   * warp MMA (one thread) issues tcgen05.mma: S = Q K_j^T into tensor memory (TMEM), and
-//     O += P V_j with P read from TMEM (aliasing S) and V from shared memory; at d = 64 a warp of
-//     its own issues the S products into three rotating TMEM buffers (see AttnCfg::S3);
+//     O += P V_j with P read from TMEM and V from shared memory. With two bf16 Q tiles a warp of
+//     its own issues the S products: at d = 64 into three rotating TMEM buffers that P aliases
+//     (AttnCfg::S3), at d = 128 into one buffer both tiles share, P having a TMEM area of its own
+//     (AttnCfg::S1); e4m3 keeps P in shared memory;
 //   * one softmax warpgroup per Q tile (one thread per query row) reads S from TMEM, masks,
 //     takes the row max, evaluates exp2 with the scale folded in, accumulates the row sum,
 //     writes P back to TMEM and rescales O in TMEM when the running max moves;
@@ -128,7 +130,14 @@ struct AttnCfg {
   static constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
   static constexpr int RESERVE = 1024 + 1024;             // alignment slack + static shared
   static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES - P_BYTES) / TILE_BYTES;
-  static constexpr int NS = NS_FIT > 8 ? 8 : NS_FIT;      // K/V ring stages
+  // K/V ring stages. With a dedicated S-issuer warp (two bf16 Q tiles) the count is even, so each
+  // stage holds only K tiles or only V tiles: K stages are waited for by the S issuer alone and V
+  // stages by the PV issuers alone, each of which has waited for the stage's previous load itself.
+  // A parity wait cannot tell phases two apart, and with an odd count a PV issuer whose tile has
+  // no keys in a work tile (a ragged sequence's end) would wait for a V stage whose previous load,
+  // a K tile it never waits for, has not landed, and pass it two phases early.
+  static constexpr int NS_CAP = NS_FIT > 8 ? 8 : NS_FIT;
+  static constexpr int NS = (NQ == 2 && !FP8 && (NS_CAP & 1)) ? NS_CAP - 1 : NS_CAP;
   static constexpr int SMEM_BYTES = Q_BYTES + P_BYTES + NS * TILE_BYTES + 1024;
   static constexpr int KSTEPS_QK = D * ELT / 32;          // one MMA k-step covers 32 bytes of K
   static constexpr int KSTEPS_PV = BN * ELT / 32;
@@ -140,6 +149,15 @@ struct AttnCfg {
   // by a warp of their own (the otherwise idle twelfth warp), so a tile's S_{j+1} is issued as
   // soon as a buffer is free, not behind its PV_j, and is ready when its softmax finishes step j.
   static constexpr bool S3 = (NQ == 2 && D == 64);
+  // Two bf16 Q tiles at d = 128 fill TMEM with two O tiles, so P cannot alias a per-tile S
+  // buffer without chaining S_{j+1} to PV_j. Instead both tiles share one 128-column S buffer
+  // and each writes its P (64 columns of bf16 pairs) to an area of its own: the S issuer puts the
+  // next S into the buffer as soon as the softmax that owns the current one has loaded it into
+  // registers, whatever the PVs are doing. TMEM: S at 0, P of tile q at P_COL + 64 q, O at 256.
+  static constexpr bool S1 = (NQ == 2 && D == 128 && !FP8);
+  static constexpr bool SISS = S3 || S1;                  // a warp of its own issues every S
+  static constexpr int NSB = S3 ? 3 : 1;                  // S buffers the S issuer rotates through
+  static constexpr int P_COL = 128;
   // S-ready, P-ready and PV-done barriers: one per S buffer (one Q tile) or per Q tile (two); in
   // three-buffer mode three per Q tile, the tile's g-th S product using index g % 3. A tile can
   // then have up to three S products (or P halves, or PVs) outstanding without two of them
@@ -157,29 +175,31 @@ struct AttnCfg {
   static constexpr int WARP_S = WARP_LOAD + 1;            // three-buffer mode: the S issuer
   // Two Q tiles: 12 warps (softmax x8, MMA x2, load, and the S issuer at d = 64, else idle) so the
   // third warpgroup can hand registers to the softmax warpgroups with setmaxnreg. The launch gives
-  // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them, or
-  // at d = 64 (whose softmax gains from the room: 0.99 -> 0.97 ms on the 16k-key workload)
-  // 256 x 216 + 128 x 72 = 64,512. The host checks the compiled register count first (an
-  // over-subscribed increase never returns).
+  // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them.
+  // (256 x 216 + 128 x 72 at d = 64 was faster while the softmax took its row maximum with a
+  // max chain; with the maximum from the TMEM loads it is 2.4% slower on the 16k-key workload.)
+  // The host checks the compiled register count first (an over-subscribed increase never
+  // returns).
   static constexpr bool REG_SPLIT = (NQ == 2);
   // With a two-stage ring (d = 256: 64 KB tiles) K_j always takes stage 0 and V_j stage 1. Then
   // K and V get a producer warp each (WARP_LOAD: Q and K, WARP_LOAD + 1: V), so the next K can
   // load as soon as S has read the last one, without queueing behind V's wait for PV.
   static constexpr bool TWO_LOADERS = (NS == 2);
   static constexpr int THREADS = REG_SPLIT ? 384 : (SOFTMAX_WARPS + MMA_WARPS + 1 + (TWO_LOADERS ? 1 : 0)) * 32;
-  static constexpr uint32_t REGS_SOFTMAX = D == 64 ? 216 : 200, REGS_OTHER = D == 64 ? 72 : 96;
+  static constexpr uint32_t REGS_SOFTMAX = 200, REGS_OTHER = 96;
   static constexpr int REGS_NEEDED = SOFTMAX_WARPS * 32 * REGS_SOFTMAX + 128 * REGS_OTHER;
   static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
   static constexpr uint32_t IDESC_QK = make_idesc(FMT, 128, BN, false, false);
   static constexpr uint32_t IDESC_PV = make_idesc(FMT, 128, D, false, true);
   static_assert(NS >= 2, "K/V ring needs at least two stages");
+  static_assert(!SISS || NS % 2 == 0, "an S-issuer warp needs an even number of K/V stages");
   static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
   static_assert(D % CE == 0, "head dim must fill whole 128-byte rows");
 };
 
 // Wait-site codes recorded in the status word when a bounded wait gives up.
 enum : uint32_t { SITE_Q_EMPTY = 1, SITE_KV_EMPTY = 2, SITE_Q_FULL = 3, SITE_KV_FULL = 4, SITE_P_FULL = 5,
-                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9, SITE_S_TURN = 10,
+                  SITE_S_FULL = 6, SITE_O_DONE = 7, SITE_DRAIN = 8, SITE_O_FULL = 9,
                   SITE_S_FREE = 12 };
 
 struct TileCoord {
@@ -308,10 +328,10 @@ __device__ __forceinline__ int kv_tiles_for(const TileCoord& tc, int qt, const A
   return pos0 / C::BN + 1;
 }
 
-// Three-buffer mode: the position of Q tile qt's S_j among all S products of the CTA, in issue
+// S issuer modes: the position of Q tile qt's S_j among all S products of the CTA, in issue
 // order, for a work tile whose two Q tiles visit n0 and n1 KV tiles, given the count issued before
-// the work tile. The two issuers alternate turns (S0_j, then S1_j) and skip the turns of S
-// products their tile does not need, so that order is fixed. S number k lives in buffer k % 3.
+// the work tile. The S issuer takes S0_j, then S1_j, skipping the S products a tile does not
+// need, so that order is fixed. S number k lives in buffer k % NSB.
 __device__ __forceinline__ uint32_t s_number(uint32_t sbase, int qt, int j, int n0, int n1) {
   return sbase + (uint32_t)(min(j, n0) + min(j, n1) + ((qt == 1 && j < n0) ? 1 : 0));
 }
@@ -478,11 +498,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // kv_empty / q_empty take one arrival per MMA-issuer warp (a tcgen05.commit after the MMAs
   // that read the stage, or a plain arrive for a stage that warp's Q tile does not need).
-  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain[C::MMA_WARPS + (C::S3 ? 1 : 0)];
-  // s_turn[q]: issuer q may take its next S turn. The two issuers alternate S issues
-  // (S0_j, S1_j, S0_{j+1}, ...), which keeps the two Q tiles' softmax phases staggered so the
-  // tensor core always has the other tile's GEMMs to run.
-  __shared__ __align__(8) uint64_t bar_s_turn[2];
+  __shared__ __align__(8) uint64_t bar_q_full, bar_q_empty, bar_drain[C::MMA_WARPS + (C::SISS ? 1 : 0)];
   __shared__ __align__(8) uint64_t bar_kv_full[C::NS], bar_kv_empty[C::NS];
   // o_done: one phase per PV product (rescale waits); o_full: one phase per work tile, after its
   // last PV (epilogue waits). With one Q tile the S MMAs run a step ahead of the PVs, so at the
@@ -493,7 +509,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // reused only after the PV that read it has been issued).
   // s_free[b] (three-buffer mode): the PV that read S buffer b has completed, so b can take a new S.
   __shared__ __align__(8) uint64_t bar_s_full[C::N_SBAR], bar_p_half[C::N_SBAR][2], bar_o_done[C::N_OBAR], bar_o_full[C::NQ];
-  __shared__ __align__(8) uint64_t bar_s_free[C::S3 ? 3 : 1];
+  // s_free[b] (S issuer modes): S buffer b may take a new S. Three S buffers: the PV that read P
+  // from b has completed (one commit). Shared S buffer: the softmax warps that own the S in it
+  // have loaded it (one arrival per warp).
+  __shared__ __align__(8) uint64_t bar_s_free[C::SISS ? C::NSB : 1];
   // s_read[q] (P in shared memory): the softmax warps of Q tile q have loaded S from TMEM.
   __shared__ __align__(8) uint64_t bar_s_read[C::NQ];
   __shared__ uint32_t tmem_slot;
@@ -517,15 +536,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     abort_flag = 0u;
     mbar_init(smem_addr(&bar_q_full), 1);
     mbar_init(smem_addr(&bar_q_empty), C::MMA_WARPS);
-    for (int i = 0; i < C::MMA_WARPS + (C::S3 ? 1 : 0); ++i) mbar_init(smem_addr(&bar_drain[i]), 1);
-    mbar_init(smem_addr(&bar_s_turn[0]), 1);
-    mbar_init(smem_addr(&bar_s_turn[1]), 1);
+    for (int i = 0; i < C::MMA_WARPS + (C::SISS ? 1 : 0); ++i) mbar_init(smem_addr(&bar_drain[i]), 1);
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(smem_addr(&bar_kv_full[i]), 1);
       mbar_init(smem_addr(&bar_kv_empty[i]), C::MMA_WARPS);
     }
-    if constexpr (C::S3)
-      for (int i = 0; i < 3; ++i) mbar_init(smem_addr(&bar_s_free[i]), 1);
+    if constexpr (C::SISS)
+      for (int i = 0; i < C::NSB; ++i) mbar_init(smem_addr(&bar_s_free[i]), C::S1 ? 4 : 1);
     if constexpr (C::PSMEM)
       for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_s_read[i]), 4);
     for (int i = 0; i < C::N_SBAR; ++i) {
@@ -538,7 +555,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     for (int i = 0; i < C::N_OBAR; ++i) mbar_init(smem_addr(&bar_o_done[i]), 1);
     for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_o_full[i]), 1);
     fence_mbar_init();
-    mbar_arrive(smem_addr(&bar_s_turn[0]));   // issuer 0 takes the first S turn
   }
   if (warp == C::WARP_MMA) {
     tmem_alloc(smem_addr(&tmem_slot), C::TMEM_COLS);
@@ -706,7 +722,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       const int myq = warp - C::WARP_MMA;   // Q tile (and S/P buffer) this warp issues for
-      uint32_t ring = 0, nq_loads = 0, p_cnt = 0, turns = 0;
+      uint32_t ring = 0, nq_loads = 0, p_cnt = 0;
       bool ok = true;
 
       auto wait_kv = [&](uint32_t pos) -> bool {
@@ -720,21 +736,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       const uint32_t d_s = tmem + (myq ? C::S_COL1 : C::S_COL0);
       const uint32_t d_o = tmem + C::O_COL + myq * C::D;
       const uint32_t a_q = sQ + myq * C::TILE_BYTES;
-      // One S turn: wait for this issuer's turn, issue S (if this Q tile needs it), pass the turn.
-      // With P in shared memory (e4m3) S_{j+1} waits only for the softmax to have loaded S_j; there
-      // the turns cost 3% (C5), so they are skipped.
-      auto s_turn = [&](bool issue, uint32_t k_addr) -> bool {
-        if constexpr (!C::PSMEM) {
-          if (!mbar_wait(smem_addr(&bar_s_turn[myq]), turns & 1, ctl, SITE_S_TURN)) return false;
-          ++turns;
-        }
+      // S of this Q tile into its own S buffer (P in shared memory). The two issuers do not take
+      // turns: S_{j+1} waits only for the softmax to have loaded S_j, and turns cost 3% (C5).
+      auto issue_s = [&](bool issue, uint32_t k_addr) {
         if (issue) {
           tc_fence_after();
           issue_qk<C>(d_s, a_q, k_addr, C::IDESC_QK | p.qk_negate);
           tc_commit(smem_addr(&bar_s_full[myq]));
         }
-        if constexpr (!C::PSMEM) mbar_arrive(smem_addr(&bar_s_turn[myq ^ 1]));
-        return true;
       };
       if constexpr (C::PSMEM) {
         // P in shared memory: S_{j+1} goes into this tile's S buffer as soon as the softmax has
@@ -764,7 +773,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
           if (!wait_kv(base)) { ok = false; break; }
           if (n > 0 && !wait_read()) { ok = false; break; }
-          if (!s_turn(n > 0, sKV + (base % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+          issue_s(n > 0, sKV + (base % C::NS) * C::TILE_BYTES);
           read_pending = read_pending || n > 0;
           release(&bar_kv_empty[base % C::NS], n > 0);
           if (nmax == 1) release(&bar_q_empty, n > 0);
@@ -773,7 +782,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const uint32_t pos_k = base + 2 * (j + 1);
               if (!wait_kv(pos_k)) { ok = false; break; }
               if (j + 1 < n && !wait_read()) { ok = false; break; }
-              if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
+              issue_s(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES);
               read_pending = read_pending || j + 1 < n;
               release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
               if (j + 2 == nmax) release(&bar_q_empty, n > 0);
@@ -798,11 +807,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           ring = base + 2 * nmax;
         }
-      } else if constexpr (C::S3) {
-        // Three S buffers: the S issuer warp issues every S; this warp issues its Q tile's PVs.
+      } else if constexpr (C::SISS) {
+        // The S issuer warp issues every S; this warp issues its Q tile's PVs. Three S buffers:
         // PV_j reads P_j from S buffer k % 3 (k: S number of S_j); its completion frees that
         // buffer (s_free) and is signalled on o_done for rescales. Barriers of this tile's g-th S
-        // product: index 3 myq + g % 3, phase g / 3.
+        // product: index 3 myq + g % 3, phase g / 3. Shared S buffer: PV_j reads P_j from this
+        // tile's P area; its completion (o_done, index myq, phase g) lets the softmax write the
+        // next P there.
         uint32_t sbase = 0;   // S products of both Q tiles before the current work tile
         uint32_t g = 0;       // S products of this Q tile before the current work tile
         for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
@@ -820,17 +831,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             if (!wait_kv(pos_v)) { ok = false; break; }
             if (j < n) {
               const uint32_t gj = gb + j;
-              const uint32_t par = (gj / 3u) & 1u;
-              const uint32_t bi = 3u * myq + gj % 3u;
-              const uint32_t b = s_number(sb, myq, j, n0, n1) % 3u;
+              const uint32_t par = C::S3 ? (gj / 3u) & 1u : gj & 1u;
+              const uint32_t bi = C::S3 ? 3u * myq + gj % 3u : (uint32_t)myq;
+              const uint32_t b = C::S3 ? s_number(sb, myq, j, n0, n1) % 3u : 0u;
+              const uint32_t a_p = C::S3 ? tmem + b * 128u : tmem + C::P_COL + 64u * myq;
               const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
               if (!mbar_wait(smem_addr(&bar_p_half[bi][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
               tc_fence_after();
-              issue_pv_half<C, 0>(d_o, tmem + b * 128u, b_v, j > 0);
+              issue_pv_half<C, 0>(d_o, a_p, b_v, j > 0);
               if (!mbar_wait(smem_addr(&bar_p_half[bi][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
               tc_fence_after();
-              issue_pv_half<C, 1>(d_o, tmem + b * 128u, b_v, true);
-              tc_commit(smem_addr(&bar_s_free[b]));
+              issue_pv_half<C, 1>(d_o, a_p, b_v, true);
+              if constexpr (C::S3) tc_commit(smem_addr(&bar_s_free[b]));
               tc_commit(smem_addr(&bar_o_done[bi]));
               if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
             }
@@ -838,71 +850,19 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
           ring = base + 2 * nmax;
         }
-      } else {
-      for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
-        const TileCoord tc = decode_tile<C>(t, p);
-        const int n = kv_tiles_for<C>(tc, myq, p);
-        int nmax = 0;
-        for (int qt = 0; qt < C::NQ; ++qt) {
-          const int nq = kv_tiles_for<C>(tc, qt, p);
-          nmax = nq > nmax ? nq : nmax;
-        }
-        if (C::VARLEN && nmax == 0) continue;
-        if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
-        ++nq_loads;
-        const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
-        if (!wait_kv(base)) { ok = false; break; }
-        if (!s_turn(n > 0, sKV + (base % C::NS) * C::TILE_BYTES)) { ok = false; break; }
-        release(&bar_kv_empty[base % C::NS], n > 0);
-        if (nmax == 1) release(&bar_q_empty, n > 0);
-        for (int j = 0; ok && j < nmax; ++j) {
-          const uint32_t pos_v = base + 2 * j + 1;
-          if (!wait_kv(pos_v)) { ok = false; break; }
-          ATTN_TRACE(15, myq, j);
-          if (j < n) {
-            const uint32_t par = p_cnt & 1;
-            const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
-            if (!mbar_wait(smem_addr(&bar_p_half[myq][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
-            ATTN_TRACE(1, myq, j);
-            tc_fence_after();
-            issue_pv_half<C, 0>(d_o, d_s, b_v, j > 0);
-            if (!mbar_wait(smem_addr(&bar_p_half[myq][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
-            ATTN_TRACE(3, myq, j);
-            tc_fence_after();
-            issue_pv_half<C, 1>(d_o, d_s, b_v, true);
-            ATTN_TRACE(13, myq, j);
-            ++p_cnt;
-            if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
-          }
-          if (j + 1 < nmax) {
-            const uint32_t pos_k = pos_v + 1;
-            if (!wait_kv(pos_k)) { ok = false; break; }
-            ATTN_TRACE(18, myq, j + 1);
-            if (!s_turn(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES)) { ok = false; break; }
-            ATTN_TRACE(14, myq, j + 1);
-          }
-          // Stage releases after S_{j+1}'s issue, off the path from P_j to S_{j+1}: V_j's stage is
-          // then freed when S_{j+1} completes instead of PV_j, which the ring's depth absorbs.
-          release(&bar_kv_empty[pos_v % C::NS], j < n);
-          if (j + 1 < nmax) {
-            release(&bar_kv_empty[(pos_v + 1) % C::NS], j + 1 < n);
-            if (j + 2 == nmax) release(&bar_q_empty, n > 0);
-          }
-        }
-        ring = base + 2 * nmax;
-      }
       }
       // Every MMA this warp issued must finish before TMEM is released.
       tc_commit(smem_addr(&bar_drain[myq]));
       const uint64_t t0 = global_timer_ns();
       while (!mbar_try_wait(smem_addr(&bar_drain[myq]), 0) && global_timer_ns() - t0 < p.timeout_ns) {}
     }
-  } else if (C::S3 && warp == C::WARP_S) {
-    // ------------------------------------------------------------------ S issuer, three S buffers
+  } else if (C::SISS && warp == C::WARP_S) {
+    // ------------------------------------------------------------------ S issuer
     if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       // S products in the order S0_0, S1_0, S0_1, S1_1, ... (skipping those a Q tile does not
-      // need), the k-th into buffer k % 3 once the PV of the (k-3)-th has read that buffer.
+      // need), the k-th into buffer k % NSB once that buffer is free of the (k - NSB)-th: three
+      // buffers, its PV has read P from it; one shared buffer, its softmax has loaded it.
       uint32_t ring = 0, nq_loads = 0, sbase = 0, g0 = 0, g1 = 0;
       bool ok = true;
       for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
@@ -923,8 +883,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           for (int qt = 0; ok && qt < 2; ++qt) {
             if (j >= (qt ? n1 : n0)) continue;
             const uint32_t k = s_number(sb, qt, j, n0, n1);
-            const uint32_t b = k % 3u;
-            if (k >= 3u && !mbar_wait(smem_addr(&bar_s_free[b]), ((k / 3u) - 1u) & 1u, ctl, SITE_S_FREE)) {
+            const uint32_t b = k % (uint32_t)C::NSB;
+            if (k >= (uint32_t)C::NSB &&
+                !mbar_wait(smem_addr(&bar_s_free[b]), ((k / C::NSB) - 1u) & 1u, ctl, SITE_S_FREE)) {
               ok = false;
               break;
             }
@@ -932,7 +893,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             issue_qk<C>(tmem + b * 128u, sQ + qt * C::TILE_BYTES, sKV + (pos_k % C::NS) * C::TILE_BYTES,
                         C::IDESC_QK | p.qk_negate);
             const uint32_t gj = (qt ? gb1 : gb0) + j;
-            tc_commit(smem_addr(&bar_s_full[3u * qt + gj % 3u]));
+            tc_commit(smem_addr(&bar_s_full[C::S3 ? 3u * qt + gj % 3u : (uint32_t)qt]));
           }
           if (!ok) break;
           // K_j's stage and, after the last S, Q: both arrivals of each come from this warp.
@@ -1039,14 +1000,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     uint32_t s_cnt0 = 0u, s_cnt1 = 0u;
     uint32_t pv_cnt = 0;            // PV products of this Q tile committed so far
     uint32_t tiles_done = 0;        // work tiles of this Q tile finished (o_full phases)
-    uint32_t sbase = 0, g = 0;      // three buffers: S products of the CTA / of this Q tile so far
+    uint32_t sbase = 0, g = 0;      // S issuer modes: S products of the CTA / of this Q tile so far
     bool ok = true;
     for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
       const TileCoord tc = decode_tile<C>(t, p);
       const int n = kv_tiles_for<C>(tc, qt, p);
       int n0 = 0, n1 = 0;
       uint32_t sb = 0, gb = 0;
-      if constexpr (C::S3) {
+      if constexpr (C::SISS) {
         n0 = kv_tiles_for<C>(tc, 0, p);
         n1 = kv_tiles_for<C>(tc, 1, p);
         sb = sbase;
@@ -1090,8 +1051,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
       float l = 0.0f;        // running sum of exp2(s * x - m)
       for (int j = 0; j < n; ++j) {
         // buf: index of this S's barriers; s_col: its TMEM buffer (three buffers: S number % 3)
+        // buf: index of this S's barriers; s_col: its TMEM buffer (three buffers: S number % 3;
+        // shared S buffer: column 0).
         const int buf = C::S3 ? 3 * qt + (int)((gb + j) % 3u) : (C::NQ == 2 ? qt : (j & 1));
-        const uint32_t s_col = C::S3 ? (s_number(sb, qt, j, n0, n1) % 3u) * 128u : (buf ? C::S_COL1 : C::S_COL0);
+        const uint32_t s_col = C::S3 ? (s_number(sb, qt, j, n0, n1) % 3u) * 128u
+                                     : C::S1 ? 0u : (buf ? C::S_COL1 : C::S_COL0);
         // Scales of the two 64-key halves of this tile (they differ only with K block descales;
         // read before the wait so the load latency hides behind it).
         float s_lo = s, s_hi = s;
@@ -1101,10 +1065,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           s_hi = s_q * __ldg(dk_row + min(kb + 1, n_kblk - 1) * p.dk_sn);
         }
         const uint32_t s_cnt = (C::NQ == 2 || buf == 0) ? s_cnt0 : s_cnt1;
-        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), C::S3 ? ((gb + j) / 3u) & 1u : s_cnt & 1, ctl, SITE_S_FULL);
+        const uint32_t s_par = C::S3 ? ((gb + j) / 3u) & 1u : C::S1 ? (gb + j) & 1u : s_cnt & 1u;
+        bool w = mbar_wait(smem_addr(&bar_s_full[buf]), s_par, ctl, SITE_S_FULL);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         if (r == 0) ATTN_TRACE(4, qt, j);
-        if constexpr (!C::S3) {
+        if constexpr (!C::SISS) {
           if (C::NQ == 2 || buf == 0) ++s_cnt0;
           else ++s_cnt1;
         }
@@ -1132,11 +1097,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         reg_fence32(sr + 64);
         reg_fence32(sr + 96);
         asm volatile("" : "+f"(mq0), "+f"(mq1), "+f"(mq2), "+f"(mq3));
-        if constexpr (C::PSMEM) {
-          // S is in registers: the issuer may put S_{j+1} into this buffer now.
+        if constexpr (C::PSMEM || C::S1) {
+          // S is in registers: the issuer may put the next S into this buffer now.
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&bar_s_read[qt]));
+          if (lane == 0) mbar_arrive(smem_addr(C::PSMEM ? &bar_s_read[qt] : &bar_s_free[0]));
         }
         if (r == 0) ATTN_TRACE(5, qt, j);
         float x[128];
@@ -1217,6 +1182,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             fence_proxy_async_smem();
           } else {
             if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
+            else if (C::S1) tmem_st_32cols(tmem + lane_base + C::P_COL + 64u * qt + h * 32, pk);
             else tmem_st_32cols(tS + h * 32, pk);
             tmem_st_wait();
             tc_fence_before();
@@ -1271,9 +1237,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
         }
         if (r == 0) ATTN_TRACE(6, qt, j);
-        if constexpr (C::PSMEM) {
-          // S_j was issued before PV_{j-1}: wait for that PV before P_j overwrites P_{j-1} in
-          // shared memory (and before any rescale of O).
+        if constexpr (C::PSMEM || C::S1) {
+          // S_j may have been issued before PV_{j-1}: wait for that PV before P_j overwrites
+          // P_{j-1} (in shared memory, or in this tile's TMEM P area) and before any rescale of O.
           if (j > 0) {
             w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -1290,8 +1256,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (j > 0) {
             // Rescale O before any half of P_j is released: PV_j must accumulate onto the
             // rescaled O, and O must not be touched while PV_{j-1} is still accumulating into
-            // it. Two Q tiles: S_j's commit already covered PV_{j-1} (same issuing thread), so O
-            // is settled. One Q tile: S_j was issued before PV_{j-1}; wait for that PV. Three S
+            // it. Two Q tiles, P aliasing S: S_j's commit already covered PV_{j-1} (same issuing
+            // thread), so O is settled. P in shared memory or in a P area: PV_{j-1} was waited
+            // for above. One Q tile: S_j was issued before PV_{j-1}; wait for that PV. Three S
             // buffers: S_j comes from another warp, so wait for PV_{j-1} as well.
             if constexpr (C::S3) {
               const uint32_t gp = gb + j - 1;   // this tile's PV_{j-1}

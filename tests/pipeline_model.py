@@ -1,6 +1,8 @@
-"""Executable models of two synchronisation protocols of the forward kernel with two Q tiles per
-CTA: d = 64 (three rotating S buffers in tensor memory, a dedicated S-issuer warp; `run`) and
-e4m3 at d = 128 (P in shared memory, S_{j+1} issued once S_j is loaded; `run_psmem`).
+"""Executable models of the synchronisation protocols of the forward kernel with two Q tiles per
+CTA: bf16 with a dedicated S-issuer warp (`run`), either at d = 64 (three rotating S buffers in
+tensor memory that P aliases, mode "s3") or at d = 128 (one S buffer both tiles share, P in a
+tensor-memory area per tile, mode "s1"); and e4m3 at d = 128 (P in shared memory, S_{j+1} issued
+once S_j is loaded; `run_psmem`).
 
 This is test infrastructure: a model of the kernel's warp roles and mbarriers, not the kernel. It
 runs the roles as Python generators under random interleavings and checks three things:
@@ -19,18 +21,31 @@ Roles, as in the kernel:
              does not need. S number k goes to buffer k % 3 once the PV of number k - 3 has
              completed (s_free). It releases each K stage and, after the last S, Q;
   PV issuer  one per Q tile: waits for the two P halves of its tile's S_j, issues PV_j, and commits
-             s_free (the buffer), o_done (for rescales), and o_full after the tile's last PV;
+             s_free (the buffer), o_done (for rescales), and o_full after the tile's last PV. At
+             a step where its tile has no S (past a ragged end, or the shorter causal tile's last
+             step) it still waits for the V stage before releasing it;
   softmax    one per Q tile: waits for S_j, maybe rescales O (after waiting for PV_{j-1}), writes
              P_j over S_j, and at the end of the work tile waits for o_full.
+
+Mode "s1" (d = 128): S number k always goes to the one shared buffer, once the softmax that owns S
+number k - 1 has loaded it (s_free, arrived by the softmax, not by a PV). The softmax writes P_j
+to its tile's own P area after waiting for PV_{j-1}, which read the P before it.
+
+Both modes need an even number of K/V stages (`ns`): then each stage holds only K tiles (waited
+for by the S issuer) or only V tiles (waited for by the PV issuers), and every waiter has waited
+for the stage's previous load itself. With an odd count a PV issuer whose tile has no keys in a
+work tile, paced by nothing, can reach a V stage whose previous load (a K tile it never waits for)
+has not landed, and its parity wait then passes two phases early.
   tensor pipe executes MMAs and commits in issue order: one shared in-order queue, or (a weaker
-             model) one queue per issuing warp.
+             model) one queue per issuing warp;
+  TMA        lands the producer's K/V copies in any order.
 
 Each Q tile has M S-ready, P-ready and PV-done barriers, its g-th S product using index g % M and
 phase g // M. The kernel uses M = 3. `run_psmem` documents its own roles.
 """
 import random
 
-NS = 8   # K/V ring stages of the d = 64 instance
+NS = 8   # K/V ring stages of the d = 64 instance (the d = 128 instance has 5)
 
 
 class ProtocolError(Exception):
@@ -67,9 +82,14 @@ def s_number(sbase, qt, j, n0, n1):
     return sbase + min(j, n0) + min(j, n1) + (1 if (qt == 1 and j < n0) else 0)
 
 
-def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, skip_rescale_wait=False):
+def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, skip_rescale_wait=False,
+        mode="s3", ns=NS):
     """Runs the work tiles [(n0, n1), ...] of one CTA to completion under a random schedule."""
     rnd = random.Random(seed)
+    s1 = mode == "s1"
+    if s1:
+        M = 1
+    NS = ns
     q_full, q_empty = Bar("q_full", 1), Bar("q_empty", 2)
     kv_full = [Bar(f"kv_full{i}", 1) for i in range(NS)]
     kv_empty = [Bar(f"kv_empty{i}", 2) for i in range(NS)]
@@ -77,6 +97,10 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
     p_half = [[Bar(f"p_half{i}.{h}", 1) for h in range(2)] for i in range(2 * M)]
     o_done = [Bar(f"o_done{i}", 1) for i in range(2 * M)]
     s_free = [Bar(f"s_free{i}", 1) for i in range(3)]
+    nsb = 1 if s1 else 3          # S buffers
+    inflight = []                 # K/V copies issued but not landed: TMA completes them in any order
+    s_loaded = set()              # s1: S numbers the softmax has loaded
+    p_area = [None, None]         # s1: the P each tile's tensor-memory P area holds
     o_full = [Bar(f"o_full{i}", 1) for i in range(2)]
     tmem = [None, None, None]                 # ("S", k) or ("P", k)
     pv_done = set()                           # S numbers whose PV has completed
@@ -106,7 +130,7 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
                 if ring >= NS:
                     yield from wait(kv_empty[slot], (ring // NS - 1) & 1, ring // NS - 1)
                 yield
-                kv_full[slot].arrive()
+                inflight.append(slot)
                 ring += 1
 
     def s_issuer():
@@ -128,9 +152,9 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
                 for qt in range(2):
                     if j < (n1 if qt else n0):
                         k = s_number(sb, qt, j, n0, n1)
-                        if k >= 3 and not skip_s_free:
-                            yield from wait(s_free[k % 3], (k // 3 - 1) & 1, k // 3 - 1)
-                        enqueue(2, ("S", k, k % 3))
+                        if k >= nsb and not skip_s_free:
+                            yield from wait(s_free[k % nsb], (k // nsb - 1) & 1, k // nsb - 1)
+                        enqueue(2, ("S", k, k % nsb))
                         commit(2, s_full[M * qt + (gb[qt] + j) % M])
                 commit(2, kv_empty[pos_k % NS])
                 commit(2, kv_empty[pos_k % NS])
@@ -159,7 +183,8 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
                     for h in range(2):
                         yield from wait(p_half[M * myq + gj % M][h], (gj // M) & 1, gj // M)
                     enqueue(myq, ("PV", k, k % 3, myq, ti, j))
-                    commit(myq, s_free[k % 3])
+                    if not s1:
+                        commit(myq, s_free[k % 3])
                     commit(myq, o_done[M * myq + gj % M])
                     if j + 1 == n:
                         commit(myq, o_full[myq])
@@ -182,18 +207,32 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
                 gj = gb + j
                 k = s_number(sb, qt, j, n0, n1)
                 yield from wait(s_full[M * qt + gj % M], (gj // M) & 1, gj // M)
-                if tmem[k % 3] != ("S", k):
-                    raise ProtocolError(f"softmax {qt} expected S{k} in buffer {k % 3}, found {tmem[k % 3]}")
+                if tmem[k % nsb] != ("S", k):
+                    raise ProtocolError(f"softmax {qt} expected S{k} in buffer {k % nsb}, found {tmem[k % nsb]}")
                 yield
-                if j > 0 and rnd.random() < rescale_p:
-                    if not skip_rescale_wait:
-                        gp = gj - 1
-                        yield from wait(o_done[M * qt + gp % M], (gp // M) & 1, gp // M)
-                    if (ti, j - 1) not in pv_complete[qt]:
-                        raise ProtocolError("O rescaled while PV_{j-1} may still accumulate into it")
-                if tmem[k % 3] != ("S", k):
-                    raise ProtocolError(f"S{k} overwritten before its P was written")
-                tmem[k % 3] = ("P", k)
+                if s1:
+                    # S is in registers: the shared buffer may take the next S. P_j then waits for
+                    # PV_{j-1}, which read this tile's P area (and that wait also covers rescales).
+                    s_loaded.add(k)
+                    s_free[0].arrive()
+                    yield
+                    if j > 0:
+                        if not skip_rescale_wait:
+                            gp = gj - 1
+                            yield from wait(o_done[qt], gp & 1, gp)
+                        if (ti, j - 1) not in pv_complete[qt]:
+                            raise ProtocolError(f"P{k} written before the PV before it read P or O settled")
+                    p_area[qt] = ("P", k)
+                else:
+                    if j > 0 and rnd.random() < rescale_p:
+                        if not skip_rescale_wait:
+                            gp = gj - 1
+                            yield from wait(o_done[M * qt + gp % M], (gp // M) & 1, gp // M)
+                        if (ti, j - 1) not in pv_complete[qt]:
+                            raise ProtocolError("O rescaled while PV_{j-1} may still accumulate into it")
+                    if tmem[k % 3] != ("S", k):
+                        raise ProtocolError(f"S{k} overwritten before its P was written")
+                    tmem[k % 3] = ("P", k)
                 p_half[M * qt + gj % M][0].arrive()
                 yield
                 p_half[M * qt + gj % M][1].arrive()
@@ -206,13 +245,17 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
         if op[0] == "S":
             _, k, b = op
             prev = tmem[b]
-            if prev is not None and (prev != ("P", k - 3) or (k - 3) not in pv_done):
+            if s1:
+                if prev is not None and (prev != ("S", k - 1) or (k - 1) not in s_loaded):
+                    raise ProtocolError(f"S{k} overwrites buffer {b} holding {prev} before the softmax loaded it")
+            elif prev is not None and (prev != ("P", k - 3) or (k - 3) not in pv_done):
                 raise ProtocolError(f"S{k} overwrites buffer {b} holding {prev}")
             tmem[b] = ("S", k)
         elif op[0] == "PV":
             _, k, b, qt, ti, j = op
-            if tmem[b] != ("P", k):
-                raise ProtocolError(f"PV{k} reads buffer {b} holding {tmem[b]}")
+            held = p_area[qt] if s1 else tmem[b]
+            if held != ("P", k):
+                raise ProtocolError(f"PV{k} reads P holding {held}")
             pv_done.add(k)
             pv_complete[qt].add((ti, j))
         else:
@@ -224,9 +267,16 @@ def run(tiles, seed, shared_pipe=True, rescale_p=0.3, M=3, skip_s_free=False, sk
                 execute(q.pop(0)[1])
             yield
 
+    def tma():
+        while True:
+            if inflight:
+                kv_full[inflight.pop(rnd.randrange(len(inflight)))].arrive()
+            yield
+
     procs = {"producer": producer(), "s_issuer": s_issuer(), "pv0": pv_issuer(0), "pv1": pv_issuer(1),
              "softmax0": softmax(0), "softmax1": softmax(1)}
     finite = set(procs)
+    procs["tma"] = tma()
     if shared_pipe:
         procs["pipe"] = pipe(shared)
     else:
@@ -261,6 +311,16 @@ def random_tiles(rnd, kind):
     return out
 
 
+def random_tiles_causal_ragged(rnd):
+    """Causal ragged batches as the varlen plan yields them: one more KV tile for the second Q
+    tile, or none at all where the second tile lies past the sequence's end."""
+    out = []
+    for _ in range(rnd.randint(1, 10)):
+        n0 = rnd.randint(1, 8)
+        out.append((n0, 0 if rnd.random() < 0.5 else n0 + 1))
+    return out
+
+
 SCHEDULES = ((True, 0.3), (False, 0.3), (True, 1.0), (False, 1.0))
 
 
@@ -268,8 +328,8 @@ def sweep(n_cases, case_seed, **kw):
     """Runs n_cases random tile lists under every schedule; returns the first failure or None."""
     rnd = random.Random(case_seed)
     for i in range(n_cases):
-        kind = ("noncausal", "causal", "ragged")[i % 3]
-        tiles = random_tiles(rnd, kind)
+        kind = ("noncausal", "causal", "ragged", "causal-ragged")[i % 4]
+        tiles = random_tiles_causal_ragged(rnd) if kind == "causal-ragged" else random_tiles(rnd, kind)
         for shared, rp in SCHEDULES:
             try:
                 run(tiles, seed=i * 7 + shared + int(rp * 10), shared_pipe=shared, rescale_p=rp, **kw)
