@@ -16,10 +16,10 @@
 //     (mojostudio.in), section 2, the producer's multi-stage TMA pipeline with expected
 //     transaction bytes);
 //   * warp MMA (one thread) issues tcgen05.mma: S = Q K_j^T into tensor memory (TMEM), and
-//     O += P V_j with P read from TMEM and V from shared memory. With two bf16 Q tiles a warp of
-//     its own issues the S products: at d = 64 into three rotating TMEM buffers that P aliases
-//     (AttnCfg::S3), at d = 128 into one buffer both tiles share, P having a TMEM area of its own
-//     (AttnCfg::S1); e4m3 keeps P in shared memory;
+//     O += P V_j with P read from TMEM and V from shared memory. With two Q tiles a warp of its
+//     own issues the S products: at d = 64 into three rotating TMEM buffers that P aliases
+//     (AttnCfg::S3), at d = 128 (bf16 and e4m3) into one buffer both tiles share, P having a TMEM
+//     area of its own (AttnCfg::S1);
 //   * one softmax warpgroup per Q tile (one thread per query row) reads S from TMEM, masks,
 //     takes the row max, evaluates exp2 with the scale folded in, accumulates the row sum,
 //     writes P back to TMEM and rescales O in TMEM when the running max moves;
@@ -118,18 +118,11 @@ struct AttnCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes (one TMA box)
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one Q, K or V tile
   static constexpr int Q_BYTES = NQ * TILE_BYTES;
-  // e4m3 with two Q tiles: P goes to shared memory (one 16 KB tile per Q tile, laid out like a Q
-  // tile) and the PV product reads it from there. The S buffer in TMEM is then free as soon as the
-  // softmax has loaded S_j, so S_{j+1} can be issued into it while the softmax still works on
-  // step j. (bf16 at d = 128 has no shared memory to spare for P, nor shared-memory bandwidth:
-  // its PV would read twice as many bytes per cycle as the e4m3 one.)
-  static constexpr bool PSMEM = FP8_ && (D_ <= 128 && !SPLIT_);
   // Non-causal bf16 prefill at d <= 128 may take the share deal of its last tiles (tail_mode 3).
   static constexpr bool SHARES = !CAUSAL_ && !SPLIT_ && !VARLEN_ && !FP8_ && D_ <= 128;
-  static constexpr int P_BYTES = PSMEM ? Q_BYTES : 0;
   static constexpr int SMEM_LIMIT = 232448;               // 227 KB per CTA
   static constexpr int RESERVE = 1024 + 1024;             // alignment slack + static shared
-  static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES - P_BYTES) / TILE_BYTES;
+  static constexpr int NS_FIT = (SMEM_LIMIT - RESERVE - Q_BYTES) / TILE_BYTES;
   // K/V ring stages. With a dedicated S-issuer warp (two bf16 Q tiles) the count is even, so each
   // stage holds only K tiles or only V tiles: K stages are waited for by the S issuer alone and V
   // stages by the PV issuers alone, each of which has waited for the stage's previous load itself.
@@ -137,8 +130,8 @@ struct AttnCfg {
   // no keys in a work tile (a ragged sequence's end) would wait for a V stage whose previous load,
   // a K tile it never waits for, has not landed, and pass it two phases early.
   static constexpr int NS_CAP = NS_FIT > 8 ? 8 : NS_FIT;
-  static constexpr int NS = (NQ == 2 && !FP8 && (NS_CAP & 1)) ? NS_CAP - 1 : NS_CAP;
-  static constexpr int SMEM_BYTES = Q_BYTES + P_BYTES + NS * TILE_BYTES + 1024;
+  static constexpr int NS = (NQ == 2 && (NS_CAP & 1)) ? NS_CAP - 1 : NS_CAP;
+  static constexpr int SMEM_BYTES = Q_BYTES + NS * TILE_BYTES + 1024;
   static constexpr int KSTEPS_QK = D * ELT / 32;          // one MMA k-step covers 32 bytes of K
   static constexpr int KSTEPS_PV = BN * ELT / 32;
   static constexpr int PV_ROWS = 32 / ELT;                // V rows consumed per PV k-step
@@ -149,12 +142,13 @@ struct AttnCfg {
   // by a warp of their own (the otherwise idle twelfth warp), so a tile's S_{j+1} is issued as
   // soon as a buffer is free, not behind its PV_j, and is ready when its softmax finishes step j.
   static constexpr bool S3 = (NQ == 2 && D == 64);
-  // Two bf16 Q tiles at d = 128 fill TMEM with two O tiles, so P cannot alias a per-tile S
-  // buffer without chaining S_{j+1} to PV_j. Instead both tiles share one 128-column S buffer
-  // and each writes its P (64 columns of bf16 pairs) to an area of its own: the S issuer puts the
-  // next S into the buffer as soon as the softmax that owns the current one has loaded it into
-  // registers, whatever the PVs are doing. TMEM: S at 0, P of tile q at P_COL + 64 q, O at 256.
-  static constexpr bool S1 = (NQ == 2 && D == 128 && !FP8);
+  // Two Q tiles at d = 128 fill TMEM with two O tiles, so P cannot alias a per-tile S buffer
+  // without chaining S_{j+1} to PV_j. Instead both tiles share one 128-column S buffer and each
+  // writes its P (P_COLS columns: 64 for bf16 pairs, 32 for e4m3 quadruples) to an area of its
+  // own: the S issuer puts the next S into the buffer as soon as the softmax that owns the current
+  // one has loaded it into registers, whatever the PVs are doing. TMEM: S at 0, P of tile q at
+  // P_COL + P_COLS q, O at 256.
+  static constexpr bool S1 = (NQ == 2 && D == 128);
   static constexpr bool SISS = S3 || S1;                  // a warp of its own issues every S
   static constexpr int NSB = S3 ? 3 : 1;                  // S buffers the S issuer rotates through
   static constexpr int P_COL = 128;
@@ -457,24 +451,6 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint3
   }
 }
 
-// Half H of O += P V with P in shared memory, laid out like a Q tile (K-major, 128-byte swizzle:
-// each row's keys in 128-byte chunks of CHUNK_BYTES-strided 128-row blocks, 32 bytes per k-step;
-// one chunk per row for e4m3, two for bf16), and V MN-major as below.
-template <class C, int H>
-__device__ __forceinline__ void issue_pv_half_ss(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr,
-                                                 bool accumulate_first) {
-  constexpr int KH = C::KSTEPS_PV / 2;
-  const uint64_t a0 = make_sdesc_sw128(a_addr, 16, 1024);
-  const uint64_t b0 = make_sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
-#pragma unroll
-  for (int i = 0; i < KH; ++i) {
-    const int kk = H * KH + i;
-    const uint32_t acc = (H > 0 || i > 0) ? 1u : (accumulate_first ? 1u : 0u);
-    mma_f16_or_f8<C::FP8>(d_tmem, a0 + (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4),
-                          b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4), C::IDESC_PV, acc);
-  }
-}
-
 // Half H of O += P V: the k-steps covering keys [64 H, 64 H + 64) of the tile. P comes from
 // TMEM (8 columns per k-step), V from shared memory (MN-major, PV_ROWS rows per k-step).
 template <class C, int H>
@@ -513,8 +489,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   // from b has completed (one commit). Shared S buffer: the softmax warps that own the S in it
   // have loaded it (one arrival per warp).
   __shared__ __align__(8) uint64_t bar_s_free[C::SISS ? C::NSB : 1];
-  // s_read[q] (P in shared memory): the softmax warps of Q tile q have loaded S from TMEM.
-  __shared__ __align__(8) uint64_t bar_s_read[C::NQ];
   __shared__ uint32_t tmem_slot;
   __shared__ volatile uint32_t abort_flag;
 
@@ -528,8 +502,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
   if (C::SPLIT || (kDense && (p.tail_mode == 1 || p.tail_mode == 3))) griddep_launch_dependents();
   const uint32_t smem_base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   const uint32_t sQ = smem_base;
-  const uint32_t sP = smem_base + C::Q_BYTES;   // P tiles (e4m3, two Q tiles); empty otherwise
-  const uint32_t sKV = sP + C::P_BYTES;
+  const uint32_t sKV = smem_base + C::Q_BYTES;
   const WaitCtl ctl{&abort_flag, p.status, p.timeout_ns};
 
   if (tid == 0) {
@@ -543,14 +516,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
     if constexpr (C::SISS)
       for (int i = 0; i < C::NSB; ++i) mbar_init(smem_addr(&bar_s_free[i]), C::S1 ? 4 : 1);
-    if constexpr (C::PSMEM)
-      for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_s_read[i]), 4);
     for (int i = 0; i < C::N_SBAR; ++i) {
       mbar_init(smem_addr(&bar_s_full[i]), 1);
-      // One arrival per softmax warp (P in TMEM) or per softmax thread (P in shared memory, where
-      // each thread's generic-proxy stores are fenced for the tensor core by that thread).
-      mbar_init(smem_addr(&bar_p_half[i][0]), C::PSMEM ? 128 : 4);
-      mbar_init(smem_addr(&bar_p_half[i][1]), C::PSMEM ? 128 : 4);
+      // One arrival per softmax warp.
+      mbar_init(smem_addr(&bar_p_half[i][0]), 4);
+      mbar_init(smem_addr(&bar_p_half[i][1]), 4);
     }
     for (int i = 0; i < C::N_OBAR; ++i) mbar_init(smem_addr(&bar_o_done[i]), 1);
     for (int i = 0; i < C::NQ; ++i) mbar_init(smem_addr(&bar_o_full[i]), 1);
@@ -722,7 +692,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     if constexpr (C::REG_SPLIT) setmaxnreg_dec<C::REGS_OTHER>();
     if (lane == 0) {
       const int myq = warp - C::WARP_MMA;   // Q tile (and S/P buffer) this warp issues for
-      uint32_t ring = 0, nq_loads = 0, p_cnt = 0;
+      uint32_t ring = 0;
       bool ok = true;
 
       auto wait_kv = [&](uint32_t pos) -> bool {
@@ -733,81 +703,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (used) tc_commit(smem_addr(bar));
         else mbar_arrive(smem_addr(bar));
       };
-      const uint32_t d_s = tmem + (myq ? C::S_COL1 : C::S_COL0);
       const uint32_t d_o = tmem + C::O_COL + myq * C::D;
-      const uint32_t a_q = sQ + myq * C::TILE_BYTES;
-      // S of this Q tile into its own S buffer (P in shared memory). The two issuers do not take
-      // turns: S_{j+1} waits only for the softmax to have loaded S_j, and turns cost 3% (C5).
-      auto issue_s = [&](bool issue, uint32_t k_addr) {
-        if (issue) {
-          tc_fence_after();
-          issue_qk<C>(d_s, a_q, k_addr, C::IDESC_QK | p.qk_negate);
-          tc_commit(smem_addr(&bar_s_full[myq]));
-        }
-      };
-      if constexpr (C::PSMEM) {
-        // P in shared memory: S_{j+1} goes into this tile's S buffer as soon as the softmax has
-        // loaded S_j (s_read), in this issuer's turn, before PV_j. PV_j reads P_j from shared
-        // memory; its completion (o_done) lets the softmax overwrite P and rescale O.
-        uint32_t sr_cnt = 0;         // S loads of this Q tile's softmax waited for
-        bool read_pending = false;   // an S was issued whose load has not been waited for
-        // Before an S goes into this tile's buffer, the softmax must have loaded the one before.
-        auto wait_read = [&]() -> bool {
-          if (!read_pending) return true;
-          if (!mbar_wait(smem_addr(&bar_s_read[myq]), sr_cnt & 1, ctl, SITE_S_FULL)) return false;
-          ++sr_cnt;
-          read_pending = false;
-          return true;
-        };
-        for (int turn = 0, t = next_tile<C>(0, p); ok && t < n_tiles; t = next_tile<C>(++turn, p)) {
-          const TileCoord tc = decode_tile<C>(t, p);
-          const int n = kv_tiles_for<C>(tc, myq, p);
-          int nmax = 0;
-          for (int qt = 0; qt < C::NQ; ++qt) {
-            const int nq = kv_tiles_for<C>(tc, qt, p);
-            nmax = nq > nmax ? nq : nmax;
-          }
-          if (C::VARLEN && nmax == 0) continue;
-          if (!mbar_wait(smem_addr(&bar_q_full), nq_loads & 1, ctl, SITE_Q_FULL)) { ok = false; break; }
-          ++nq_loads;
-          const uint32_t base = ring;  // K_j at base + 2j, V_j at base + 2j + 1
-          if (!wait_kv(base)) { ok = false; break; }
-          if (n > 0 && !wait_read()) { ok = false; break; }
-          issue_s(n > 0, sKV + (base % C::NS) * C::TILE_BYTES);
-          read_pending = read_pending || n > 0;
-          release(&bar_kv_empty[base % C::NS], n > 0);
-          if (nmax == 1) release(&bar_q_empty, n > 0);
-          for (int j = 0; ok && j < nmax; ++j) {
-            if (j + 1 < nmax) {
-              const uint32_t pos_k = base + 2 * (j + 1);
-              if (!wait_kv(pos_k)) { ok = false; break; }
-              if (j + 1 < n && !wait_read()) { ok = false; break; }
-              issue_s(j + 1 < n, sKV + (pos_k % C::NS) * C::TILE_BYTES);
-              read_pending = read_pending || j + 1 < n;
-              release(&bar_kv_empty[pos_k % C::NS], j + 1 < n);
-              if (j + 2 == nmax) release(&bar_q_empty, n > 0);
-            }
-            const uint32_t pos_v = base + 2 * j + 1;
-            if (!wait_kv(pos_v)) { ok = false; break; }
-            if (j < n) {
-              const uint32_t par = p_cnt & 1;
-              const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
-              const uint32_t a_p = sP + myq * C::TILE_BYTES;
-              if (!mbar_wait(smem_addr(&bar_p_half[myq][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
-              tc_fence_after();
-              issue_pv_half_ss<C, 0>(d_o, a_p, b_v, j > 0);
-              if (!mbar_wait(smem_addr(&bar_p_half[myq][1]), par, ctl, SITE_P_FULL)) { ok = false; break; }
-              tc_fence_after();
-              issue_pv_half_ss<C, 1>(d_o, a_p, b_v, true);
-              ++p_cnt;
-              tc_commit(smem_addr(&bar_o_done[myq]));
-              if (j + 1 == n) tc_commit(smem_addr(&bar_o_full[myq]));
-            }
-            release(&bar_kv_empty[pos_v % C::NS], j < n);
-          }
-          ring = base + 2 * nmax;
-        }
-      } else if constexpr (C::SISS) {
+      {
         // The S issuer warp issues every S; this warp issues its Q tile's PVs. Three S buffers:
         // PV_j reads P_j from S buffer k % 3 (k: S number of S_j); its completion frees that
         // buffer (s_free) and is signalled on o_done for rescales. Barriers of this tile's g-th S
@@ -834,7 +731,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const uint32_t par = C::S3 ? (gj / 3u) & 1u : gj & 1u;
               const uint32_t bi = C::S3 ? 3u * myq + gj % 3u : (uint32_t)myq;
               const uint32_t b = C::S3 ? s_number(sb, myq, j, n0, n1) % 3u : 0u;
-              const uint32_t a_p = C::S3 ? tmem + b * 128u : tmem + C::P_COL + 64u * myq;
+              const uint32_t a_p = C::S3 ? tmem + b * 128u : tmem + C::P_COL + (uint32_t)C::P_COLS * myq;
               const uint32_t b_v = sKV + (pos_v % C::NS) * C::TILE_BYTES;
               if (!mbar_wait(smem_addr(&bar_p_half[bi][0]), par, ctl, SITE_P_FULL)) { ok = false; break; }
               tc_fence_after();
@@ -1097,11 +994,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         reg_fence32(sr + 64);
         reg_fence32(sr + 96);
         asm volatile("" : "+f"(mq0), "+f"(mq1), "+f"(mq2), "+f"(mq3));
-        if constexpr (C::PSMEM || C::S1) {
-          // S is in registers: the issuer may put the next S into this buffer now.
+        if constexpr (C::S1) {
+          // S is in registers: the S issuer may put the next S into the shared buffer now.
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(C::PSMEM ? &bar_s_read[qt] : &bar_s_free[0]));
+          if (lane == 0) mbar_arrive(smem_addr(&bar_s_free[0]));
         }
         if (r == 0) ATTN_TRACE(5, qt, j);
         float x[128];
@@ -1161,40 +1058,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           }
         };
         auto store_half = [&](int h, const uint32_t* pk) {
-          if constexpr (C::PSMEM) {
-            // Row r of this tile's P in shared memory, the layout a TMA copy of a Q tile leaves: 128
-            // bytes per row and chunk, 16-byte piece c of row r at c ^ (r % 8) (128-byte swizzle).
-            // e4m3: the half's 64 bytes are pieces 4h .. 4h + 3 of the row's one chunk; bf16: the
-            // half's 128 bytes are all eight pieces of chunk h.
-            if constexpr (C::FP8) {
-              const uint32_t row = sP + qt * C::TILE_BYTES + r * 128;
-#pragma unroll
-              for (int i = 0; i < 4; ++i)
-                st_shared_v4(row + ((uint32_t)((h * 4 + i) ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1],
-                             pk[4 * i + 2], pk[4 * i + 3]);
-            } else {
-              const uint32_t row = sP + qt * C::TILE_BYTES + h * C::CHUNK_BYTES + r * 128;
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                st_shared_v4(row + ((uint32_t)(i ^ (r & 7)) << 4), pk[4 * i], pk[4 * i + 1], pk[4 * i + 2],
-                             pk[4 * i + 3]);
-            }
-            fence_proxy_async_smem();
-          } else {
-            if (C::FP8) tmem_st_16cols(tS + h * 16, pk);
-            else if (C::S1) tmem_st_32cols(tmem + lane_base + C::P_COL + 64u * qt + h * 32, pk);
-            else tmem_st_32cols(tS + h * 32, pk);
+          {
+            // P of this tile: its own P area (shared S buffer), else over the start of S.
+            const uint32_t tP = C::S1 ? tmem + lane_base + C::P_COL + (uint32_t)C::P_COLS * qt : tS;
+            if (C::FP8) tmem_st_16cols(tP + h * 16, pk);
+            else tmem_st_32cols(tP + h * 32, pk);
             tmem_st_wait();
             tc_fence_before();
           }
-          if constexpr (C::PSMEM) {
-            mbar_arrive(smem_addr(&bar_p_half[buf][h]));
-          } else {
-            // Every lane's TMEM stores are complete and fenced; once the warp has converged, one
-            // lane arrives for it.
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&bar_p_half[buf][h]));
-          }
+          // Every lane's TMEM stores are complete and fenced; once the warp has converged, one
+          // lane arrives for it.
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&bar_p_half[buf][h]));
           if (r == 0) ATTN_TRACE(7 + h, qt, j);
         };
         uint32_t pk[PKN];
@@ -1237,9 +1112,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
         }
         if (r == 0) ATTN_TRACE(6, qt, j);
-        if constexpr (C::PSMEM || C::S1) {
+        if constexpr (C::S1) {
           // S_j may have been issued before PV_{j-1}: wait for that PV before P_j overwrites
-          // P_{j-1} (in shared memory, or in this tile's TMEM P area) and before any rescale of O.
+          // P_{j-1} in this tile's P area and before any rescale of O.
           if (j > 0) {
             w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
             if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -1256,10 +1131,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           if (j > 0) {
             // Rescale O before any half of P_j is released: PV_j must accumulate onto the
             // rescaled O, and O must not be touched while PV_{j-1} is still accumulating into
-            // it. Two Q tiles, P aliasing S: S_j's commit already covered PV_{j-1} (same issuing
-            // thread), so O is settled. P in shared memory or in a P area: PV_{j-1} was waited
-            // for above. One Q tile: S_j was issued before PV_{j-1}; wait for that PV. Three S
-            // buffers: S_j comes from another warp, so wait for PV_{j-1} as well.
+            // it. Shared S buffer: PV_{j-1} was waited for above. One Q tile: S_j was issued
+            // before PV_{j-1}; wait for that PV. Three S buffers: S_j comes from another warp,
+            // so wait for PV_{j-1} as well.
             if constexpr (C::S3) {
               const uint32_t gp = gb + j - 1;   // this tile's PV_{j-1}
               w = mbar_wait(smem_addr(&bar_o_done[3 * qt + gp % 3u]), (gp / 3u) & 1u, ctl, SITE_O_DONE);

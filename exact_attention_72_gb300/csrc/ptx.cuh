@@ -42,9 +42,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -379,10 +376,6 @@ __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wa
 }  // namespace gb300
 
 namespace gb300 {
-// 16-byte store to shared memory (a 32-bit shared address).
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 // 32-byte store to global memory (the address 32-byte aligned): eight words, w[0] at the lowest
 // address. One lane then fills a whole 32-byte sector.
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* w) {

@@ -1,8 +1,7 @@
-"""Executable models of the synchronisation protocols of the forward kernel with two Q tiles per
-CTA: bf16 with a dedicated S-issuer warp (`run`), either at d = 64 (three rotating S buffers in
-tensor memory that P aliases, mode "s3") or at d = 128 (one S buffer both tiles share, P in a
-tensor-memory area per tile, mode "s1"); and e4m3 at d = 128 (P in shared memory, S_{j+1} issued
-once S_j is loaded; `run_psmem`).
+"""Executable model of the synchronisation protocols of the forward kernel with two Q tiles per
+CTA and a dedicated S-issuer warp (`run`): at d = 64 three rotating S buffers in tensor memory that
+P aliases (mode "s3"), at d = 128 (bf16 and e4m3) one S buffer both tiles share with P in a
+tensor-memory area per tile (mode "s1").
 
 This is test infrastructure: a model of the kernel's warp roles and mbarriers, not the kernel. It
 runs the roles as Python generators under random interleavings and checks three things:
@@ -41,7 +40,7 @@ has not landed, and its parity wait then passes two phases early.
   TMA        lands the producer's K/V copies in any order.
 
 Each Q tile has M S-ready, P-ready and PV-done barriers, its g-th S product using index g % M and
-phase g // M. The kernel uses M = 3. `run_psmem` documents its own roles.
+phase g // M. The kernel uses M = 3 at d = 64 and M = 1 in mode "s1".
 """
 import random
 
@@ -333,206 +332,6 @@ def sweep(n_cases, case_seed, **kw):
         for shared, rp in SCHEDULES:
             try:
                 run(tiles, seed=i * 7 + shared + int(rp * 10), shared_pipe=shared, rescale_p=rp, **kw)
-            except ProtocolError as e:
-                return f"{kind} {tiles}: {e}"
-    return None
-
-
-def run_psmem(tiles, seed, shared_pipe=True, rescale_p=0.3, skip_read_wait=False, skip_pv_wait=False):
-    """The e4m3 two-Q-tile pipeline with P in shared memory.
-
-    Each Q tile has one TMEM S buffer and one shared-memory P tile. Issuer q (one per Q tile,
-    alternating S turns with the other) puts S_{j+1} into its buffer once its softmax has loaded
-    S_j (s_read), then issues PV_j from the P tile after both P halves (p_half). Each PV commits
-    o_done; the softmax waits for PV_{j-1} there before it overwrites P or rescales O.
-    """
-    rnd = random.Random(seed)
-    q_full, q_empty = Bar("q_full", 1), Bar("q_empty", 2)
-    kv_full = [Bar(f"kv_full{i}", 1) for i in range(NS)]
-    kv_empty = [Bar(f"kv_empty{i}", 2) for i in range(NS)]
-    s_turn = [Bar("s_turn0", 1, pre=1), Bar("s_turn1", 1)]
-    s_full = [Bar(f"s_full{q}", 1) for q in range(2)]
-    s_read = [Bar(f"s_read{q}", 1) for q in range(2)]
-    p_half = [[Bar(f"p_half{q}.{h}", 1) for h in range(2)] for q in range(2)]
-    o_done = [Bar(f"o_done{q}", 1) for q in range(2)]
-    o_full = [Bar(f"o_full{q}", 1) for q in range(2)]
-    s_buf = [None, None]          # TMEM: ("S", g) written, ("read", g) once loaded
-    p_buf = [None, None]          # shared memory: ("P", g) written, ("used", g) once PV read it
-    pv_complete = {0: set(), 1: set()}
-    queues = {0: [], 1: []}
-    shared = []
-
-    def enqueue(iss, op):
-        (shared if shared_pipe else queues[iss]).append(op)
-
-    def producer():
-        ring, nq = 0, 0
-        for (n0, n1) in tiles:
-            nmax = max(n0, n1)
-            if nmax == 0:
-                continue
-            if nq > 0:
-                yield from wait(q_empty, (nq - 1) & 1, nq - 1)
-            nq += 1
-            yield
-            q_full.arrive()
-            for _ in range(2 * nmax):
-                slot = ring % NS
-                if ring >= NS:
-                    yield from wait(kv_empty[slot], (ring // NS - 1) & 1, ring // NS - 1)
-                yield
-                kv_full[slot].arrive()
-                ring += 1
-
-    def issuer(myq):
-        ring, nq, turns, g, p_cnt, sr_cnt = 0, 0, 0, 0, 0, 0
-        read_pending = False
-
-        def wait_read():
-            nonlocal sr_cnt, read_pending
-            if read_pending and not skip_read_wait:
-                yield from wait(s_read[myq], sr_cnt & 1, sr_cnt)
-                sr_cnt += 1
-            read_pending = False
-
-        def s_turn_(issue, gj):
-            nonlocal turns
-            yield from wait(s_turn[myq], turns & 1, turns)
-            turns += 1
-            if issue:
-                enqueue(myq, ("S", myq, gj))
-                enqueue(myq, ("commit", s_full[myq]))
-            s_turn[myq ^ 1].arrive()
-
-        def release(bar, used):
-            if used:
-                enqueue(myq, ("commit", bar))
-            else:
-                bar.arrive()
-
-        for ti, (n0, n1) in enumerate(tiles):
-            n, nmax = (n1 if myq else n0), max(n0, n1)
-            if nmax == 0:
-                continue
-            gb = g
-            g += n
-            yield from wait(q_full, nq & 1, nq)
-            nq += 1
-            base = ring
-            yield from wait(kv_full[base % NS], (base // NS) & 1, base // NS)
-            if n > 0:
-                yield from wait_read()
-            yield from s_turn_(n > 0, gb)
-            read_pending = read_pending or n > 0
-            release(kv_empty[base % NS], n > 0)
-            if nmax == 1:
-                release(q_empty, n > 0)
-            for j in range(nmax):
-                if j + 1 < nmax:
-                    pos_k = base + 2 * (j + 1)
-                    yield from wait(kv_full[pos_k % NS], (pos_k // NS) & 1, pos_k // NS)
-                    if j + 1 < n:
-                        yield from wait_read()
-                    yield from s_turn_(j + 1 < n, gb + j + 1)
-                    read_pending = read_pending or j + 1 < n
-                    release(kv_empty[pos_k % NS], j + 1 < n)
-                    if j + 2 == nmax:
-                        release(q_empty, n > 0)
-                pos_v = base + 2 * j + 1
-                yield from wait(kv_full[pos_v % NS], (pos_v // NS) & 1, pos_v // NS)
-                if j < n:
-                    for h in range(2):
-                        yield from wait(p_half[myq][h], p_cnt & 1, p_cnt)
-                    p_cnt += 1
-                    enqueue(myq, ("PV", myq, gb + j, ti, j))
-                    enqueue(myq, ("commit", o_done[myq]))
-                    if j + 1 == n:
-                        enqueue(myq, ("commit", o_full[myq]))
-                release(kv_empty[pos_v % NS], j < n)
-                yield
-            ring = base + 2 * nmax
-
-    def softmax(qt):
-        g, pv_cnt, tiles_done = 0, 0, 0
-        for ti, (n0, n1) in enumerate(tiles):
-            n = n1 if qt else n0
-            gb = g
-            g += n
-            if n == 0:
-                continue
-            for j in range(n):
-                gj = gb + j
-                yield from wait(s_full[qt], gj & 1, gj)
-                if s_buf[qt] != ("S", gj):
-                    raise ProtocolError(f"softmax {qt} expected S{gj}, found {s_buf[qt]}")
-                s_buf[qt] = ("read", gj)
-                s_read[qt].arrive()
-                yield
-                if j > 0 and not skip_pv_wait:
-                    yield from wait(o_done[qt], (pv_cnt + j - 1) & 1, pv_cnt + j - 1)
-                if j > 0 and rnd.random() < rescale_p and (ti, j - 1) not in pv_complete[qt]:
-                    raise ProtocolError("O rescaled while PV_{j-1} may still accumulate into it")
-                if p_buf[qt] is not None and p_buf[qt][0] != "used":
-                    raise ProtocolError(f"P{gj} overwrites {p_buf[qt]} before its PV read it")
-                p_buf[qt] = ("P", gj)
-                p_half[qt][0].arrive()
-                yield
-                p_half[qt][1].arrive()
-            yield from wait(o_full[qt], tiles_done & 1, tiles_done)
-            if any((ti, j) not in pv_complete[qt] for j in range(n)):
-                raise ProtocolError("epilogue read O before the tile's last PV completed")
-            pv_cnt += n
-            tiles_done += 1
-
-    def execute(op):
-        if op[0] == "S":
-            _, q, gj = op
-            if s_buf[q] is not None and s_buf[q][0] != "read":
-                raise ProtocolError(f"S{gj} of tile {q} overwrites {s_buf[q]} before the softmax loaded it")
-            s_buf[q] = ("S", gj)
-        elif op[0] == "PV":
-            _, q, gj, ti, j = op
-            if p_buf[q] != ("P", gj):
-                raise ProtocolError(f"PV{gj} of tile {q} reads {p_buf[q]}")
-            p_buf[q] = ("used", gj)
-            pv_complete[q].add((ti, j))
-        else:
-            op[1].arrive()
-
-    def pipe(q):
-        while True:
-            if q:
-                execute(q.pop(0))
-            yield
-
-    procs = {"producer": producer(), "iss0": issuer(0), "iss1": issuer(1), "softmax0": softmax(0),
-             "softmax1": softmax(1)}
-    finite = set(procs)
-    if shared_pipe:
-        procs["pipe"] = pipe(shared)
-    else:
-        procs["pipe0"], procs["pipe1"] = pipe(queues[0]), pipe(queues[1])
-    steps = 0
-    while finite:
-        name = rnd.choice(list(procs))
-        try:
-            next(procs[name])
-        except StopIteration:
-            del procs[name]
-            finite.discard(name)
-        steps += 1
-        if steps > 1_000_000:
-            raise ProtocolError("no progress: " + ", ".join(sorted(finite)))
-
-
-def sweep_psmem(n_cases, case_seed, **kw):
-    rnd = random.Random(case_seed)
-    for i in range(n_cases):
-        kind = ("noncausal", "causal", "ragged")[i % 3]
-        tiles = random_tiles(rnd, kind)
-        for shared, rp in SCHEDULES:
-            try:
-                run_psmem(tiles, seed=i * 7 + shared + int(rp * 10), shared_pipe=shared, rescale_p=rp, **kw)
             except ProtocolError as e:
                 return f"{kind} {tiles}: {e}"
     return None
