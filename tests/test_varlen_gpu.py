@@ -5,6 +5,8 @@
   tile and 256-row work-tile edges, empty query or key sequences, more queries than keys (rows
   that see nothing under the bottom-right causal mask) and more keys than queries, GQA, every
   head dim, e4m3.
+* Sequences that end in the first half of a work tile, over hundreds of launches: every launch
+  finishes and gives the same bits.
 * The plan read back: a permutation of all (sequence, head, query block) tiles, costs never
   increasing. A plan built for other arguments, or from bad offsets, is refused on the GPU: the
   forward writes nothing and the status word reports it.
@@ -103,6 +105,32 @@ def test_varlen_parity(w):
     x = inputs.make_varlen_inputs(w)
     o, lse, _ = run_varlen(w, x)
     check(w, x, o, lse)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
+def test_ragged_ends_over_many_launches(dtype):
+    # Every sequence ends in the first half of a 256-row work tile, so its last work tile has a
+    # second Q tile with no keys while the first one walks up to 17 key tiles. The issuer of that
+    # idle tile then only paces itself on the K/V ring, the case that needs the ring's even stage
+    # count. Hundreds of launches back to back must all finish (no bounded wait gives up) and
+    # give the same bits; the first is checked against the oracle.
+    w = vw("ragged_ends_" + dtype, [256 * k + 100 for k in range(1, 9)], H=4, Hkv=2, dtype=dtype, seed=8200)
+    x = inputs.make_varlen_inputs(w)
+    o, lse, plan = run_varlen(w, x)
+    check(w, x, o, lse)
+    cu_q = torch.tensor(w.cu_q, dtype=torch.int32, device="cuda")
+    cu_k = torch.tensor(w.cu_k, dtype=torch.int32, device="cuda")
+    kw = {}
+    if dtype == "fp8_e4m3":
+        kw = {n: torch.tensor([s], dtype=torch.float32, device="cuda")
+              for n, s in (("descale_q", x.descale_q), ("descale_k", x.descale_k), ("descale_v", x.descale_v))}
+    q, k, v = x.q.cuda(), x.k.cuda(), x.v.cuda()
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    for _ in range(400):
+        binding.attn_fwd_varlen(q, k, v, cu_q, cu_k, plan, w.causal, scale=w.scale, out=o2, lse=lse2, **kw)
+    st, detail = binding.attn_get_status()
+    assert st == binding.ATTN_OK, (st, hex(detail))
+    assert torch.equal(o2, o) and torch.equal(lse2, lse)
 
 
 @pytest.mark.parametrize("d,causal", [(64, True), (128, True), (128, False), (256, True)])
