@@ -197,11 +197,20 @@ FWD_KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "ptx.cuh", "varlen.cuh", "launch_im
                       "attn_fwd_bf16_d64.cu", "attn_fwd_bf16_d256.cu", "attn_fwd_fp8_d128.cu")
 
 
+def _code_only(text: str) -> str:
+    """The source without comments, blank lines or trailing blanks: edits to comments alone leave
+    the hash, and so the committed traffic figures, in force."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     for name in FWD_KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(ROOT, "exact_attention_72_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

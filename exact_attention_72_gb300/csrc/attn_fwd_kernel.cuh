@@ -161,13 +161,14 @@ struct AttnCfg {
   static constexpr int O_COL = S3 ? 384 : 256;            // O tile qt at O_COL + qt * D
   static constexpr int TMEM_COLS = 512;
   // Roles: warps [0, 4 NQ) softmax (one warpgroup per Q tile), then one MMA-issuer warp per Q
-  // tile, then the TMA warp. With two Q tiles each tile has its own issuer, so one issuer's
-  // waits for its softmax never hold up the other tile's MMAs.
+  // tile, then the TMA warp. With two Q tiles each tile's warp issues its PVs, so one issuer's
+  // waits for its softmax never hold up the other tile's MMAs, and a warp of its own issues
+  // every S.
   static constexpr int MMA_WARPS = NQ;
   static constexpr int SOFTMAX_WARPS = 4 * NQ;            // one warpgroup per Q tile
   static constexpr int WARP_MMA = SOFTMAX_WARPS, WARP_LOAD = SOFTMAX_WARPS + MMA_WARPS;
-  static constexpr int WARP_S = WARP_LOAD + 1;            // three-buffer mode: the S issuer
-  // Two Q tiles: 12 warps (softmax x8, MMA x2, load, and the S issuer at d = 64, else idle) so the
+  static constexpr int WARP_S = WARP_LOAD + 1;            // two Q tiles: the S issuer
+  // Two Q tiles: 12 warps (softmax x8, PV issuers x2, load, S issuer) so the
   // third warpgroup can hand registers to the softmax warpgroups with setmaxnreg. The launch gives
   // 384 x 168 = 64,512 registers; the split below takes 256 x 200 + 128 x 96 = 63,488 of them.
   // (256 x 216 + 128 x 72 at d = 64 was faster while the softmax took its row maximum with a
