@@ -1113,7 +1113,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           m_tile = fmax3(fmax3(a8[0], a8[1], a8[2]), fmax3(a8[3], a8[4], a8[5]), fmaxf(a8[6], a8[7])) * s;
         }
         if (r == 0) ATTN_TRACE(6, qt, j);
-        if constexpr (C::S1) {
+        // e4m3 with the shared S buffer writes both P halves at once after the second half's
+        // exponentials (its PVs are short, so an early first half buys little), and waits for
+        // PV_{j-1} only there or before a rescale of O.
+        constexpr bool LATE_P = C::S1 && C::FP8;
+        if constexpr (C::S1 && !LATE_P) {
           // S_j may have been issued before PV_{j-1}: wait for that PV before P_j overwrites
           // P_{j-1} in this tile's P area and before any rescale of O.
           if (j > 0) {
@@ -1139,7 +1143,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
               const uint32_t gp = gb + j - 1;   // this tile's PV_{j-1}
               w = mbar_wait(smem_addr(&bar_o_done[3 * qt + gp % 3u]), (gp / 3u) & 1u, ctl, SITE_O_DONE);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-            } else if constexpr (C::NQ == 1) {
+            } else if constexpr (C::NQ == 1 || LATE_P) {
               w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
               if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
             }
@@ -1161,10 +1165,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
           acc1 = acc0;
           exp_half(0, f2_pack(-m, -m), pk, acc0, acc1);
         }
-        store_half(0, pk);
-        exp_half(1, f2_pack(-m, -m), pk, acc0, acc1);
-        if (r == 0) ATTN_TRACE(17, qt, j);
-        store_half(1, pk);
+        if constexpr (LATE_P) {
+          uint32_t pk1[PKN];
+          exp_half(1, f2_pack(-m, -m), pk1, acc0, acc1);
+          if (r == 0) ATTN_TRACE(17, qt, j);
+          // PV_{j-1} still reads P_{j-1} from this tile's P area. (After a rescale this phase has
+          // completed already; o_done cannot complete another before P_j is handed over.)
+          if (j > 0) {
+            w = mbar_wait(smem_addr(&bar_o_done[qt]), (pv_cnt + j - 1) & 1, ctl, SITE_O_DONE);
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          }
+          const uint32_t tP = tmem + lane_base + C::P_COL + (uint32_t)C::P_COLS * qt;
+          tmem_st_16cols(tP, pk);
+          tmem_st_16cols(tP + 16, pk1);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_addr(&bar_p_half[buf][0]));
+            mbar_arrive(smem_addr(&bar_p_half[buf][1]));
+          }
+          if (r == 0) ATTN_TRACE(8, qt, j);
+        } else {
+          store_half(0, pk);
+          exp_half(1, f2_pack(-m, -m), pk, acc0, acc1);
+          if (r == 0) ATTN_TRACE(17, qt, j);
+          store_half(1, pk);
+        }
         float l0, l1, l2, l3;
         f2_unpack(acc0, l0, l1);
         f2_unpack(acc1, l2, l3);
