@@ -18,16 +18,20 @@ def _built(cuda_device):
     binding.attn_debug_set(timeout_ns=1_000_000_000)   # a correct launch never waits this long
 
 
-# The last case has its keys halved across two launches; CTA 0 of each skips a copy.
-@pytest.mark.parametrize("d,causal,N", [(128, True, 512), (256, False, 512), (64, False, 512), (128, False, 2048)])
-def test_skipped_copy_times_out_and_context_survives(d, causal, N):
-    w = inputs.Workload("fault", B=1, H=4, Hkv=2, N=N, d=d, causal=causal, seed=3)
+# The fourth case has its keys halved across two launches; CTA 0 of each skips a copy. The e4m3
+# cases run the pipeline whose softmax warps exchange row maxima in pairs.
+@pytest.mark.parametrize("d,causal,N,dtype", [(128, True, 512, "bf16"), (256, False, 512, "bf16"),
+                                              (64, False, 512, "bf16"), (128, False, 2048, "bf16"),
+                                              (128, True, 512, "fp8_e4m3"), (128, False, 2048, "fp8_e4m3")])
+def test_skipped_copy_times_out_and_context_survives(d, causal, N, dtype):
+    w = inputs.Workload("fault", B=1, H=4, Hkv=2, N=N, d=d, causal=causal, seed=3, dtype=dtype)
     x = inputs.make_inputs(w)
-    q, k, v, _ = to_device(x)
+    q, k, v, desc = to_device(x)
+    kw = {} if desc is None else dict(descale_q=desc[0], descale_k=desc[1], descale_v=desc[2])
     binding.attn_clear_status()
     binding.attn_debug_set(timeout_ns=50_000_000, skip_load=True)
     try:
-        binding.attn_fwd(q, k, v, causal=causal)
+        binding.attn_fwd(q, k, v, causal=causal, **kw)
         st, detail = binding.attn_get_status()
     finally:
         binding.attn_debug_set(1_000_000_000, False)
