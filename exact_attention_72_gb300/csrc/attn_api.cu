@@ -188,18 +188,21 @@ bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// [B, N, heads, d] tensor -> 4-D map (d, N, heads, B), box (128-byte row, 128 rows, 1, 1),
-// 128-byte swizzle; rows past N read as zeros.
+// [B, N, heads, d] tensor -> 4-D map (d, N, heads, B), box (one swizzle row, 128 rows, 1, 1);
+// rows past N read as zeros. The swizzle row is 128 bytes, or 64 where a whole row of d is 64
+// bytes (e4m3 at d = 64), as the kernel's AttnCfg::SWZ.
 bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int heads, int B, int box_rows = 128) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t elt = fp8 ? 1 : 2;
+  const bool swz64 = d * elt < 128;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)heads * d * elt, (cuuint64_t)d * elt, (cuuint64_t)N * heads * d * elt};
-  cuuint32_t box[4] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)((swz64 ? 64 : 128) / elt), (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
-             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -251,7 +254,7 @@ size_t splitkv_part_o_bytes(int B, int H, int Nq, int d, int S) {
 
 bool supported_dim(int d, attn_dtype_t dtype) {
   if (dtype == ATTN_DTYPE_BF16) return d == 64 || d == 128 || d == 256;
-  if (dtype == ATTN_DTYPE_FP8_E4M3) return d == 128 || d == 256;
+  if (dtype == ATTN_DTYPE_FP8_E4M3) return d == 64 || d == 128 || d == 256;
   return false;
 }
 
@@ -274,7 +277,7 @@ attn_status_t check_shape(int B, int H, int Hkv, int N, int d, float scale, attn
 
 template <int D>
 cudaError_t dispatch_d(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128 || D == 256) {
+  if constexpr (D == 64 || D == 128 || D == 256) {
     if (fp8) return causal ? gb300::launch_attn_fwd<D, true, true>(a, s) : gb300::launch_attn_fwd<D, false, true>(a, s);
   }
   return causal ? gb300::launch_attn_fwd<D, true, false>(a, s) : gb300::launch_attn_fwd<D, false, false>(a, s);
@@ -567,6 +570,8 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   if (st != ATTN_OK) return st;
   st = check_shape(B, H, Hkv, Nq, d, scale, dtype);
   if (st != ATTN_OK) return st;
+  // The split-KV instances are built for e4m3 at d = 128 and 256 only.
+  if (dtype == ATTN_DTYPE_FP8_E4M3 && d == 64) return ATTN_ERR_UNSUPPORTED;
   const int G = H / Hkv;
   if (G > 128 || (128 % G) != 0) return ATTN_ERR_UNSUPPORTED;   // G packed rows must tile 128
   const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
@@ -670,6 +675,8 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
   if (total_q < 0 || total_k < 0 || B < 1) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_shape(1, H, Hkv, total_q > 0 ? total_q : 1, d, scale, dtype);
   if (st != ATTN_OK) return st;
+  // The varlen instances are built for e4m3 at d = 128 and 256 only.
+  if (dtype == ATTN_DTYPE_FP8_E4M3 && d == 64) return ATTN_ERR_UNSUPPORTED;
   if (varlen_tile_bound(B, H, total_q, d) >= INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
   if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || !plan) return ATTN_ERR_INVALID_ARG;

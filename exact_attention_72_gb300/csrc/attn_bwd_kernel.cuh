@@ -65,6 +65,7 @@ struct BwdCfg {
   static constexpr int CE = 64;                           // bf16 elements in one 128-byte row
   static constexpr int NCH = D / CE;
   static constexpr int CHUNK_BYTES = 128 * 128;
+  static constexpr int SWZ = 128, SBO = 1024;             // 128-byte swizzle (issue_qk)
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // 128 rows x D bf16
   static constexpr int KSTEPS_QK = D / 16;
   static constexpr int KSTEPS_PV = 8;                     // 128 rows of the MN-major B operand

@@ -113,9 +113,13 @@ struct AttnCfg {
   // they take the one-tile pipeline, whose S double buffer lets S_{j+1} run during softmax j.
   static constexpr int NQ = (D <= 128 && !SPLIT_) ? 2 : 1;
   static constexpr int BM = 128, BN = 128;                // query rows per Q tile, keys per KV tile
-  static constexpr int CE = 128 / ELT;                    // elements in one 128-byte swizzle row
-  static constexpr int NCH = D / CE;                      // 128-byte column chunks per row
-  static constexpr int CHUNK_BYTES = 128 * 128;           // 128 rows x 128 bytes (one TMA box)
+  // Tiles are stored with the 128-byte swizzle, except e4m3 at d = 64, whose 64-byte rows take
+  // the 64-byte swizzle (the TMA box and the MMA descriptors use the same one).
+  static constexpr int SWZ = D * ELT < 128 ? 64 : 128;   // bytes per swizzle row
+  static constexpr int CE = SWZ / ELT;                    // elements in one swizzle row
+  static constexpr int NCH = D / CE;                      // swizzle-row column chunks per row
+  static constexpr int CHUNK_BYTES = 128 * SWZ;           // 128 rows of one chunk (one TMA box)
+  static constexpr int SBO = 8 * SWZ;                     // stride between 8-row groups
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;    // one Q, K or V tile
   static constexpr int Q_BYTES = NQ * TILE_BYTES;
   // Non-causal bf16 prefill at d <= 128 may take the share deal of its last tiles (tail_mode 3).
@@ -189,7 +193,7 @@ struct AttnCfg {
   static_assert(NS >= 2, "K/V ring needs at least two stages");
   static_assert(!SISS || NS % 2 == 0, "an S-issuer warp needs an even number of K/V stages");
   static_assert(O_COL + NQ * D <= TMEM_COLS, "TMEM budget");
-  static_assert(D % CE == 0, "head dim must fill whole 128-byte rows");
+  static_assert(D % CE == 0, "head dim must fill whole swizzle rows");
 };
 
 // Wait-site codes recorded in the status word when a bounded wait gives up.
@@ -443,11 +447,12 @@ __device__ __forceinline__ int s_buf_idx(int qt, int j) {
 template <class C>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr,
                                          uint32_t idesc = C::IDESC_QK) {
-  const uint64_t a0 = make_sdesc_sw128(a_addr, 16, 1024);
-  const uint64_t b0 = make_sdesc_sw128(b_addr, 16, 1024);
+  const uint64_t a0 = make_sdesc_swz(a_addr, 16, C::SBO, C::SWZ);
+  const uint64_t b0 = make_sdesc_swz(b_addr, 16, C::SBO, C::SWZ);
+  constexpr int KPR = C::SWZ / 32;   // k-steps per swizzle row
 #pragma unroll
   for (int kk = 0; kk < C::KSTEPS_QK; ++kk) {
-    const uint64_t off = (uint64_t)(((kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32) >> 4);
+    const uint64_t off = (uint64_t)(((kk / KPR) * C::CHUNK_BYTES + (kk % KPR) * 32) >> 4);
     mma_f16_or_f8<C::FP8>(d_tmem, a0 + off, b0 + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
@@ -458,12 +463,12 @@ template <class C, int H>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_addr,
                                               bool accumulate_first) {
   constexpr int KH = C::KSTEPS_PV / 2;
-  const uint64_t b0 = make_sdesc_sw128(b_addr, C::CHUNK_BYTES, 1024);
+  const uint64_t b0 = make_sdesc_swz(b_addr, C::CHUNK_BYTES, C::SBO, C::SWZ);
 #pragma unroll
   for (int i = 0; i < KH; ++i) {
     const int kk = H * KH + i;
     const uint32_t acc = (H > 0 || i > 0) ? 1u : (accumulate_first ? 1u : 0u);
-    mma_ts_f16_or_f8<C::FP8>(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * C::PV_ROWS * 128) >> 4),
+    mma_ts_f16_or_f8<C::FP8>(d_tmem, a_tmem + kk * 8, b0 + (uint64_t)((kk * C::PV_ROWS * C::SWZ) >> 4),
                              C::IDESC_PV, acc);
   }
 }

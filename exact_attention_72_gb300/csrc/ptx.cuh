@@ -200,17 +200,22 @@ constexpr uint32_t kIdescNegateA = 1u << 13;
 constexpr uint32_t kFmtBF16 = 1;
 constexpr uint32_t kFmtE4M3 = 0;
 
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand (tcgen05 format):
+// Shared-memory matrix descriptor for a swizzled operand (tcgen05 format):
 //   bits 0-13 start address >> 4; 16-29 leading-dimension byte offset >> 4;
 //   32-45 stride-dimension byte offset >> 4; bits 46-47 = 1 (descriptor version);
-//   bits 49-51 base offset (0: swizzle atoms are 1024-byte aligned); bits 61-63 = 2 (SW128).
-__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+//   bits 49-51 base offset (0: the swizzle pattern's repeat is aligned); bits 61-63 layout:
+//   2 = 128-byte swizzle, 4 = 64-byte swizzle.
+__device__ __forceinline__ uint64_t make_sdesc_swz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                                   uint32_t swizzle_bytes) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
   d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
+  d |= (uint64_t)(swizzle_bytes == 64u ? 4u : 2u) << 61;
   return d;
+}
+__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return make_sdesc_swz(saddr, lbo_bytes, sbo_bytes, 128u);
 }
 
 #define GB300_R8(p, i) "=r"(p[i]), "=r"(p[i + 1]), "=r"(p[i + 2]), "=r"(p[i + 3]), "=r"(p[i + 4]), \

@@ -53,7 +53,7 @@ typedef enum {
  *   o      [B, N, H,   d]  bfloat16 output
  *   lse    [B, H, N]       float32 output, LSE_i = ln sum_j exp(scale * q_i . k_j) over the
  *                          keys row i may see (all keys, or j <= i when causal)
- *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16, d in {128, 256} for fp8.
+ *   B, H, Hkv, N >= 1, H % Hkv == 0; d in {64, 128, 256} for bf16 and for fp8.
  *   scale  finite, nonzero float multiplying the raw dot products (usually 1/sqrt(d)); it does
  *          not include the fp8 descales. A negative scale is allowed (the kernel computes
  *          |scale| * (-Q) K^T, so the softmax's running maximum is taken over the scaled scores
@@ -125,7 +125,7 @@ int attn_fwd_tail_units(int B, int H, int N, int d, int causal, attn_dtype_t dty
  * heads differ in magnitude: "flash-attention-3" (ai.thesatyajit.com), "FP8 is a different
  * kernel" (descale pointers with strides).
  *   descale arrays: DEVICE fp32, large enough for every (b, head) the strides address.
- *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128 or 256).
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 64, 128 or 256).
  */
 attn_status_t attn_fwd_fp8_scaled(const void* q, const void* k, const void* v, void* o,
                                   float* lse, int B, int H, int Hkv, int N, int d, float scale,
@@ -171,7 +171,8 @@ attn_status_t attn_varlen_plan(const int* cu_seqlens_q, const int* cu_seqlens_k,
  *         on the GPU (nothing is written, and attn_get_status reports ATTN_ERR_INVALID_ARG); so
  *         is a tile whose sequence's rows fall outside the packed tensors (that tile is skipped).
  *   descale_q/k/v: e4m3 only, one fp32 each (per tensor), as in attn_fwd.
- * Same argument checks as attn_fwd; total_q == 0 returns ATTN_OK at once.
+ * Same argument checks as attn_fwd, except that e4m3 at d == 64 returns ATTN_ERR_UNSUPPORTED
+ * (built for d == 128 and 256); total_q == 0 returns ATTN_OK at once.
  */
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                               const int* cu_seqlens_q, const int* cu_seqlens_k, const void* plan,
@@ -220,7 +221,7 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
  *   Descales must be positive and finite. attn_quantize_e4m3 writes codes and descales in these
  *   layouts (block_rows 128 for q, 64 for k, N for v). q and k may both be rotated by the same
  *   orthogonal matrix: the scores do not change.
- *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 128 or 256).
+ *   Everything else as attn_fwd with dtype ATTN_DTYPE_FP8_E4M3 (d == 64, 128 or 256).
  */
 attn_status_t attn_fwd_fp8_blockscaled(const void* q, const void* k, const void* v, void* o,
                                        float* lse, int B, int H, int Hkv, int N, int d,
@@ -293,8 +294,9 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_d
  *   section 11 ("PackGQA": query heads of a GQA group are packed into the 128-row tile).
  *
  *   q [B, Nq, H, d], k/v [B, Nk, Hkv, d], o [B, Nq, H, d] bf16, lse [B, H, Nq] fp32: DEVICE
- *   memory, same element types, alignment and descale rules as attn_fwd. H / Hkv must divide
- *   128. 1 <= num_splits <= 128.
+ *   memory, same element types, alignment and descale rules as attn_fwd (e4m3 for d == 128 and
+ *   256 only; d == 64 returns ATTN_ERR_UNSUPPORTED). H / Hkv must divide 128.
+ *   1 <= num_splits <= 128.
  *   workspace: caller-owned DEVICE memory of at least
  *   attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes, 256-byte aligned, not
  *   overlapping the other buffers; it holds the partial results and needs no initialization.

@@ -68,7 +68,7 @@ def test_validation_rejects_bad_arguments(lib):
     assert _call(lib, scale=float("inf")) == INV
     assert _call(lib, dtype=7) == INV
     assert _call(lib, d=96) == UNS                        # head dim without an instance
-    assert _call(lib, d=64, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # e4m3 only for d = 128 and 256
+    assert _call(lib, d=96, dtype=1, dq=1 << 24, dk=1 << 24, dv=1 << 24) == UNS   # e4m3: d = 64, 128, 256
     assert _call(lib, scale=0.0) == UNS                  # 0 * (-inf) for masked scores
     assert _call(lib, dtype=1) == INV                     # fp8 without descales
     assert _call(lib, q=4097) == INV                      # misaligned (TMA needs 16 bytes)
@@ -103,6 +103,7 @@ def test_splitkv_validation(lib):
     assert call(splits=129) == INV
     assert call(H=6, Hkv=2) == UNS                 # group of 3 heads cannot tile 128 rows
     assert call(d=96) == UNS
+    assert call(d=64, dtype=1) == UNS               # split-KV e4m3 is built for d = 128 and 256
     assert call(ws_bytes=16) == INV                 # workspace too small
     assert call(ws=(1 << 28) + 8) == INV            # workspace misaligned
     assert call(ws=(1 << 16)) == INV                # workspace overlaps q
@@ -123,7 +124,7 @@ def test_fp8_scaled_validation(lib):
     assert call(dq=0) == INV                         # descale pointers are required
     assert call(dv=0) == INV
     assert call(N=0) == INV
-    assert call(d=64) == UNS                         # e4m3 is built for d = 128 and 256
+    assert call(d=96) == UNS                         # e4m3 is built for d = 64, 128 and 256
 
 
 def test_quantize_and_blockscaled_validation(lib):
@@ -147,7 +148,7 @@ def test_quantize_and_blockscaled_validation(lib):
                                             1 << 12, 1 << 13, 1 << 14, None)
 
     assert f(N=0) == INV and f(H=0) == INV
-    assert f(d=64) == UNS
+    assert f(d=96) == UNS
 
 
 def test_varlen_validation(lib):
@@ -167,14 +168,16 @@ def test_varlen_validation(lib):
     assert plan(p=(1 << 20) + 8) == INV          # plan not 16-byte aligned
     assert plan(nbytes=need - 1) == INV           # plan buffer too small
 
-    def fwd(q=1 << 16, plan=1 << 28, plan_bytes=1 << 16, B=3, H=4, Hkv=2, tq=1000, tk=900, d=128, scale=0.1):
+    def fwd(q=1 << 16, plan=1 << 28, plan_bytes=1 << 16, B=3, H=4, Hkv=2, tq=1000, tk=900, d=128, scale=0.1,
+            dtype=0):
         return lib.attn_fwd_varlen(q, 1 << 20, 1 << 24, 1 << 26, 1 << 27, 1 << 12, 1 << 13, plan, plan_bytes, B, H,
-                                   Hkv, tq, tk, d, scale, 1, 0, None, None, None, None)
+                                   Hkv, tq, tk, d, scale, 1, dtype, None, None, None, None)
 
     assert fwd(q=0) == INV and fwd(plan=0) == INV
     assert fwd(plan_bytes=16) == INV              # shorter than the plan header
     assert fwd(B=0) == INV and fwd(tq=-1) == INV and fwd(H=3, Hkv=2) == INV
     assert fwd(d=96) == UNS and fwd(scale=0.0) == UNS
+    assert fwd(d=64, dtype=1) == UNS              # varlen e4m3 is built for d = 128 and 256
     assert fwd(tq=0) == binding.ATTN_OK           # no query rows: nothing to do
 
 

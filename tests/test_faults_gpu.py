@@ -56,8 +56,6 @@ HOST_SHAPES = [
 @pytest.mark.parametrize("shape", HOST_SHAPES, ids=lambda s: "B{B}_H{H}_Hkv{Hkv}_N{N}_d{d}".format(**s))
 @pytest.mark.parametrize("dtype", ["bf16", "fp8_e4m3"])
 def test_host_entry_point_matches_device_entry_point(dtype, shape):
-    if dtype == "fp8_e4m3" and shape["d"] == 64:
-        pytest.skip("e4m3 instances are d = 128 and 256")
     w = inputs.Workload("host", dtype=dtype, seed=9, **shape)
     x = inputs.make_inputs(w)
     o_dev, lse_dev = run_cuda(w, x)

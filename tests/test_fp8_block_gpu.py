@@ -136,6 +136,9 @@ BCASES = [
     dict(B=1, H=4, Hkv=2, N=2100, causal=False, rot=False, seed=7005),
     # head dim 256 (one Q tile per work tile)
     dict(B=1, H=2, Hkv=1, N=300, causal=True, rot=True, seed=7006, d=256),
+    # head dim 64 (64-byte rows)
+    dict(B=1, H=4, Hkv=2, N=640, causal=True, rot=True, seed=7007, d=64),
+    dict(B=1, H=4, Hkv=2, N=2100, causal=False, rot=False, seed=7008, d=64),
 ]
 
 

@@ -39,6 +39,7 @@ CASES = [
     # d = 256 (128-row tiles): 17 key tiles, parts of 8 and 9, ragged query and key tails
     case("d256_ragged", H=3, Hkv=3, N=2100, d=256, seed=94),
     case("fp8_per_tensor", H=4, Hkv=2, N=2304, dtype="fp8_e4m3", seed=95),
+    case("fp8_d64", H=4, Hkv=2, N=4096, d=64, dtype="fp8_e4m3", seed=97),
     case("outliers", H=4, Hkv=1, N=2048, seed=96, k_outlier_frac=0.005),
 ]
 

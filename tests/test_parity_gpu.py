@@ -39,6 +39,9 @@ SMALL = [
     small("fp8_causal", B=1, H=2, Hkv=1, N=640, d=128, causal=True, dtype="fp8_e4m3"),
     small("fp8_d256_noncausal", B=1, H=2, Hkv=2, N=384, d=256, dtype="fp8_e4m3"),
     small("fp8_d256_causal_gqa", B=2, H=4, Hkv=2, N=640, d=256, causal=True, dtype="fp8_e4m3"),
+    # e4m3 at d = 64: 64-byte rows in the 64-byte swizzle
+    small("fp8_d64_noncausal", B=1, H=2, Hkv=2, N=512, d=64, dtype="fp8_e4m3"),
+    small("fp8_d64_causal_gqa", B=2, H=4, Hkv=2, N=640, d=64, causal=True, dtype="fp8_e4m3"),
     # 160 causal work tiles on a 152-SM grid: a second, partial turn dealt in reverse (zig-zag)
     small("causal_gqa_two_turns", B=1, H=40, Hkv=20, N=1024, d=128, causal=True, seed=78),
 ]
@@ -66,7 +69,7 @@ def test_ragged_lengths(N, causal, d):
 
 @pytest.mark.parametrize("N", [1, 129, 300])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_ragged_lengths_fp8(N, causal, d):
     w = small(f"ragged_fp8_{N}_{d}", B=1, H=2, Hkv=2, N=N, d=d, causal=causal, dtype="fp8_e4m3", seed=N + d)
     x = inputs.make_inputs(w)
