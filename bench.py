@@ -981,7 +981,8 @@ def main(argv=None):
         x = inputs.make_inputs(w)
         (run_bwd_reference if args.impl == "reference" else run_bwd_ours)(args, w, x)
         return 0
-    table = {**inputs.WORKLOADS, **inputs.DECODE_WORKLOADS, **inputs.FP8_BLOCK_WORKLOADS}
+    table = {**inputs.WORKLOADS, **inputs.DECODE_WORKLOADS, **inputs.FP8_BLOCK_WORKLOADS,
+             **inputs.EXTRA_FWD_WORKLOADS}
     w = table[name]
     if args.batch is not None:
         w = w.replace(B=args.batch, name=f"{w.name}_b{args.batch}")

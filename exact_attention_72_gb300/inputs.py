@@ -99,6 +99,13 @@ WORKLOADS = {
                                          causal=False, dtype="fp8_e4m3", seed=1005),
 }
 
+# Forward workloads beyond the five configurations: e4m3 at d = 64, in the shape of the d = 64
+# configuration.
+EXTRA_FWD_WORKLOADS = {
+    "fp8_noncausal_n16384_d64": Workload("fp8_noncausal_n16384_d64", B=1, H=16, Hkv=16, N=16384, d=64,
+                                         causal=False, dtype="fp8_e4m3", seed=1006),
+}
+
 # The headline workload the benchmark times.
 HEADLINE = "causal_gqa_bf16_n8192_d128"
 
