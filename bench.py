@@ -194,7 +194,7 @@ def hbm_peak():
 # Sources the forward kernel's device code is built from: a change to any of them voids the
 # committed DRAM-traffic figures (host-side files and other kernels do not).
 FWD_KERNEL_SOURCES = ("attn_fwd_kernel.cuh", "ptx.cuh", "varlen.cuh", "launch_impl.cuh", "attn_fwd_bf16_d128.cu",
-                      "attn_fwd_bf16_d64.cu", "attn_fwd_bf16_d256.cu", "attn_fwd_fp8_d128.cu")
+                      "attn_fwd_bf16_d64.cu", "attn_fwd_bf16_d256.cu", "attn_fwd_fp8_d128.cu", "attn_fwd_fp8_d64.cu")
 
 
 def _code_only(text: str) -> str:
