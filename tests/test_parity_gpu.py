@@ -95,7 +95,7 @@ def test_repeatable_bitwise():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-FULL = list(inputs.WORKLOADS.values())
+FULL = list(inputs.WORKLOADS.values()) + list(inputs.EXTRA_FWD_WORKLOADS.values())
 
 
 def sample_heads(w):
