@@ -222,25 +222,28 @@ bool make_rows_map(CUtensorMap* m, const void* base, int d, int N, int heads, in
 }
 
 // Packed GQA view of q [B, Nq, H, d] for split-KV decode: 5-D map (d, G, Nq, Hkv, B) so one box
-// (128-byte row, G heads, 128 / G positions, 1, 1) is 128 query rows of one kv head's group.
+// (one swizzle row, G heads, 128 / G positions, 1, 1) is 128 query rows of one kv head's group.
+// The swizzle row is 128 bytes, or 64 for e4m3 at d = 64, as in make_map.
 bool make_map_q_packed(CUtensorMap* m, const void* base, bool fp8, int d, int Nq, int H, int Hkv, int B) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t elt = fp8 ? 1 : 2;
+  const bool swz64 = d * elt < 128;
   const int G = H / Hkv;
   cuuint64_t dims[5] = {(cuuint64_t)d, (cuuint64_t)G, (cuuint64_t)Nq, (cuuint64_t)Hkv, (cuuint64_t)B};
   cuuint64_t strides[4] = {(cuuint64_t)d * elt, (cuuint64_t)H * d * elt, (cuuint64_t)G * d * elt,
                            (cuuint64_t)Nq * H * d * elt};
-  cuuint32_t box[5] = {(cuuint32_t)(128 / elt), (cuuint32_t)G, (cuuint32_t)(128 / G), 1, 1};
+  cuuint32_t box[5] = {(cuuint32_t)((swz64 ? 64 : 128) / elt), (cuuint32_t)G, (cuuint32_t)(128 / G), 1, 1};
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base),
-             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swz64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D>
 cudaError_t dispatch_split(gb300::LaunchArgs& a, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128 || D == 256) {
+  if constexpr (D == 64 || D == 128 || D == 256) {
     if (fp8) return gb300::launch_attn_fwd<D, false, true, true>(a, s);
   }
   return gb300::launch_attn_fwd<D, false, false, true>(a, s);
@@ -293,7 +296,7 @@ namespace {
 
 template <int D>
 cudaError_t dispatch_varlen(gb300::LaunchArgs& a, bool causal, bool fp8, cudaStream_t s) {
-  if constexpr (D == 128 || D == 256) {
+  if constexpr (D == 64 || D == 128 || D == 256) {
     if (fp8)
       return causal ? gb300::launch_attn_fwd<D, true, true, false, true>(a, s)
                     : gb300::launch_attn_fwd<D, false, true, false, true>(a, s);
@@ -570,8 +573,6 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   if (st != ATTN_OK) return st;
   st = check_shape(B, H, Hkv, Nq, d, scale, dtype);
   if (st != ATTN_OK) return st;
-  // The split-KV instances are built for e4m3 at d = 128 and 256 only.
-  if (dtype == ATTN_DTYPE_FP8_E4M3 && d == 64) return ATTN_ERR_UNSUPPORTED;
   const int G = H / Hkv;
   if (G > 128 || (128 % G) != 0) return ATTN_ERR_UNSUPPORTED;   // G packed rows must tile 128
   const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
@@ -675,8 +676,6 @@ attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void*
   if (total_q < 0 || total_k < 0 || B < 1) return ATTN_ERR_INVALID_ARG;
   attn_status_t st = check_shape(1, H, Hkv, total_q > 0 ? total_q : 1, d, scale, dtype);
   if (st != ATTN_OK) return st;
-  // The varlen instances are built for e4m3 at d = 128 and 256 only.
-  if (dtype == ATTN_DTYPE_FP8_E4M3 && d == 64) return ATTN_ERR_UNSUPPORTED;
   if (varlen_tile_bound(B, H, total_q, d) >= INT_MAX) return ATTN_ERR_UNSUPPORTED;
   const bool fp8 = dtype == ATTN_DTYPE_FP8_E4M3;
   if (!q || !k || !v || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || !plan) return ATTN_ERR_INVALID_ARG;

@@ -1,4 +1,5 @@
-// Split-KV (decode) instances of the attention forward: bf16 d = 64, 128, 256 and e4m3 d = 128.
+// Split-KV (decode) instances of the attention forward: bf16 d = 64, 128, 256 and e4m3 d = 128
+// (e4m3 d = 64 and 256 are built with their prefill instances).
 #include "launch_impl.cuh"
 
 namespace gb300 {

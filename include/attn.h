@@ -171,8 +171,7 @@ attn_status_t attn_varlen_plan(const int* cu_seqlens_q, const int* cu_seqlens_k,
  *         on the GPU (nothing is written, and attn_get_status reports ATTN_ERR_INVALID_ARG); so
  *         is a tile whose sequence's rows fall outside the packed tensors (that tile is skipped).
  *   descale_q/k/v: e4m3 only, one fp32 each (per tensor), as in attn_fwd.
- * Same argument checks as attn_fwd, except that e4m3 at d == 64 returns ATTN_ERR_UNSUPPORTED
- * (built for d == 128 and 256); total_q == 0 returns ATTN_OK at once.
+ * Same argument checks as attn_fwd; total_q == 0 returns ATTN_OK at once.
  */
 attn_status_t attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                               const int* cu_seqlens_q, const int* cu_seqlens_k, const void* plan,
@@ -294,9 +293,8 @@ size_t attn_fwd_host_workspace_bytes(int B, int H, int Hkv, int N, int d, attn_d
  *   section 11 ("PackGQA": query heads of a GQA group are packed into the 128-row tile).
  *
  *   q [B, Nq, H, d], k/v [B, Nk, Hkv, d], o [B, Nq, H, d] bf16, lse [B, H, Nq] fp32: DEVICE
- *   memory, same element types, alignment and descale rules as attn_fwd (e4m3 for d == 128 and
- *   256 only; d == 64 returns ATTN_ERR_UNSUPPORTED). H / Hkv must divide 128.
- *   1 <= num_splits <= 128.
+ *   memory, same element types, alignment and descale rules as attn_fwd. H / Hkv must divide
+ *   128. 1 <= num_splits <= 128.
  *   workspace: caller-owned DEVICE memory of at least
  *   attn_fwd_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes, 256-byte aligned, not
  *   overlapping the other buffers; it holds the partial results and needs no initialization.

@@ -103,7 +103,6 @@ def test_splitkv_validation(lib):
     assert call(splits=129) == INV
     assert call(H=6, Hkv=2) == UNS                 # group of 3 heads cannot tile 128 rows
     assert call(d=96) == UNS
-    assert call(d=64, dtype=1) == UNS               # split-KV e4m3 is built for d = 128 and 256
     assert call(ws_bytes=16) == INV                 # workspace too small
     assert call(ws=(1 << 28) + 8) == INV            # workspace misaligned
     assert call(ws=(1 << 16)) == INV                # workspace overlaps q
@@ -177,7 +176,6 @@ def test_varlen_validation(lib):
     assert fwd(plan_bytes=16) == INV              # shorter than the plan header
     assert fwd(B=0) == INV and fwd(tq=-1) == INV and fwd(H=3, Hkv=2) == INV
     assert fwd(d=96) == UNS and fwd(scale=0.0) == UNS
-    assert fwd(d=64, dtype=1) == UNS              # varlen e4m3 is built for d = 128 and 256
     assert fwd(tq=0) == binding.ATTN_OK           # no query rows: nothing to do
 
 

@@ -47,6 +47,7 @@ CASES = [
     dec("g16", B=1, H=16, Hkv=1, N=8, Nk=900, splits=4),
     dec("fp8", B=2, H=8, Hkv=2, N=4, Nk=1500, splits=4, dtype="fp8_e4m3"),
     dec("fp8_d256", B=1, H=4, Hkv=2, N=3, Nk=1100, d=256, splits=3, dtype="fp8_e4m3"),
+    dec("fp8_d64", B=2, H=8, Hkv=2, N=5, Nk=1300, d=64, splits=4, dtype="fp8_e4m3"),
     # the library's count for a single unit: one split per key tile (32 here), one wave
     dec("heuristic_one_unit", B=1, H=8, Hkv=1, N=1, Nk=4096, splits=0),
 ]

@@ -96,6 +96,9 @@ CASES = [
     vw("fp8_causal", [250, 600, 90], dtype="fp8_e4m3"),
     vw("fp8_noncausal", [250, 600, 90], [100, 600, 300], causal=False, dtype="fp8_e4m3"),
     vw("fp8_d256_causal", [300, 129, 40], H=2, Hkv=1, d=256, dtype="fp8_e4m3"),
+    vw("fp8_d64_causal", [333, 64, 517], H=8, Hkv=2, d=64, dtype="fp8_e4m3", seed=8020),
+    vw("fp8_d64_noncausal", [0, 200, 77, 130], [5, 200, 700, 400], d=64, causal=False, dtype="fp8_e4m3",
+       seed=8021),
     vw("many_short", inputs.varlen_lengths(40, 1, 90, 8001), H=2, Hkv=1),
 ]
 
