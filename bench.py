@@ -11,7 +11,7 @@ bf16 by default). Prints ONE JSON line on rank 0:
              ms_per_step and the roofline come from the median repeat, and every repeat's
              ms per step is listed;
   e2e        the same metric through attn_fwd_host (pinned host buffers, H2D of q/k/v and D2H
-             of o/lse inside the timed region);
+             of o/lse inside the timed region), the median of --repeats repeats of --steps calls;
   roofline   tensor-core bound: achieved TFLOP/s of the attention kernel against the measured
              dense bf16 peak (e4m3: x2 nominal ratio). A non-causal call whose last wave is halved
              along the keys runs the kernel as two launches; the step time covers both;
@@ -263,6 +263,27 @@ def timed_repeats(args, dist, stream, flush, step, with_mid=False):
     totals = [max_over_ranks(dist, sum(d)) for d in durs]
     med = sorted(range(R), key=lambda r: totals[r])[R // 2]
     return durs, mids, totals, med, t_host0, t_host1
+
+
+def timed_e2e(args, dist, stream, step):
+    """End-to-end timing: args.repeats repeats of args.steps calls of step(), each repeat
+    bracketed by a barrier and a synchronize and timed with CUDA events on `stream`; the repeat
+    totals are maxed over ranks. Returns (ms per step of the median repeat, ms per step of every
+    repeat), so a stall of the host in one repeat does not set the figure."""
+    import torch
+    per = []
+    for _ in range(max(1, args.repeats)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        per.append(max_over_ranks(dist, e0.elapsed_time(e1)) / args.steps)
+    return sorted(per)[len(per) // 2], per
 
 
 def cpu_oracle_sample(w, x, seconds: float, block_rows=512, max_steps=None):
@@ -578,21 +599,11 @@ def measure_e2e_block(args, w, x, dev, dist, world):
 
     for _ in range(max(args.warmup, 0)):
         step()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    ms, per = timed_e2e(args, dist, torch.cuda.current_stream(), step)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
-    return {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+    return {"value": w.flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "repeat_ms_per_step": per,
             "entry_point": "quantize_e4m3 + attn_fwd_fp8_blockscaled on pinned host buffers"}
 
 
@@ -613,21 +624,11 @@ def measure_e2e(args, w, x, dev, dist, world):
 
     for _ in range(max(args.warmup, 0)):
         step()
-    stream = torch.cuda.current_stream()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist)
-    ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    ms, per = timed_e2e(args, dist, torch.cuda.current_stream(), step)
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (12 if code else 0)
     d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
-    return {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms / args.steps,
+    return {"value": w.flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "repeat_ms_per_step": per,
             "entry_point": "attn_fwd_host"}
 
 
@@ -750,20 +751,11 @@ def run_bwd_ours(args, w, x):
 
         for _ in range(max(args.warmup, 0)):
             e2e_step()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-        ms = max_over_ranks(dist, e0.elapsed_time(e1))
-        e2e = {"value": flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms, per = timed_e2e(args, dist, stream, e2e_step)
+        e2e = {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hs),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outs_h),
-               "ms_per_step": ms / args.steps, "entry_point": "attn_bwd on pinned host copies"}
+               "ms_per_step": ms, "repeat_ms_per_step": per, "entry_point": "attn_bwd on pinned host copies"}
     clocks = sampler.summary(t_host0, t_host1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -925,20 +917,11 @@ def run_varlen_ours(args, w, x):
 
         for _ in range(max(args.warmup, 0)):
             e2e_step()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(dist)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-        ms = max_over_ranks(dist, e0.elapsed_time(e1))
-        e2e = {"value": w.flops * args.steps * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        ms, per = timed_e2e(args, dist, stream, e2e_step)
+        e2e = {"value": w.flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (qh, kh, vh)),
                "d2h_bytes_per_step": oh.numel() * oh.element_size() + lh.numel() * lh.element_size(),
-               "ms_per_step": ms / args.steps, "entry_point": "attn_fwd_varlen on pinned host copies"}
+               "ms_per_step": ms, "repeat_ms_per_step": per, "entry_point": "attn_fwd_varlen on pinned host copies"}
     clocks = sampler.summary(t_host0, t_host1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -36,6 +36,9 @@ def check_line(d, e2e=True):
     if e2e:
         e = d["e2e"]
         assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+        # the end-to-end step time is the median of its repeats too
+        er = sorted(e["repeat_ms_per_step"])
+        assert len(er) == d["repeats"] and abs(e["ms_per_step"] - er[len(er) // 2]) <= 1e-9 * max(1.0, e["ms_per_step"])
     assert d["gpu_launches"] >= d["steps"] * d["repeats"]
     assert "sm_mhz" in d["clocks"] and "reasons" in d["clocks"]
     # the reported step time is the median of the repeats' step times
