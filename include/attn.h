@@ -34,7 +34,7 @@ extern "C" {
 typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or overlap; nothing was launched   */
-  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement; nothing launched   */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement; nothing launched */
   ATTN_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, copy, sync, no GPU)  */
   ATTN_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (reported by attn_get_status)   */
 } attn_status_t;
