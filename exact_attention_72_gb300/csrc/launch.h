@@ -132,6 +132,8 @@ GB300_DECLARE_LAUNCH(128, false, false)
 GB300_DECLARE_LAUNCH(128, true, false)
 GB300_DECLARE_LAUNCH(256, false, false)
 GB300_DECLARE_LAUNCH(256, true, false)
+GB300_DECLARE_LAUNCH(64, false, true)
+GB300_DECLARE_LAUNCH(64, true, true)
 GB300_DECLARE_LAUNCH(128, false, true)
 GB300_DECLARE_LAUNCH(128, true, true)
 GB300_DECLARE_LAUNCH(256, false, true)
@@ -139,6 +141,7 @@ GB300_DECLARE_LAUNCH(256, true, true)
 GB300_DECLARE_SPLIT(64, false)
 GB300_DECLARE_SPLIT(128, false)
 GB300_DECLARE_SPLIT(256, false)
+GB300_DECLARE_SPLIT(64, true)
 GB300_DECLARE_SPLIT(128, true)
 GB300_DECLARE_SPLIT(256, true)
 GB300_DECLARE_VARLEN(64, false, false)
@@ -147,6 +150,8 @@ GB300_DECLARE_VARLEN(128, false, false)
 GB300_DECLARE_VARLEN(128, true, false)
 GB300_DECLARE_VARLEN(256, false, false)
 GB300_DECLARE_VARLEN(256, true, false)
+GB300_DECLARE_VARLEN(64, false, true)
+GB300_DECLARE_VARLEN(64, true, true)
 GB300_DECLARE_VARLEN(128, false, true)
 GB300_DECLARE_VARLEN(128, true, true)
 GB300_DECLARE_VARLEN(256, false, true)
